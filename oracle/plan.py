@@ -1,0 +1,153 @@
+"""Oracle of the BSA plan (logical mask -> physical tiles) -- TEST INFRASTRUCTURE ONLY.
+
+Source: "Decoupling Logical Masks from GPU Execution for Dynamic Block-Sparse
+Attention" (Tessera), abstract: a physical mapping layer retains, combines or
+subdivides logical attention blocks into physical tiles, and a task
+organisation layer groups and schedules tiles within GPU tasks.
+"CompactAttention: Accelerating Chunked Prefill with Block-Union KV Selection",
+summary: a Q-block union plus an intra-group union give a GQA-aware per-group
+KV block table.  The pages give no concrete rule; the plainest reading, used
+here and by the CUDA path (which implements it independently), is:
+
+Mapping (physical q-tile = 128 query rows, physical K/V slot = 128 key rows):
+  qu = min(bq,128) rows per q-unit, rq = 128/qu q-units per q-tile,
+  sq = bq/qu q-units per logical q-block (2 when bq = 256: subdivide);
+  ku = min(bk,128) rows per k-unit, rk = 128/ku k-units per slot,
+  sk = bk/ku k-units per logical k-block.
+  bq = 128 / bk = 128 retains; smaller blocks are combined rq (rk) to a tile
+  (slot); bq = 256 / bk = 256 are subdivided into two 128-row units.
+  NQT = Nq/128 q-tiles, NKU = Nk/ku k-units.
+  Unit mask U[b,h,x,y] = mask[b,h,x // sq, y // sk] != 0.
+
+Per plan row r = (b*H + h)*NQT + qt:
+  u[y]   = OR over the rq q-units x in the tile of U[b,h,x,y]  (Q-block union)
+  cnt    = |{y : u[y]}|,  slots = ceil(cnt / rk)
+  row_ptr = exclusive prefix sum of slots (length R+1)
+  slot_ku: the y with u[y], ascending, rk per slot, last slot padded with -1
+  slot_mask[s]: bit (i*rk + j) = U[b, h, qt*rq + i, slot_ku[s, j]] (0 for padding)
+GQA union (only when g = H/Hkv > 1), per union row (b*Hkv + hk)*NQT + qt:
+  uu[y] = OR over the g query heads of the group of u[y]  (intra-group union)
+  urow_ptr = exclusive prefix sum of |uu|; ukb = the y with uu[y], ascending
+Schedule: order = rows sorted by slots descending (longest row first), ties by
+  ascending row id (a stable counting sort).
+Totals: [total slots, selected logical blocks (mask != 0), union entries].
+
+Pins (tests/test_oracle_plan.py): a hand-worked example written out in the
+test; exhaustive enumeration of every mask on 3x3 logical grids for each
+mapping; token-level round trip (the set of token pairs the plan covers with
+sub-mask bits set equals the token-level expansion of the logical mask);
+closed-form counts of the chunked-prefill workload (65 blocks per logical row);
+permutation/monotonicity of the schedule.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+SUPPORTED_BLOCKS = (32, 64, 128, 256)
+TILE = 128
+
+
+@dataclass
+class Mapping:
+    bq: int
+    bk: int
+    qu: int
+    rq: int
+    sq: int
+    ku: int
+    rk: int
+    sk: int
+
+
+def mapping(bq: int, bk: int) -> Mapping:
+    """Retain / combine / subdivide rule for one (bq, bk) pair."""
+    if bq not in SUPPORTED_BLOCKS or bk not in SUPPORTED_BLOCKS:
+        raise ValueError(f"unsupported block sizes bq={bq} bk={bk}")
+    qu = min(bq, TILE)
+    ku = min(bk, TILE)
+    return Mapping(bq, bk, qu, TILE // qu, bq // qu, ku, TILE // ku, bk // ku)
+
+
+def unit_mask(mask: np.ndarray, mp: Mapping) -> np.ndarray:
+    """Boolean unit-level mask U [B,H,NQU,NKU]."""
+    sel = np.asarray(mask) != 0
+    return np.repeat(np.repeat(sel, mp.sq, axis=2), mp.sk, axis=3)
+
+
+def build_plan(mask, bq: int, bk: int, gqa_group: int = 1) -> dict:
+    """Return every plan array as numpy (int32 / uint32 / int64)."""
+    if hasattr(mask, "detach"):
+        mask = mask.detach().cpu().numpy()
+    mask = np.asarray(mask)
+    mp = mapping(bq, bk)
+    B, H, NQB, NKB = mask.shape
+    if H % gqa_group:
+        raise ValueError("H must be a multiple of gqa_group")
+    U = unit_mask(mask, mp)
+    NQU, NKU = U.shape[2], U.shape[3]
+    if NQU % mp.rq:
+        raise ValueError("Nq must be a multiple of 128")
+    NQT = NQU // mp.rq
+    R = B * H * NQT
+
+    # Q-block union over the q-units of each q-tile.
+    u = U.reshape(B, H, NQT, mp.rq, NKU).any(axis=3)          # [B,H,NQT,NKU]
+    cnt = u.sum(axis=3).reshape(R)
+    slots = (cnt + mp.rk - 1) // mp.rk
+    row_ptr = np.zeros(R + 1, dtype=np.int64)
+    row_ptr[1:] = np.cumsum(slots)
+    S = int(row_ptr[-1])
+    slot_ku = np.full((S, mp.rk), -1, dtype=np.int64)
+    slot_mask = np.zeros(S, dtype=np.uint64)
+    ur = u.reshape(R, NKU)
+    Ur = U.reshape(B, H, NQT, mp.rq, NKU).reshape(R, mp.rq, NKU)
+    for r in range(R):
+        ys = np.flatnonzero(ur[r])
+        n = int(slots[r])
+        if n == 0:
+            continue
+        padded = np.full(n * mp.rk, -1, dtype=np.int64)
+        padded[:ys.size] = ys
+        blk = padded.reshape(n, mp.rk)
+        slot_ku[row_ptr[r]:row_ptr[r] + n] = blk
+        bits = np.zeros(n, dtype=np.uint64)
+        for i in range(mp.rq):
+            for j in range(mp.rk):
+                y = blk[:, j]
+                on = np.zeros(n, dtype=bool)
+                valid = y >= 0
+                on[valid] = Ur[r, i, y[valid]]
+                bits |= on.astype(np.uint64) << np.uint64(i * mp.rk + j)
+        slot_mask[row_ptr[r]:row_ptr[r] + n] = bits
+
+    # Longest-row-first schedule, ties by ascending row id.
+    order = np.array(sorted(range(R), key=lambda r: (-int(slots[r]), r)), dtype=np.int64)
+
+    # GQA per-group union table.
+    if gqa_group > 1:
+        Hkv = H // gqa_group
+        uu = u.reshape(B, Hkv, gqa_group, NQT, NKU).any(axis=2).reshape(B * Hkv * NQT, NKU)
+        ucnt = uu.sum(axis=1)
+        urow_ptr = np.zeros(uu.shape[0] + 1, dtype=np.int64)
+        urow_ptr[1:] = np.cumsum(ucnt)
+        ukb = np.concatenate([np.flatnonzero(x) for x in uu]) if uu.shape[0] else np.zeros(0, np.int64)
+    else:
+        urow_ptr = np.zeros(1, dtype=np.int64)
+        ukb = np.zeros(0, dtype=np.int64)
+
+    totals = np.array([S, int((mask != 0).sum()), int(urow_ptr[-1])], dtype=np.int64)
+    return {
+        "mapping": mp,
+        "NQT": NQT,
+        "NKU": NKU,
+        "rows": R,
+        "row_ptr": row_ptr.astype(np.int32),
+        "slot_ku": slot_ku.reshape(-1).astype(np.int32),
+        "slot_mask": slot_mask.astype(np.uint32),
+        "urow_ptr": urow_ptr.astype(np.int32),
+        "ukb": ukb.astype(np.int32),
+        "order": order.astype(np.int32),
+        "totals": totals,
+    }

@@ -1,0 +1,157 @@
+"""Pins for the plan oracle (CPU only).
+
+The plan oracle is checked against hand-derived examples
+(tests/golden/plan_hand_examples.json), against a token-level reconstruction
+(the set of (query, key) token pairs the plan covers with a set sub-mask bit
+must equal the token-level expansion of the logical mask: Tessera abstract,
+"preserving specified attention interactions"), by exhaustive enumeration of
+every mask on small logical grids for every mapping, against Python set unions
+for the GQA table (CompactAttention summary), and against closed-form counts of
+the chunked-prefill workload.
+"""
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import plan as OP
+from block_sparse_attention_plan_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "plan_hand_examples.json")
+KEYS = ("row_ptr", "slot_ku", "slot_mask", "urow_ptr", "ukb", "order", "totals")
+
+
+def check_plan_invariants(mask: np.ndarray, bq: int, bk: int, g: int, p: dict):
+    """Structural checks written independently of the oracle's construction."""
+    B, H, NQB, NKB = mask.shape
+    Nq, Nk = NQB * bq, NKB * bk
+    qu, ku = min(bq, 128), min(bk, 128)
+    rq, rk = 128 // qu, 128 // ku
+    NQT = Nq // 128
+    R = B * H * NQT
+    rp, sk, sm = p["row_ptr"].astype(np.int64), p["slot_ku"].reshape(-1, rk), p["slot_mask"]
+    assert rp[0] == 0 and rp.size == R + 1 and np.all(np.diff(rp) >= 0)
+    assert p["totals"][0] == rp[-1] == sk.shape[0] == sm.size
+    assert p["totals"][1] == int((mask != 0).sum())
+    # token-level coverage
+    want = np.zeros((B, H, Nq, Nk), dtype=bool)
+    sel = mask != 0
+    for b, h, qb, kb in zip(*np.nonzero(sel)):
+        want[b, h, qb * bq:(qb + 1) * bq, kb * bk:(kb + 1) * bk] = True
+    got = np.zeros_like(want)
+    for r in range(R):
+        b, rem = divmod(r, H * NQT)
+        h, qt = divmod(rem, NQT)
+        ks = sk[rp[r]:rp[r + 1]].ravel()
+        valid = ks[ks >= 0]
+        # ascending, unique, padding only at the tail of the last slot
+        assert np.all(np.diff(valid) > 0)
+        assert np.all(ks[:valid.size] == valid)
+        assert rp[r + 1] - rp[r] == -(-valid.size // rk)  # ceil
+        for s in range(rp[r], rp[r + 1]):
+            bits = int(sm[s])
+            assert bits >> (rq * rk) == 0
+            for j in range(rk):
+                y = int(sk[s, j])
+                if y < 0:
+                    assert all(((bits >> (i * rk + j)) & 1) == 0 for i in range(rq))
+                    continue
+                assert 0 <= y < Nk // ku
+                col_on = False
+                for i in range(rq):
+                    if (bits >> (i * rk + j)) & 1:
+                        col_on = True
+                        q0 = qt * 128 + i * qu
+                        got[b, h, q0:q0 + qu, y * ku:(y + 1) * ku] = True
+                assert col_on, "a listed k-unit must be selected by some q-unit of the tile"
+    np.testing.assert_array_equal(got, want)
+    # schedule: permutation, slots non-increasing, ties by ascending row id
+    order = p["order"].astype(np.int64)
+    assert sorted(order.tolist()) == list(range(R))
+    sl = np.diff(rp)[order]
+    assert np.all(np.diff(sl) <= 0)
+    for a, c in zip(order[:-1], order[1:]):
+        if np.diff(rp)[a] == np.diff(rp)[c]:
+            assert a < c
+    # GQA union table against Python sets
+    if g > 1:
+        Hkv = H // g
+        urp, ukb = p["urow_ptr"].astype(np.int64), p["ukb"]
+        assert urp.size == B * Hkv * NQT + 1 and p["totals"][2] == urp[-1]
+        for b in range(B):
+            for hk in range(Hkv):
+                for qt in range(NQT):
+                    s = set()
+                    for h in range(hk * g, (hk + 1) * g):
+                        r = (b * H + h) * NQT + qt
+                        s |= set(int(y) for y in sk[rp[r]:rp[r + 1]].ravel() if y >= 0)
+                    ur = (b * Hkv + hk) * NQT + qt
+                    assert ukb[urp[ur]:urp[ur + 1]].tolist() == sorted(s)
+    else:
+        assert p["urow_ptr"].tolist() == [0] and p["ukb"].size == 0 and p["totals"][2] == 0
+
+
+def test_hand_worked_examples():
+    cases = json.load(open(GOLDEN))["cases"]
+    for c in cases:
+        mask = np.array(c["mask"], dtype=np.uint8)
+        p = OP.build_plan(mask, c["bq"], c["bk"], c["gqa_group"])
+        for k in KEYS:
+            assert p[k].tolist() == c[k], (c["name"], k, p[k].tolist(), c[k])
+        check_plan_invariants(mask, c["bq"], c["bk"], c["gqa_group"], p)
+
+
+GRIDS = {32: 4, 64: 2, 128: 3, 256: 3}  # NQB so that Nq is a multiple of 128
+
+
+@pytest.mark.parametrize("bq,bk", list(itertools.product((32, 64, 128, 256), repeat=2)))
+def test_exhaustive_small_grids(bq, bk):
+    nqb = GRIDS[bq]
+    nkb = max(1, 9 // nqb) if nqb != 4 else 2
+    n = nqb * nkb
+    for bits in range(1 << n):
+        m = np.array([(bits >> t) & 1 for t in range(n)], dtype=np.uint8).reshape(1, 1, nqb, nkb)
+        p = OP.build_plan(m, bq, bk, 1)
+        check_plan_invariants(m, bq, bk, 1, p)
+
+
+@pytest.mark.parametrize("bq,bk,g", [(64, 32, 2), (32, 64, 4), (128, 256, 2), (256, 64, 1)])
+def test_random_masks_nonbinary_bytes(bq, bk, g):
+    w = W.random_problem(11, 2, 4, 4 // g, 512, 768, 16, bq, bk, 0.3, values=True)
+    m = w.mask.numpy()
+    assert m.max() > 1
+    p = OP.build_plan(m, bq, bk, g)
+    check_plan_invariants(m, bq, bk, g, p)
+
+
+def test_chunked_prefill_closed_form_counts():
+    w = W.make_workload("chunked_prefill", data=False)
+    m = w.mask.numpy()
+    assert np.all((m != 0).sum(-1) == 65)            # sink + 16-block window + top-48
+    assert int((m != 0).sum()) == 32 * 64 * 65 == 133120
+    p = OP.build_plan(m, 64, 64, 4)
+    assert p["totals"][1] == 133120
+    rp = p["row_ptr"].astype(np.int64)
+    sk = p["slot_ku"].reshape(-1, 2)
+    # each q-tile covers q-blocks 2t, 2t+1: its unit count is the size of the
+    # union of their two 65-block sets
+    for h in (0, 17, 31):
+        for qt in (0, 13, 31):
+            r = h * 32 + qt
+            s = set(np.flatnonzero(m[0, h, 2 * qt])) | set(np.flatnonzero(m[0, h, 2 * qt + 1]))
+            ks = sk[rp[r]:rp[r + 1]].ravel()
+            assert sorted(s) == ks[ks >= 0].tolist()
+
+
+def test_mapping_rule():
+    assert (OP.mapping(128, 128).rq, OP.mapping(128, 128).rk) == (1, 1)
+    mp = OP.mapping(32, 64)
+    assert (mp.qu, mp.rq, mp.sq, mp.ku, mp.rk, mp.sk) == (32, 4, 1, 64, 2, 1)
+    mp = OP.mapping(256, 256)
+    assert (mp.qu, mp.rq, mp.sq, mp.ku, mp.rk, mp.sk) == (128, 1, 2, 128, 1, 2)
+    with pytest.raises(ValueError):
+        OP.mapping(48, 64)
+    with pytest.raises(ValueError):
+        OP.build_plan(np.ones((1, 1, 3, 2), np.uint8), 64, 64)  # Nq = 192
