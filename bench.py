@@ -1,0 +1,346 @@
+#!/usr/bin/env python
+"""Benchmark of block-sparse attention forward (plan + forward per step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl {gb300,reference}]
+
+One step = the whole hot path over one synthetic problem: bsa_plan (three
+kernels) then bsa_forward (one persistent kernel), inputs already resident in
+HBM.  Metric: effective TFLOP/s over active tiles = (selected logical blocks x
+4*bq*bk*d) / step time.  Default workload: the video-DiT configuration
+(B=1, H=24, N=16384, d=128, 128x128 blocks, 3D-local + 5% random mask).
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs an independent replica
+of the workload (the path needs no exchange); value = work of all ranks / the
+slowest rank's time ("scaling": "weak").
+
+--impl reference times the fp64 CPU oracle (the only reference implementation
+this method has) on the host cores, a bounded sample of the same workload per
+step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+
+def _cores() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+# The CPU oracle uses NumPy's BLAS: one thread per usable core.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(_cores()))
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "effective TFLOP/s over active tiles & % of GB300 BF16 tensor peak"
+UNIT = "TFLOP/s"
+L2_BYTES = 129e6
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples (wall-clock stamped) for one GPU."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str, period_ms: int = 20):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(period_ms), "-i", gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, smax = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            reasons = [n for n, v in zip(self.NAMES, parts[5:9]) if v.lower() == "active"]
+            self.samples.append((time.time(), sm, smax, reasons))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        src = "timed_region"
+        if not win and self.samples:
+            # region shorter than the sampling period: nearest samples around it
+            win = sorted(self.samples, key=lambda s: abs(s[0] - 0.5 * (t0 + t1)))[:3]
+            src = "nearest_to_timed_region"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({r for s in win for r in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in win), "sm_max_mhz": max(s[2] for s in win),
+                "reasons": reasons, "samples": len(win), "window": src}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_sample_rate(w, budget_s: float, seed: int = 0, start: int = 0):
+    """Time the fp64 oracle on (b, h, q-block) samples taken in a seeded
+    permutation order until ``budget_s`` seconds pass.  Returns
+    (TFLOP/s over active tiles, seconds, samples done, next start)."""
+    from oracle import attention as OA
+    B, H, NQB = w.mask.shape[:3]
+    cnt = (w.mask != 0).sum(-1).numpy()
+    perm = np.random.default_rng(seed).permutation(B * H * NQB)
+    flop_blk = 4.0 * w.bq * w.bk * w.d
+    t0 = time.perf_counter()
+    flop = 0.0
+    done = 0
+    i = start
+    while time.perf_counter() - t0 < budget_s and done < perm.size:
+        chunk = []
+        for _ in range(8):
+            f = int(perm[i % perm.size])
+            i += 1
+            b, rem = divmod(f, H * NQB)
+            h, qb = divmod(rem, NQB)
+            chunk.append((b, h, qb))
+        OA.sampled_qblocks(w.q, w.k, w.v, w.mask, w.bq, w.bk, chunk)
+        flop += sum(flop_blk * cnt[b, h, qb] for b, h, qb in chunk)
+        done += len(chunk)
+    dt = time.perf_counter() - t0
+    return flop / dt / 1e12, dt, done, i
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    from block_sparse_attention_plan_gb300 import workloads as W
+    w = W.make_workload(args.config)
+    per_step = max(0.5, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    start = 0
+    for _ in range(args.warmup):
+        _, _, _, start = oracle_sample_rate(w, per_step, start=start)
+    rates, secs, n = [], 0.0, 0
+    for _ in range(args.steps):
+        r, dt, done, start = oracle_sample_rate(w, per_step, start=start)
+        rates.append(r)
+        secs += dt
+        n += done
+    value = float(np.mean(rates))
+    B, H, NQB = w.mask.shape[:3]
+    sample = (f"{n} (b,h,q-block) rows of {B * H * NQB} in a seeded permutation, "
+              f"{per_step:.1f} s per step, fp64 NumPy oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(w):
+    inputs = (w.q.numel() + w.k.numel() + w.v.numel()) * 2 if w.q is not None else 0
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nk": w.Nk,
+            "d": w.d, "bq": w.bq, "bk": w.bk, "active_blocks": w.active_blocks,
+            "density": round(w.density, 4), "active_flop_per_step": w.active_flop,
+            "l2": (f"inputs {inputs / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB, no flush"
+                   if inputs > L2_BYTES else "L2 flushed between steps")}
+
+
+def run_gb300(args):
+    ws, rank, local = _dist()
+    import block_sparse_attention_plan_gb300 as bsa
+    from block_sparse_attention_plan_gb300 import workloads as W
+
+    w = W.make_workload(args.config)
+    peak, peak_sus, peak_src = _peaks()
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        # before any CUDA work: the oracle on the host cores, bounded sample
+        r, dt, n, _ = oracle_sample_rate(w, args.cpu_seconds)
+        B, H, NQB = w.mask.shape[:3]
+        cpu = {"value": r, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+               "sample": f"{n} of {B * H * NQB} (b,h,q-block) rows of the same workload, seeded "
+                         f"permutation, {dt:.1f} s, fp64 NumPy oracle"}
+
+    dist = ws > 1
+    if dist:
+        import torch.distributed as td
+        td.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    mask_d = w.mask.to(dev)
+    q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    L = bsa.plan_layout(*w.mask.shape, w.bq, w.bk, w.gqa_group)
+    wsbuf = torch.empty(int(L.workspace_bytes), dtype=torch.uint8, device=dev)
+    flop = w.active_flop
+
+    def step(ev=None):
+        p = bsa.plan(mask_d, w.bq, w.bk, w.gqa_group, workspace=wsbuf)
+        if ev is not None:
+            ev[0].record(stream)
+        bsa.forward(p, q, k, v, out=o, lse=lse)
+        if ev is not None:
+            ev[1].record(stream)
+        return p
+
+    def barrier():
+        if dist:
+            torch.distributed.barrier()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = str(local)
+    clocks = ClockSampler(uuid)
+
+    p = None
+    for _ in range(args.warmup):
+        p = step()
+    torch.cuda.synchronize()
+    if p is not None:
+        st, det = bsa.sync_status(p)
+        if st != 0:
+            raise RuntimeError(f"device status {st} detail {det:#x} during warm-up")
+
+    fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        p = step(fev[i])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier()
+    st, det = bsa.sync_status(p)
+    if st != 0:
+        raise RuntimeError(f"device status {st} detail {det:#x} in the timed region")
+    ms = e0.elapsed_time(e1) / args.steps
+    fwd_ms = float(np.mean([a.elapsed_time(b) for a, b in fev]))
+    if dist:
+        t = torch.tensor([ms, fwd_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, fwd_ms = float(t[0]), float(t[1])
+    clk = clocks.summary(t_wall0, t_wall1)
+
+    # end to end through the public API, host (pinned) buffers, copies timed
+    mask_h = w.mask.pin_memory()
+    q_h, k_h, v_h = w.q.pin_memory(), w.k.pin_memory(), w.v.pin_memory()
+    n_e2e = max(2, min(args.steps, args.e2e_steps))
+    bsa.attention(mask_h, q_h, k_h, v_h, w.bq, w.bk)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        oh, lh = bsa.attention(mask_h, q_h, k_h, v_h, w.bq, w.bk)
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+    clocks.stop()
+    h2d = mask_h.numel() + (q_h.numel() + k_h.numel() + v_h.numel()) * 2
+    d2h = oh.numel() * 2 + lh.numel() * 4
+
+    value = flop * ws / (ms * 1e-3) / 1e12
+    achieved = flop / (fwd_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(w),
+        "pct_of_peak": 100.0 * value / ws / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": args.traffic,
+                     "kernel": "bsa_fwd_kernel<128>" if w.d == 128 else "bsa_fwd_kernel<64>",
+                     "forward_ms": fwd_ms, "peak_source": f"{peak_src} bf16 burst",
+                     "frac_of_sustained": achieved / peak_sus},
+        "e2e": {"value": flop * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--config", default="video_dit")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per forward launch from an ncu capture of this kernel")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,244 @@
+"""ctypes binding of libbsa (include/bsa.h).  Argument marshalling only: every
+step of planning and attention runs in the library's CUDA kernels.  PyTorch
+supplies device memory and streams."""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbsa.so")
+
+BSA_OK = 0
+STATUS_NAMES = {
+    0: "BSA_OK", -1: "BSA_ERR_INVALID_ARG", -2: "BSA_ERR_UNSUPPORTED", -3: "BSA_ERR_ARCH",
+    -4: "BSA_ERR_CUDA", -5: "BSA_ERR_WORKSPACE", -6: "BSA_ERR_TIMEOUT", -7: "BSA_ERR_PLAN_MISMATCH",
+}
+PLAN_NO_UNION = 0x1
+
+
+class BsaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+class Layout(ctypes.Structure):
+    """Mirror of ``bsa_plan_layout``."""
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "B", "H", "Hkv", "NQB", "NKB", "bq", "bk", "gqa_group",
+        "qu", "rq", "sq", "ku", "rk", "sk",
+        "NQT", "NKU", "rows", "urows", "max_row_slots", "segments")] + [
+        ("slot_capacity", ctypes.c_int64), ("union_capacity", ctypes.c_int64)] + [
+        (n, ctypes.c_uint64) for n in (
+            "off_row_ptr", "off_slot_ku", "off_slot_mask", "off_urow_ptr", "off_ukb",
+            "off_order", "off_totals", "off_control", "off_scratch", "workspace_bytes")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """Load libbsa.so (built in-tree by ``block_sparse_attention_plan_gb300.build``).
+    Raises if it is missing: there is no fallback path."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built; run block_sparse_attention_plan_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, F, U8P, VP = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p
+    lib.bsa_version.restype = I
+    lib.bsa_version.argtypes = []
+    lib.bsa_status_string.restype = ctypes.c_char_p
+    lib.bsa_status_string.argtypes = [I]
+    lib.bsa_plan_layout_query.restype = I
+    lib.bsa_plan_layout_query.argtypes = [I, I, I, I, I, I, I, I, ctypes.POINTER(Layout)]
+    lib.bsa_plan_create.restype = I
+    lib.bsa_plan_create.argtypes = [U8P, I, I, I, I, I, I, I, VP, ctypes.c_size_t, I, VP,
+                                    ctypes.POINTER(P)]
+    lib.bsa_plan_get_layout.restype = I
+    lib.bsa_plan_get_layout.argtypes = [P, ctypes.POINTER(Layout)]
+    lib.bsa_plan_workspace.restype = VP
+    lib.bsa_plan_workspace.argtypes = [P]
+    lib.bsa_plan_destroy.restype = None
+    lib.bsa_plan_destroy.argtypes = [P]
+    lib.bsa_forward.restype = I
+    lib.bsa_forward.argtypes = [P, VP, VP, VP, VP, VP, I, F, VP]
+    lib.bsa_sync_status.restype = I
+    lib.bsa_sync_status.argtypes = [P, VP, ctypes.POINTER(ctypes.c_int32)]
+    lib.bsa_plan_check.restype = I
+    lib.bsa_plan_check.argtypes = [P, VP]
+    lib.bsa_watchdog_selftest.restype = I
+    lib.bsa_watchdog_selftest.argtypes = [VP, I, VP]
+    _lib = lib
+    return lib
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, what: str):
+    if status != BSA_OK:
+        raise BsaError(status, what)
+
+
+def plan_layout(B: int, H: int, NQB: int, NKB: int, bq: int, bk: int, gqa_group: int = 1,
+                flags: int = 0) -> Layout:
+    L = Layout()
+    _check(library().bsa_plan_layout_query(B, H, NQB, NKB, bq, bk, gqa_group, flags, ctypes.byref(L)),
+           "bsa_plan_layout_query")
+    return L
+
+
+class Plan:
+    """A plan built on the GPU.  Holds the caller-side workspace tensor (which
+    owns every plan array) and the library's host handle."""
+
+    def __init__(self, handle: ctypes.c_void_p, workspace: torch.Tensor, layout: Layout,
+                 mask: torch.Tensor):
+        self._handle = handle
+        self.workspace = workspace
+        self.layout = layout
+        self.mask = mask  # keeps the mask alive while the plan kernels may still read it
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if self._handle is None:
+            raise RuntimeError("plan destroyed")
+        return self._handle
+
+    def _view(self, off: int, count: int, dtype: torch.dtype) -> torch.Tensor:
+        nbytes = count * torch.empty(0, dtype=dtype).element_size()
+        return self.workspace[off:off + nbytes].view(dtype)
+
+    def arrays(self) -> dict:
+        """Device views of the plan arrays (sliced to their used lengths where
+        the totals are needed: that read synchronises)."""
+        L = self.layout
+        totals = self._view(L.off_totals, 4, torch.int64).cpu()
+        S = int(totals[0])
+        U = int(totals[2])
+        return {
+            "row_ptr": self._view(L.off_row_ptr, L.rows + 1, torch.int32),
+            "slot_ku": self._view(L.off_slot_ku, S * L.rk, torch.int32),
+            "slot_mask": self._view(L.off_slot_mask, S, torch.int32),
+            "urow_ptr": self._view(L.off_urow_ptr, L.urows + 1, torch.int32),
+            "ukb": self._view(L.off_ukb, U, torch.int32),
+            "order": self._view(L.off_order, L.rows, torch.int32),
+            "totals": totals,
+        }
+
+    def control(self) -> torch.Tensor:
+        return self._view(self.layout.off_control, 16, torch.int32)
+
+    def destroy(self):
+        if self._handle is not None:
+            library().bsa_plan_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def plan(mask: torch.Tensor, bq: int, bk: int, gqa_group: int = 1, flags: int = 0,
+         stream: Optional[torch.cuda.Stream] = None,
+         workspace: Optional[torch.Tensor] = None) -> Plan:
+    """Build the plan of a device u8 mask [B, H, Nq/bq, Nk/bk] (bsa_plan_create)."""
+    if mask.dtype != torch.uint8 or not mask.is_cuda or mask.dim() != 4:
+        raise ValueError("mask must be a CUDA uint8 tensor [B, H, NQB, NKB]")
+    mask = mask.contiguous()
+    B, H, NQB, NKB = mask.shape
+    L = plan_layout(B, H, NQB, NKB, bq, bk, gqa_group, flags)
+    if workspace is None:
+        workspace = torch.empty(int(L.workspace_bytes), dtype=torch.uint8, device=mask.device)
+    h = ctypes.c_void_p()
+    _check(library().bsa_plan_create(
+        ctypes.c_void_p(mask.data_ptr()), B, H, NQB, NKB, bq, bk, gqa_group,
+        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), flags, _stream_ptr(stream),
+        ctypes.byref(h)), "bsa_plan_create")
+    return Plan(h, workspace, L, mask)
+
+
+def forward(p: Plan, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+            scale: Optional[float] = None,
+            stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Block-sparse attention over plan ``p`` (bsa_forward).  Returns (O, LSE)."""
+    L = p.layout
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor [B, H, N, d]")
+    B, Hq, Nq, d = q.shape
+    if (B, Hq, Nq) != (L.B, L.H, L.NQB * L.bq):
+        raise ValueError("q shape does not match the plan")
+    if tuple(k.shape) != (L.B, L.Hkv, L.NKB * L.bk, d) or k.shape != v.shape:
+        raise ValueError("k/v shape does not match the plan")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device)
+    sc = 0.0 if scale is None else float(scale)
+    _check(library().bsa_forward(
+        p.handle, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+        ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+        ctypes.c_void_p(lse.data_ptr()), d, sc, _stream_ptr(stream)), "bsa_forward")
+    return out, lse
+
+
+def sync_status(p: Plan, stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, int]:
+    """(status, detail) the last forward on this plan left (synchronises)."""
+    det = ctypes.c_int32(0)
+    st = library().bsa_sync_status(p.handle, _stream_ptr(stream), ctypes.byref(det))
+    return st, det.value
+
+
+def plan_check(p: Plan, stream: Optional[torch.cuda.Stream] = None) -> int:
+    return library().bsa_plan_check(p.handle, _stream_ptr(stream))
+
+
+def watchdog_selftest(limit_us: int = 20000, device: Optional[torch.device] = None) -> int:
+    buf = torch.zeros(4, dtype=torch.int32, device=device or "cuda")
+    return library().bsa_watchdog_selftest(ctypes.c_void_p(buf.data_ptr()), limit_us,
+                                           _stream_ptr(None))
+
+
+def attention(mask: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bq: int,
+              bk: int, scale: Optional[float] = None, device: str = "cuda",
+              stream: Optional[torch.cuda.Stream] = None):
+    """One call from host or device tensors: copies inputs to the device (from
+    pinned memory, asynchronously), plans, runs, and copies O/LSE back when the
+    inputs were on the host.  Returns (O, LSE) on the inputs' device."""
+    host = not q.is_cuda
+    g = q.shape[1] // k.shape[1]
+    if host:
+        mask_d = mask.to(device, non_blocking=True)
+        q_d, k_d, v_d = (t.to(device, non_blocking=True) for t in (q, k, v))
+    else:
+        mask_d, q_d, k_d, v_d = mask, q, k, v
+    pl = plan(mask_d, bq, bk, g, stream=stream)
+    o, lse = forward(pl, q_d, k_d, v_d, scale=scale, stream=stream)
+    if host:
+        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        o_h.copy_(o, non_blocking=True)
+        l_h.copy_(lse, non_blocking=True)
+        (stream or torch.cuda.current_stream()).synchronize()
+        return o_h, l_h
+    return o, lse
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)

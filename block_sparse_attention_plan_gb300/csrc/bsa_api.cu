@@ -1,0 +1,372 @@
+// Host side of libbsa: argument validation, workspace layout, TMA tensor-map
+// encoding, launches and status reporting.  See include/bsa.h for the
+// contract of every entry point.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "bsa_internal.h"
+
+using namespace bsa;
+
+namespace {
+
+constexpr uint32_t kPlanMagic = 0xB5A9147Au;
+
+struct PlanImpl {
+  uint32_t magic;
+  bsa_plan_layout L;
+  uint8_t* ws;
+  PlanDev dev;
+  int device;
+};
+
+inline bool supported_block(int b) { return b == 32 || b == 64 || b == 128 || b == 256; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255); }
+
+bsa_status compute_layout(int B, int H, int NQB, int NKB, int bq, int bk, int g, int flags,
+                          bsa_plan_layout* L, int* nkeys_out, int* usegs_out) {
+  if (!L) return BSA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || NQB < 1 || NKB < 1 || g < 1) return BSA_ERR_INVALID_ARG;
+  if (!supported_block(bq) || !supported_block(bk)) return BSA_ERR_UNSUPPORTED;
+  if (H % g) return BSA_ERR_INVALID_ARG;
+  if (flags & ~BSA_PLAN_NO_UNION) return BSA_ERR_INVALID_ARG;
+  bsa_plan_layout l;
+  std::memset(&l, 0, sizeof(l));
+  l.B = B; l.H = H; l.Hkv = H / g; l.NQB = NQB; l.NKB = NKB; l.bq = bq; l.bk = bk; l.gqa_group = g;
+  l.qu = bq < kTile ? bq : kTile;
+  l.rq = kTile / l.qu;
+  l.sq = bq / l.qu;
+  l.ku = bk < kTile ? bk : kTile;
+  l.rk = kTile / l.ku;
+  l.sk = bk / l.ku;
+  const long long NQU = (long long)NQB * l.sq;
+  if (NQU % l.rq) return BSA_ERR_INVALID_ARG;  // Nq must be a multiple of 128
+  const long long NQT = NQU / l.rq;
+  const long long NKU = (long long)NKB * l.sk;
+  const long long rows = (long long)B * H * NQT;
+  const long long urows = (g > 1 && !(flags & BSA_PLAN_NO_UNION)) ? (long long)B * (H / g) * NQT : 0;
+  const long long max_slots = (NKU + l.rk - 1) / l.rk;
+  if (rows > (1ll << 30) || NKU > (1ll << 30)) return BSA_ERR_UNSUPPORTED;
+  if (max_slots + 1 > kMaxKeys) return BSA_ERR_UNSUPPORTED;
+  const long long slot_cap = rows * max_slots;
+  const long long union_cap = urows * NKU;
+  if (slot_cap * l.rk >= (1ll << 31) || union_cap >= (1ll << 31)) return BSA_ERR_UNSUPPORTED;
+  l.NQT = (int)NQT;
+  l.NKU = (int)NKU;
+  l.rows = (int)rows;
+  l.urows = (int)urows;
+  l.max_row_slots = (int)max_slots;
+  l.segments = (int)((rows + kPlanSegRows - 1) / kPlanSegRows);
+  l.slot_capacity = slot_cap;
+  l.union_capacity = union_cap;
+  const int nkeys = (int)max_slots + 1;
+  const int usegs = (int)((urows + kPlanSegRows - 1) / kPlanSegRows);
+  uint64_t off = 0;
+  l.off_row_ptr = off;   off = align256(off + 4ull * (rows + 1));
+  l.off_slot_ku = off;   off = align256(off + 4ull * slot_cap * l.rk);
+  l.off_slot_mask = off; off = align256(off + 4ull * slot_cap);
+  l.off_urow_ptr = off;  off = align256(off + 4ull * (urows + 1));
+  l.off_ukb = off;       off = align256(off + 4ull * union_cap);
+  l.off_order = off;     off = align256(off + 4ull * rows);
+  l.off_totals = off;    off = align256(off + 8ull * 4);
+  l.off_control = off;   off = align256(off + 4ull * 16);
+  l.off_scratch = off;
+  off = align256(off + 4ull * rows);                       // slots
+  off = align256(off + 4ull * rows);                       // lcnt
+  off = align256(off + 4ull * (urows + 1));                // ucnt
+  off = align256(off + 4ull * (uint64_t)l.segments * nkeys);  // hist / sort bases
+  l.workspace_bytes = off;
+  *L = l;
+  if (nkeys_out) *nkeys_out = nkeys;
+  if (usegs_out) *usegs_out = usegs;
+  return BSA_OK;
+}
+
+// Device capability check, cached per device.
+bsa_status check_arch(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+  static std::mutex mu;
+  static std::vector<int> cache;  // 0 unknown, 1 ok, 2 bad
+  std::lock_guard<std::mutex> lock(mu);
+  if ((int)cache.size() <= dev) cache.resize(dev + 1, 0);
+  if (cache[dev] == 0) {
+    int maj = 0, min = 0;
+    if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return BSA_ERR_CUDA;
+    cache[dev] = (maj == 10 && min == 3) ? 1 : 2;
+  }
+  if (dev_out) *dev_out = dev;
+  return cache[dev] == 1 ? BSA_OK : BSA_ERR_ARCH;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2D bf16 view [rows, d] with a box of {64, box_rows} and 128-byte swizzle.
+bool encode_map(CUtensorMap* m, const void* base, uint64_t rows, int d, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+long long env_ll(const char* name, long long dflt) {
+  const char* s = std::getenv(name);
+  if (!s || !*s) return dflt;
+  char* end = nullptr;
+  const long long v = std::strtoll(s, &end, 10);
+  return (end && *end == 0 && v > 0) ? v : dflt;
+}
+
+const PlanImpl* as_impl(const bsa_plan* p) {
+  const PlanImpl* q = reinterpret_cast<const PlanImpl*>(p);
+  return (q && q->magic == kPlanMagic) ? q : nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+int bsa_version(void) { return BSA_VERSION; }
+
+const char* bsa_status_string(int s) {
+  switch (s) {
+    case BSA_OK: return "BSA_OK";
+    case BSA_ERR_INVALID_ARG: return "BSA_ERR_INVALID_ARG";
+    case BSA_ERR_UNSUPPORTED: return "BSA_ERR_UNSUPPORTED";
+    case BSA_ERR_ARCH: return "BSA_ERR_ARCH";
+    case BSA_ERR_CUDA: return "BSA_ERR_CUDA";
+    case BSA_ERR_WORKSPACE: return "BSA_ERR_WORKSPACE";
+    case BSA_ERR_TIMEOUT: return "BSA_ERR_TIMEOUT";
+    case BSA_ERR_PLAN_MISMATCH: return "BSA_ERR_PLAN_MISMATCH";
+    default: return "BSA_ERR_UNKNOWN";
+  }
+}
+
+bsa_status bsa_plan_layout_query(int B, int H, int NQB, int NKB, int bq, int bk, int gqa_group,
+                                 int flags, bsa_plan_layout* out) {
+  return compute_layout(B, H, NQB, NKB, bq, bk, gqa_group, flags, out, nullptr, nullptr);
+}
+
+bsa_status bsa_plan_create(const uint8_t* mask, int B, int H, int NQB, int NKB, int bq, int bk,
+                           int gqa_group, void* workspace, size_t workspace_bytes, int flags,
+                           void* stream, bsa_plan** out) {
+  if (!out) return BSA_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!mask || !workspace) return BSA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return BSA_ERR_INVALID_ARG;
+  bsa_plan_layout L;
+  int nkeys = 0, usegs = 0;
+  bsa_status st = compute_layout(B, H, NQB, NKB, bq, bk, gqa_group, flags, &L, &nkeys, &usegs);
+  if (st != BSA_OK) return st;
+  if (workspace_bytes < L.workspace_bytes) return BSA_ERR_WORKSPACE;
+  int dev = 0;
+  st = check_arch(&dev);
+  if (st != BSA_OK) return st;
+
+  PlanImpl* impl = new (std::nothrow) PlanImpl;
+  if (!impl) return BSA_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  impl->magic = kPlanMagic;
+  impl->L = L;
+  impl->ws = ws;
+  impl->device = dev;
+  PlanDev& d = impl->dev;
+  d.mask = mask;
+  d.row_ptr = reinterpret_cast<int32_t*>(ws + L.off_row_ptr);
+  d.slot_ku = reinterpret_cast<int32_t*>(ws + L.off_slot_ku);
+  d.slot_mask = reinterpret_cast<uint32_t*>(ws + L.off_slot_mask);
+  d.urow_ptr = reinterpret_cast<int32_t*>(ws + L.off_urow_ptr);
+  d.ukb = reinterpret_cast<int32_t*>(ws + L.off_ukb);
+  d.order = reinterpret_cast<int32_t*>(ws + L.off_order);
+  d.totals = reinterpret_cast<long long*>(ws + L.off_totals);
+  d.control = reinterpret_cast<int32_t*>(ws + L.off_control);
+  uint64_t off = L.off_scratch;
+  d.slots = reinterpret_cast<int32_t*>(ws + off); off = align256(off + 4ull * L.rows);
+  d.lcnt = reinterpret_cast<int32_t*>(ws + off);  off = align256(off + 4ull * L.rows);
+  d.ucnt = reinterpret_cast<int32_t*>(ws + off);  off = align256(off + 4ull * (L.urows + 1));
+  d.hist = reinterpret_cast<int32_t*>(ws + off);
+  d.B = B; d.H = H; d.Hkv = L.Hkv; d.g = gqa_group; d.NQB = NQB; d.NKB = NKB;
+  d.qu = L.qu; d.rq = L.rq; d.sq = L.sq; d.ku = L.ku; d.rk = L.rk; d.sk = L.sk;
+  d.NQT = L.NQT; d.NKU = L.NKU; d.rows = L.rows; d.urows = L.urows;
+  d.nkeys = nkeys; d.segments = L.segments; d.usegments = usegs;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(d.control, 0, 64, s) != cudaSuccess || launch_plan(d, s) != cudaSuccess) {
+    delete impl;
+    return BSA_ERR_CUDA;
+  }
+  *out = reinterpret_cast<bsa_plan*>(impl);
+  return BSA_OK;
+}
+
+bsa_status bsa_plan_get_layout(const bsa_plan* plan, bsa_plan_layout* out) {
+  const PlanImpl* p = as_impl(plan);
+  if (!p || !out) return BSA_ERR_INVALID_ARG;
+  *out = p->L;
+  return BSA_OK;
+}
+
+void* bsa_plan_workspace(const bsa_plan* plan) {
+  const PlanImpl* p = as_impl(plan);
+  return p ? p->ws : nullptr;
+}
+
+void bsa_plan_destroy(bsa_plan* plan) {
+  PlanImpl* p = reinterpret_cast<PlanImpl*>(plan);
+  if (!p || p->magic != kPlanMagic) return;
+  p->magic = 0;
+  delete p;
+}
+
+bsa_status bsa_forward(const bsa_plan* plan, const void* Q, const void* K, const void* V, void* O,
+                       float* LSE, int d, float scale, void* stream) {
+  const PlanImpl* p = as_impl(plan);
+  if (!plan) return BSA_ERR_INVALID_ARG;
+  if (!p) return BSA_ERR_PLAN_MISMATCH;
+  if (!Q || !K || !V || !O || !LSE) return BSA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+    return BSA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return BSA_ERR_UNSUPPORTED;
+  if (!(scale == scale) || std::isinf(scale)) return BSA_ERR_INVALID_ARG;
+  int dev = 0;
+  bsa_status st = check_arch(&dev);
+  if (st != BSA_OK) return st;
+  if (dev != p->device) return BSA_ERR_PLAN_MISMATCH;
+  const bsa_plan_layout& L = p->L;
+  const long long Nq = (long long)L.NQB * L.bq, Nk = (long long)L.NKB * L.bk;
+  const long long qrows = (long long)L.B * L.H * Nq, kvrows = (long long)L.B * L.Hkv * Nk;
+  if (qrows >= (1ll << 31) || kvrows >= (1ll << 31)) return BSA_ERR_UNSUPPORTED;
+
+  FwdParams fp;
+  std::memset(&fp, 0, sizeof(fp));
+  if (!encode_map(&fp.tmQ, Q, (uint64_t)qrows, d, kTile) ||
+      !encode_map(&fp.tmK, K, (uint64_t)kvrows, d, L.ku) ||
+      !encode_map(&fp.tmV, V, (uint64_t)kvrows, d, L.ku))
+    return BSA_ERR_CUDA;
+  const PlanDev& pd = p->dev;
+  fp.row_ptr = pd.row_ptr;
+  fp.slot_ku = pd.slot_ku;
+  fp.slot_mask = pd.slot_mask;
+  fp.order = pd.order;
+  fp.control = pd.control;
+  fp.O = static_cast<uint16_t*>(O);
+  fp.LSE = LSE;
+  fp.slot_capacity = L.slot_capacity;
+  fp.watchdog_ns = env_ll("BSA_WATCHDOG_MS", 1000) * 1000000ll;
+  fp.H = L.H; fp.Hkv = L.Hkv; fp.g = L.gqa_group; fp.NQT = L.NQT; fp.NKU = L.NKU;
+  fp.Nq = (int)Nq; fp.Nk = (int)Nk; fp.rq = L.rq; fp.rk = L.rk; fp.qu = L.qu; fp.ku = L.ku;
+  fp.rows = L.rows;
+  const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)d);
+  fp.scale_log2 = (float)(sc * 1.4426950408889634);
+
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  long long grid = env_ll("BSA_GRID", sms);
+  if (grid > L.rows) grid = L.rows;
+  if (grid < 1) grid = 1;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(pd.control, 0, 64, s) != cudaSuccess) return BSA_ERR_CUDA;
+  if (launch_forward(fp, d, (int)grid, s) != cudaSuccess) return BSA_ERR_CUDA;
+  return BSA_OK;
+}
+
+bsa_status bsa_sync_status(const bsa_plan* plan, void* stream, int32_t* detail) {
+  const PlanImpl* p = as_impl(plan);
+  if (!p) return BSA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BSA_ERR_CUDA;
+  int32_t ctl[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(ctl, p->dev.control, sizeof(ctl), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  if (detail) *detail = ctl[kCtlDetail];
+  return static_cast<bsa_status>(ctl[kCtlStatus]);
+}
+
+bsa_status bsa_plan_check(const bsa_plan* plan, void* stream) {
+  const PlanImpl* p = as_impl(plan);
+  if (!p) return BSA_ERR_INVALID_ARG;
+  const bsa_plan_layout& L = p->L;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BSA_ERR_CUDA;
+  std::vector<int32_t> rp(L.rows + 1), order(L.rows);
+  if (cudaMemcpy(rp.data(), p->dev.row_ptr, 4ull * (L.rows + 1), cudaMemcpyDeviceToHost) !=
+          cudaSuccess ||
+      cudaMemcpy(order.data(), p->dev.order, 4ull * L.rows, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  if (rp[0] != 0) return BSA_ERR_PLAN_MISMATCH;
+  for (int r = 0; r < L.rows; ++r)
+    if (rp[r + 1] < rp[r] || rp[r + 1] - rp[r] > L.max_row_slots) return BSA_ERR_PLAN_MISMATCH;
+  const long long S = rp[L.rows];
+  if (S > L.slot_capacity) return BSA_ERR_PLAN_MISMATCH;
+  std::vector<int32_t> ku((size_t)S * L.rk);
+  if (S > 0 && cudaMemcpy(ku.data(), p->dev.slot_ku, 4ull * S * L.rk, cudaMemcpyDeviceToHost) !=
+                   cudaSuccess)
+    return BSA_ERR_CUDA;
+  for (int r = 0; r < L.rows; ++r) {
+    const long long a = (long long)rp[r] * L.rk, b = (long long)rp[r + 1] * L.rk;
+    int prev = -1;
+    bool padded = false;
+    for (long long i = a; i < b; ++i) {
+      const int y = ku[i];
+      if (y < 0) {
+        if (y != -1 || b - i > L.rk - 1) return BSA_ERR_PLAN_MISMATCH;  // only in the last slot
+        padded = true;
+        continue;
+      }
+      if (padded || y >= L.NKU || y <= prev) return BSA_ERR_PLAN_MISMATCH;
+      prev = y;
+    }
+    if (b > a && ku[a] < 0) return BSA_ERR_PLAN_MISMATCH;
+  }
+  std::vector<char> seen(L.rows, 0);
+  for (int i = 0; i < L.rows; ++i) {
+    const int r = order[i];
+    if (r < 0 || r >= L.rows || seen[r]) return BSA_ERR_PLAN_MISMATCH;
+    seen[r] = 1;
+  }
+  return BSA_OK;
+}
+
+bsa_status bsa_watchdog_selftest(int32_t* status, int limit_us, void* stream) {
+  if (!status || limit_us <= 0) return BSA_ERR_INVALID_ARG;
+  bsa_status st = check_arch(nullptr);
+  if (st != BSA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(status, 0, 16, s) != cudaSuccess) return BSA_ERR_CUDA;
+  if (launch_watchdog_selftest(status, (long long)limit_us * 1000ll, s) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BSA_ERR_CUDA;
+  int32_t h[4];
+  if (cudaMemcpy(h, status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return BSA_ERR_CUDA;
+  if (h[3] != 0) return BSA_OK;  // the wait completed: no timeout observed
+  return static_cast<bsa_status>(h[kCtlStatus]);
+}
+
+}  // extern "C"

@@ -1,0 +1,541 @@
+// Block-sparse attention forward for sm_103a: a persistent, warp-specialised
+// flash-style kernel that computes only the K/V tiles a plan lists.
+//
+// Source of the method: "Decoupling Logical Masks from GPU Execution for
+// Dynamic Block-Sparse Attention" (Tessera), abstract -- compute only the
+// blocks a logical mask selects, with tiles grouped per GPU task so that data
+// movement overlaps computation.  Online softmax over tiles (running max and
+// sum, rescaling the partial output) is the FlashAttention fusion the pages
+// refer to ("Sol-Attn" summary: inline sparsification inside the online
+// softmax).
+//
+// One CTA (384 threads) per SM, looping over plan rows (one 128-row q-tile of
+// one head each) in longest-row-first order:
+//   warp 0      TMA producer: Q tile (double-buffered), then the K and V
+//               tiles of the row's slots into a ring of shared-memory stages
+//               guarded by full/empty mbarriers.  A slot of 128 keys is
+//               gathered as rk boxes of ku rows (ku = 128 / rk).
+//   warp 1      MMA issuer (one thread): tcgen05.mma S = Q K^T (both operands
+//               in shared memory) and O += P V (P read from tensor memory).
+//   warp 2      owns the tensor-memory allocation (512 columns).
+//   warps 4-7   softmax warpgroup A: even slots of the row.
+//   warps 8-11  softmax warpgroup B: odd slots of the row.
+// Each warpgroup keeps its own running max/sum and its own O accumulator, so
+// the tensor pipe works on one group's tile while the other group runs its
+// softmax; the two partial results are merged in the epilogue.
+//
+// Tensor memory (512 fp32 columns x 128 lanes; lane = q-tile row):
+//   [0,128) S_A (P_A packed bf16 in [0,64))   [128,256) S_B / P_B
+//   [256,256+d) O_A                           [384,384+d) O_B
+//
+// Every wait is bounded (watchdog): on expiry the CTA records
+// BSA_ERR_TIMEOUT in the plan's status word, lets its in-flight copies and
+// MMAs land, frees tensor memory and exits.
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "bsa_device.cuh"
+#include "bsa_internal.h"
+
+namespace bsa {
+namespace {
+
+using namespace dev;
+
+constexpr int kThreads = 384;
+constexpr int kTmemCols = 512;
+// Register split: 384 threads x 168 at launch = 64,512 registers =
+// 128 x kRegsControl (warps 0-3) + 256 x kRegsSoftmax (warps 4-11).
+constexpr int kRegsControl = 56;
+constexpr int kRegsSoftmax = 224;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split");
+__device__ __forceinline__ uint32_t col_s(int w) { return (uint32_t)(w * 128); }
+__device__ __forceinline__ uint32_t col_o(int w) { return (uint32_t)(256 + w * 128); }
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only past 2^8 growth
+
+template <int D>
+struct Cfg {
+  static constexpr int kTileBytes = 128 * D * 2;   // 128 rows x d bf16
+  static constexpr int kChunks = D / 64;           // 64-column (128-byte) swizzle blocks
+  static constexpr int kChunkBytes = 128 * 128;    // one block of 128 rows
+  static constexpr int kStages = (D == 128) ? 5 : 12;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffRing = 2 * kTileBytes;
+  static constexpr int kOffBar = kOffRing + kStages * kTileBytes;
+  // barriers
+  static constexpr int kBarQFull = 0, kBarQEmpty = 2, kBarKvFull = 4;
+  static constexpr int kBarKvEmpty = kBarKvFull + kStages;
+  static constexpr int kBarSFull = kBarKvEmpty + kStages;
+  static constexpr int kBarPFull = kBarSFull + 2;
+  static constexpr int kBarODone = kBarPFull + 2;
+  static constexpr int kBarXchg = kBarODone + 2;
+  static constexpr int kBarDrain = kBarXchg + 2;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kOffML = kOffMisc + 16;             // float [4][128]: mA, mB, lA, lB
+  static constexpr int kSmemBytes = kOffML + 4 * 128 * 4;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct Item {
+  int n;       // slots of the row (0 = empty or rejected)
+  int s0;      // first slot index
+  int bh;      // b*H + h
+  int qt;      // q-tile
+  int kvrow0;  // first K/V row of the head's sequence in the [B*Hkv*Nk, d] view
+};
+
+__device__ __forceinline__ void record_status(int32_t* ctl, int code, int site) {
+  if (atomicCAS(ctl + kCtlStatus, 0, code) == 0)
+    atomicExch(ctl + kCtlDetail, (int)((blockIdx.x << 8) | (site & 0xff)));
+}
+
+// Decode one schedule entry, rejecting out-of-range plan data (the row is then
+// treated as empty and BSA_ERR_PLAN_MISMATCH is recorded).
+__device__ __forceinline__ Item load_item(const FwdParams& p, int it, bool report) {
+  Item m{0, 0, 0, 0, 0};
+  const int row = __ldg(p.order + it);
+  if (row < 0 || row >= p.rows) {
+    if (report) record_status(p.control, -7, kSitePlanRange);
+    return m;
+  }
+  const int s0 = __ldg(p.row_ptr + row), s1 = __ldg(p.row_ptr + row + 1);
+  m.bh = row / p.NQT;
+  m.qt = row % p.NQT;
+  if (s0 < 0 || s1 < s0 || (long long)s1 > p.slot_capacity) {
+    if (report) record_status(p.control, -7, kSitePlanRange + 1);
+    return m;
+  }
+  const int b = m.bh / p.H, h = m.bh % p.H;
+  m.n = s1 - s0;
+  m.s0 = s0;
+  m.kvrow0 = (b * p.Hkv + h / p.g) * p.Nk;
+  return m;
+}
+
+// Shared-memory views common to all roles.
+template <int D>
+struct Smem {
+  using C = Cfg<D>;
+  uint32_t base;
+  __device__ __forceinline__ uint32_t bar(int i) const { return base + C::kOffBar + 8u * (uint32_t)i; }
+  __device__ __forceinline__ uint32_t q(int qb) const { return base + C::kOffQ + qb * C::kTileBytes; }
+  __device__ __forceinline__ uint32_t stage(int s) const {
+    return base + C::kOffRing + (uint32_t)s * C::kTileBytes;
+  }
+};
+
+// Bounded wait used during teardown: ignores the abort flag, short limit.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const Watchdog& wd) {
+  volatile int no_abort = 0;
+  Watchdog quick{&no_abort, wd.status, wd.detail, 100000000ll};
+  mbar_wait(bar, parity, quick, kSiteDrain);
+}
+
+// ------------------------------------------------------------------ producer
+template <int D>
+__device__ __forceinline__ bool load_kv_tile(const FwdParams& p, const Smem<D>& sm,
+                                             const CUtensorMap* map, const Item& m, int j,
+                                             uint32_t& kv_it, uint64_t pol, const Watchdog& wd) {
+  using C = Cfg<D>;
+  const int stage = (int)(kv_it % C::kStages);
+  const uint32_t ph = (kv_it / C::kStages) & 1u;
+  if (!mbar_wait(sm.bar(C::kBarKvEmpty + stage), ph ^ 1u, wd, kSiteKvEmpty)) return false;
+  const uint32_t full = sm.bar(C::kBarKvFull + stage);
+  mbar_arrive_expect_tx(full, C::kTileBytes);
+  const int32_t* ent = p.slot_ku + (size_t)(m.s0 + j) * p.rk;
+  int first = __ldg(ent);
+  if (first < 0 || first >= p.NKU) {
+    record_status(p.control, -7, kSitePlanRange + 2);
+    first = 0;
+  }
+  const uint32_t dst0 = sm.stage(stage);
+  for (int u = 0; u < p.rk; ++u) {
+    int y = __ldg(ent + u);
+    if (y < 0) {
+      y = first;  // padding position: load real rows, the sub-mask hides them
+    } else if (y >= p.NKU) {
+      record_status(p.control, -7, kSitePlanRange + 3);
+      y = first;
+    }
+    const int row = m.kvrow0 + y * p.ku;
+#pragma unroll
+    for (int c = 0; c < C::kChunks; ++c)
+      tma_load_2d(dst0 + c * C::kChunkBytes + u * p.ku * 128, map, c * 64, row, full, pol);
+  }
+  ++kv_it;
+  return true;
+}
+
+template <int D>
+__device__ __noinline__ void producer_role(const FwdParams& p, const Smem<D>& sm,
+                                           const Watchdog& wd) {
+  using C = Cfg<D>;
+  tma_prefetch_desc(&p.tmQ);
+  tma_prefetch_desc(&p.tmK);
+  tma_prefetch_desc(&p.tmV);
+  const uint64_t pol_q = policy_evict_first();
+  const uint64_t pol_kv = policy_evict_last();
+  uint32_t q_it = 0, kv_it = 0;
+  bool ok = true;
+  for (int it = blockIdx.x; it < p.rows && ok; it += gridDim.x) {
+    const Item m = load_item(p, it, true);
+    if (m.n == 0) continue;
+    const int qb = (int)(q_it & 1u);
+    if (!mbar_wait(sm.bar(C::kBarQEmpty + qb), ((q_it >> 1) & 1u) ^ 1u, wd, kSiteQEmpty)) break;
+    mbar_arrive_expect_tx(sm.bar(C::kBarQFull + qb), C::kTileBytes);
+    const int qrow = m.bh * p.Nq + m.qt * 128;
+#pragma unroll
+    for (int c = 0; c < C::kChunks; ++c)
+      tma_load_2d(sm.q(qb) + c * C::kChunkBytes, &p.tmQ, c * 64, qrow, sm.bar(C::kBarQFull + qb),
+                  pol_q);
+    ++q_it;
+    // Ring order = MMA consumption order: K0, K1, then V_j, K_{j+2} for each j.
+    ok = load_kv_tile<D>(p, sm, &p.tmK, m, 0, kv_it, pol_kv, wd);
+    if (ok && m.n > 1) ok = load_kv_tile<D>(p, sm, &p.tmK, m, 1, kv_it, pol_kv, wd);
+    for (int j = 0; j < m.n && ok; ++j) {
+      ok = load_kv_tile<D>(p, sm, &p.tmV, m, j, kv_it, pol_kv, wd);
+      if (ok && j + 2 < m.n) ok = load_kv_tile<D>(p, sm, &p.tmK, m, j + 2, kv_it, pol_kv, wd);
+    }
+  }
+  if (*wd.abort_flag) {
+    // Let copies already issued land before the CTA's shared memory goes away.
+    const uint32_t nk = kv_it < (uint32_t)C::kStages ? kv_it : (uint32_t)C::kStages;
+    for (uint32_t t = kv_it - nk; t < kv_it; ++t)
+      drain_wait(sm.bar(C::kBarKvFull + (int)(t % C::kStages)), (t / C::kStages) & 1u, wd);
+    const uint32_t nq = q_it < 2u ? q_it : 2u;
+    for (uint32_t t = q_it - nq; t < q_it; ++t)
+      drain_wait(sm.bar(C::kBarQFull + (int)(t & 1u)), (t >> 1) & 1u, wd);
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+// S_w = Q K^T for the next K tile of the ring (both operands K-major, 128B
+// swizzle; 16 columns of d per instruction).
+template <int D>
+__device__ __forceinline__ bool issue_s(const Smem<D>& sm, uint32_t tmem, int qb, int w,
+                                        uint32_t& kv_it, const Watchdog& wd) {
+  using C = Cfg<D>;
+  constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
+  const int stage = (int)(kv_it % C::kStages);
+  if (!mbar_wait(sm.bar(C::kBarKvFull + stage), (kv_it / C::kStages) & 1u, wd, kSiteKvFull))
+    return false;
+  tc_fence_after();
+  const uint32_t qa = sm.q(qb), ka = sm.stage(stage);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
+    mma_ss(tmem + col_s(w), smem_desc_sw128(qa + off, 16, 1024),
+           smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+  }
+  mma_commit(sm.bar(C::kBarKvEmpty + stage));
+  mma_commit(sm.bar(C::kBarSFull + w));
+  ++kv_it;
+  return true;
+}
+
+template <int D>
+__device__ __noinline__ void mma_role(const FwdParams& p, const Smem<D>& sm, uint32_t tmem,
+                                      const Watchdog& wd) {
+  using C = Cfg<D>;
+  constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
+  uint32_t q_it = 0, kv_it = 0, pc0 = 0, pc1 = 0;
+  bool ok = true;
+  for (int it = blockIdx.x; it < p.rows && ok; it += gridDim.x) {
+    const Item m = load_item(p, it, false);
+    if (m.n == 0) continue;
+    const int qb = (int)(q_it & 1u);
+    if (!mbar_wait(sm.bar(C::kBarQFull + qb), (q_it >> 1) & 1u, wd, kSiteQFull)) break;
+    tc_fence_after();
+    ok = issue_s<D>(sm, tmem, qb, 0, kv_it, wd);
+    if (ok && m.n > 1) ok = issue_s<D>(sm, tmem, qb, 1, kv_it, wd);
+    if (ok && m.n <= 2) mma_commit(sm.bar(C::kBarQEmpty + qb));
+    for (int j = 0; j < m.n && ok; ++j) {
+      const int w = j & 1;
+      uint32_t& pc = w ? pc1 : pc0;
+      if (!mbar_wait(sm.bar(C::kBarPFull + w), pc & 1u, wd, kSitePFull)) {
+        ok = false;
+        break;
+      }
+      ++pc;
+      tc_fence_after();
+      const int stage = (int)(kv_it % C::kStages);
+      if (!mbar_wait(sm.bar(C::kBarKvFull + stage), (kv_it / C::kStages) & 1u, wd, kSiteKvFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t va = sm.stage(stage);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        // 16 keys per instruction: P columns [8kk, 8kk+8) (bf16 pairs) and V
+        // rows [16kk, 16kk+16) (MN-major: LBO = next 64 columns of d).
+        mma_ts(tmem + col_o(w), tmem + col_s(w) + 8 * kk,
+               smem_desc_sw128(va + kk * 2048, C::kChunkBytes, 1024), kIdescPV,
+               (j >= 2 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(sm.bar(C::kBarKvEmpty + stage));
+      ++kv_it;
+      if (j + 2 >= m.n) mma_commit(sm.bar(C::kBarODone + w));
+      if (j + 2 < m.n) {
+        ok = issue_s<D>(sm, tmem, qb, w, kv_it, wd);
+        if (ok && j + 2 == m.n - 1) mma_commit(sm.bar(C::kBarQEmpty + qb));
+      }
+    }
+    ++q_it;
+  }
+  // Drain: every MMA issued so far has completed once this arrives.
+  mma_commit(sm.bar(C::kBarDrain));
+  drain_wait(sm.bar(C::kBarDrain), 0, wd);
+}
+
+// ------------------------------------------------------------------ softmax
+template <int D>
+__device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, const Smem<D>& sm,
+                                             uint32_t tmem, const Watchdog& wd) {
+  using C = Cfg<D>;
+  float* ml = reinterpret_cast<float*>(smem + C::kOffML);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int w = (warp - 4) >> 2;          // 0 = group A (even slots), 1 = group B (odd slots)
+  const int quad = warp & 3;              // TMEM lane quadrant of this warp
+  const int rloc = quad * 32 + lane;      // row within the q-tile
+  const uint32_t tl = (uint32_t)(quad * 32) << 16;
+  const uint32_t s_addr = tmem + tl + col_s(w);
+  const int qi = rloc / p.qu;
+  const bool submask = (p.rq * p.rk) > 1;
+  const uint32_t my_bits_mask = (1u << p.rk) - 1u;
+  const float sl2 = p.scale_log2;
+  uint32_t sc = 0, oc = 0, xc = 0;
+  for (int it = blockIdx.x; it < p.rows && !*wd.abort_flag; it += gridDim.x) {
+    const Item m = load_item(p, it, false);
+    const int nw = (w == 0) ? (m.n + 1) >> 1 : m.n >> 1;
+    float m_ref = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int k = 0; k < nw; ++k) {
+      const int slot = m.s0 + 2 * k + w;
+      uint32_t bits = 0xffffffffu;
+      if (submask) bits = (__ldg(p.slot_mask + slot) >> (qi * p.rk)) & my_bits_mask;
+      if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarSFull + w), sc & 1u, wd, kSiteSFull))) {
+        ok = false;
+        break;
+      }
+      ++sc;
+      tc_fence_after();
+      uint32_t v[128];
+      tmem_ld32_at<0>(s_addr + 0, v);
+      tmem_ld32_at<32>(s_addr + 32, v);
+      tmem_ld32_at<64>(s_addr + 64, v);
+      tmem_ld32_at<96>(s_addr + 96, v);
+      tmem_wait_ld();
+      if (submask) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int unit = (c * 32) / p.ku;
+          if (!((bits >> unit) & 1u)) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[c * 32 + e] = __float_as_uint(-INFINITY);
+          }
+        }
+      }
+      float mx4[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) mx4[c] = __uint_as_float(v[c]);
+#pragma unroll
+      for (int e = 4; e < 128; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(v[e]));
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      const float m_new = fmaxf(m_ref, mx * sl2);
+      float factor = 1.f;
+      if (m_ref == -INFINITY) {
+        m_ref = m_new;  // nothing weighted accumulated yet: O holds zeros
+      } else if (m_new > m_ref + kRescaleThreshold) {
+        factor = ex2_approx(m_ref - m_new);
+        m_ref = m_new;
+      }
+      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
+      // p = 2^(s*scale*log2e - m_ref), packed as bf16 pairs into the first
+      // 64 columns of this group's S region (keys 2c, 2c+1 -> column c).
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(v[c * 32 + 2 * e]), sl2, -mb));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(v[c * 32 + 2 * e + 1]), sl2, -mb));
+          sum0 += p0;
+          sum1 += p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(s_addr + c * 16, pk);
+      }
+      const float sum = sum0 + sum1;
+      if (__any_sync(0xffffffffu, factor != 1.f)) {
+        const uint32_t o_addr = tmem + tl + col_o(w);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_addr + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+          tmem_st32(o_addr + c * 32, o);
+        }
+      }
+      tmem_wait_st();
+      l_run = l_run * factor + sum;
+      tc_fence_before();
+      mbar_arrive(sm.bar(C::kBarPFull + w));
+    }
+    if (!ok) break;
+    // ------------------------------------------------------------ epilogue
+    if (nw > 0) {
+      if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarODone + w), oc & 1u, wd, kSiteODone)))
+        break;
+      ++oc;
+    }
+    ml[w * 128 + rloc] = m_ref;
+    ml[(2 + w) * 128 + rloc] = l_run;
+    tc_fence_before();
+    mbar_arrive(sm.bar(C::kBarXchg + 0));
+    if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarXchg + 0), xc & 1u, wd, kSiteXchg))) break;
+    tc_fence_after();
+    const float mA = ml[rloc], mB = ml[128 + rloc];
+    const float lA = ml[256 + rloc], lB = ml[384 + rloc];
+    const int nA = (m.n + 1) >> 1, nB = m.n >> 1;
+    const float M = fmaxf(mA, mB);
+    const float fA = (lA > 0.f) ? ex2_approx(mA - M) : 0.f;
+    const float fB = (nB > 0 && lB > 0.f) ? ex2_approx(mB - M) : 0.f;
+    const float L = lA * fA + lB * fB;
+    const float inv = (L > 0.f) ? 1.f / L : 0.f;
+    const size_t orow = (size_t)m.bh * p.Nq + (size_t)m.qt * 128 + rloc;
+    uint4* optr = reinterpret_cast<uint4*>(p.O + orow * D);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+      const int col0 = w * (D / 2) + c * 32;
+      uint32_t a[32], bb[32];
+      if (nA > 0) tmem_ld32(tmem + tl + col_o(0) + col0, a);
+      if (nB > 0) tmem_ld32(tmem + tl + col_o(1) + col0, bb);
+      tmem_wait_ld();
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        float o0 = 0.f, o1 = 0.f;
+        if (nA > 0) {
+          o0 = __uint_as_float(a[2 * e]) * fA;
+          o1 = __uint_as_float(a[2 * e + 1]) * fA;
+        }
+        if (nB > 0) {
+          o0 = fmaf(__uint_as_float(bb[2 * e]), fB, o0);
+          o1 = fmaf(__uint_as_float(bb[2 * e + 1]), fB, o1);
+        }
+        pk[e] = pack_bf16x2(o0 * inv, o1 * inv);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        optr[col0 / 8 + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
+    if (w == 0) p.LSE[orow] = (L > 0.f) ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+    tc_fence_before();
+    mbar_arrive(sm.bar(C::kBarXchg + 1));
+    if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarXchg + 1), xc & 1u, wd, kSiteXchg))) break;
+    ++xc;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using C = Cfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const Smem<D> sm{smem_u32(smem)};
+  volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  const Watchdog wd{abort_flag, p.control + kCtlStatus, p.control + kCtlDetail, p.watchdog_ns};
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    if (sm.base & 1023u) record_failure(wd, -4, 0);  // layout assumption violated
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(sm.bar(C::kBarQFull + i), 1);
+      mbar_init(sm.bar(C::kBarQEmpty + i), 1);
+      mbar_init(sm.bar(C::kBarSFull + i), 1);
+      mbar_init(sm.bar(C::kBarPFull + i), 128);
+      mbar_init(sm.bar(C::kBarODone + i), 1);
+      mbar_init(sm.bar(C::kBarXchg + i), 256);
+    }
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(sm.bar(C::kBarKvFull + s), 1);
+      mbar_init(sm.bar(C::kBarKvEmpty + s), 1);
+    }
+    mbar_init(sm.bar(C::kBarDrain), 1);
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 2) {
+    tmem_alloc(sm.base + C::kOffMisc, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp >= 4) {
+    regs_inc<kRegsSoftmax>();
+    softmax_role<D>(p, smem, sm, tmem, wd);
+  } else {
+    regs_dec<kRegsControl>();
+    if (lane == 0 && !*abort_flag) {
+      if (warp == 0) producer_role<D>(p, sm, wd);
+      else if (warp == 1) mma_role<D>(p, sm, tmem, wd);
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+__global__ void watchdog_selftest_kernel(int32_t* status, long long limit_ns) {
+  __shared__ __align__(8) uint64_t b;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  const uint32_t bar = smem_u32(&b);
+  mbar_init(bar, 1);
+  fence_barrier_init();
+  Watchdog wd{&abort_flag, status + kCtlStatus, status + kCtlDetail, limit_ns};
+  // Nothing ever arrives on this barrier: the wait must give up by itself.
+  if (mbar_wait(bar, 0, wd, kSiteSelftest)) status[3] = 1;
+}
+
+template <int D>
+cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t stream) {
+  const int smem = Cfg<D>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(bsa_fwd_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  bsa_fwd_kernel<D><<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int forward_smem_bytes(int d) { return d == 64 ? Cfg<64>::kSmemBytes : Cfg<128>::kSmemBytes; }
+
+cudaError_t launch_forward(const FwdParams& p, int d, int grid, cudaStream_t stream) {
+  if (d == 64) return launch_d<64>(p, grid, stream);
+  return launch_d<128>(p, grid, stream);
+}
+
+cudaError_t launch_watchdog_selftest(int32_t* status, long long limit_ns, cudaStream_t stream) {
+  watchdog_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace bsa

@@ -1,0 +1,68 @@
+// Internal declarations shared by the host API and the kernels of libbsa.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "bsa.h"
+
+namespace bsa {
+
+constexpr int kTile = 128;            // physical q-tile rows and K/V slot rows
+constexpr int kPlanSegRows = 256;     // rows per segment of the schedule sort
+constexpr int kMaxKeys = 12288;       // bound on (slots per row + 1) for the sort
+constexpr int kCtlWorkCounter = 0;    // control word indices
+constexpr int kCtlStatus = 1;
+constexpr int kCtlDetail = 2;
+
+// Wait sites recorded in the status detail word (low 8 bits).
+enum WaitSite : int {
+  kSiteQEmpty = 1, kSiteQFull, kSiteKvEmpty, kSiteKvFull, kSiteSFull, kSitePFull,
+  kSiteODone, kSiteXchg, kSiteDrain, kSiteSelftest, kSitePlanRange = 0x40
+};
+
+// Device views of a plan's workspace.
+struct PlanDev {
+  const uint8_t* mask;
+  int32_t* row_ptr;
+  int32_t* slot_ku;
+  uint32_t* slot_mask;
+  int32_t* urow_ptr;
+  int32_t* ukb;
+  int32_t* order;
+  long long* totals;
+  int32_t* control;
+  int32_t* slots;   // scratch: slots per row
+  int32_t* lcnt;    // scratch: selected logical blocks owned by the row
+  int32_t* ucnt;    // scratch: union entries per union row
+  int32_t* hist;    // scratch: [segments][nkeys] histogram, then sort bases
+  int B, H, Hkv, g, NQB, NKB;
+  int qu, rq, sq, ku, rk, sk;
+  int NQT, NKU, rows, urows, nkeys, segments, usegments;
+};
+
+// Kernel parameters of the forward pass (passed as a __grid_constant__).
+struct FwdParams {
+  CUtensorMap tmQ;   // Q viewed as [B*Hq*Nq, d], box {64, 128}, 128B swizzle
+  CUtensorMap tmK;   // K viewed as [B*Hkv*Nk, d], box {64, ku}
+  CUtensorMap tmV;   // V likewise
+  const int32_t* row_ptr;
+  const int32_t* slot_ku;
+  const uint32_t* slot_mask;
+  const int32_t* order;
+  int32_t* control;
+  uint16_t* O;       // bf16 bits
+  float* LSE;
+  long long slot_capacity;
+  long long watchdog_ns;
+  int H, Hkv, g, NQT, NKU, Nq, Nk, rq, rk, qu, ku, rows;
+  float scale_log2;  // scale * log2(e)
+};
+
+cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream);
+cudaError_t launch_forward(const FwdParams& p, int d, int grid, cudaStream_t stream);
+int forward_smem_bytes(int d);
+cudaError_t launch_watchdog_selftest(int32_t* status, long long limit_ns, cudaStream_t stream);
+
+}  // namespace bsa

@@ -1,0 +1,188 @@
+/*
+ * bsa.h -- C ABI of libbsa: dynamic block-sparse attention (BSA) forward for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes ("Decoupling Logical Masks from GPU Execution for
+ * Dynamic Block-Sparse Attention" (Tessera), abstract): attention computed
+ * only over the (query-block, key-block) pairs that a logical block mask
+ * selects, with every selected interaction preserved.  For batch b, query head
+ * h (KV head h / g) and query row i, with J the keys whose block the mask
+ * selects for i's block:
+ *     O[i]   = sum_{j in J} exp(s_j - m) V[j] / sum_{j in J} exp(s_j - m),
+ *     s_j    = scale * <Q[i], K[j]>,  scale = 1/sqrt(d) unless overridden,
+ *     LSE[i] = m + ln(sum_{j in J} exp(s_j - m))  (natural log),
+ * and O[i] = 0, LSE[i] = -inf when J is empty.
+ *
+ * Two stages, both stream-ordered and free of host synchronisation:
+ *   bsa_plan_create  -- the physical mapping and task organisation layers of
+ *                       the Tessera abstract: logical blocks are retained,
+ *                       combined or subdivided into 128-row physical tiles,
+ *                       and each (batch, head, 128-row q-tile) gets a CSR list
+ *                       of the K/V tiles it needs, plus a longest-row-first
+ *                       schedule and (for GQA) a per-group union table
+ *                       ("CompactAttention", summary: Q-block union plus
+ *                       intra-group union).
+ *   bsa_forward      -- runs attention over exactly the tiles of a plan.
+ *
+ * Conventions
+ *   - Every pointer argument named "device" is a CUDA device pointer owned by
+ *     the caller; the library never allocates, frees or retains device
+ *     memory.  The only host allocation is the small bsa_plan handle.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls enqueue work on it and return without synchronising,
+ *     except bsa_sync_status and bsa_plan_check, which synchronise it.
+ *   - Layouts are row-major and contiguous: mask u8 [B][H][NQB][NKB];
+ *     Q and O bf16 [B][Hq][Nq][d]; K and V bf16 [B][Hkv][Nk][d];
+ *     LSE fp32 [B][Hq][Nq].  Nq = NQB*bq, Nk = NKB*bk, Hkv = Hq/gqa_group.
+ *   - Argument errors are detected on the host, before anything is enqueued,
+ *     and returned as a negative bsa_status.  Errors the kernels detect
+ *     (watchdog expiry, an out-of-range plan entry) are recorded in a status
+ *     word in the plan workspace and reported by bsa_sync_status.
+ */
+#ifndef BSA_H_
+#define BSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BSA_VERSION 1
+
+typedef enum bsa_status {
+  BSA_OK = 0,
+  BSA_ERR_INVALID_ARG = -1,   /* null/misaligned pointer, bad size or shape */
+  BSA_ERR_UNSUPPORTED = -2,   /* block size, head dim or size outside the supported set */
+  BSA_ERR_ARCH = -3,          /* current device is not compute capability 10.3 */
+  BSA_ERR_CUDA = -4,          /* a CUDA runtime/driver call failed */
+  BSA_ERR_WORKSPACE = -5,     /* workspace too small */
+  BSA_ERR_TIMEOUT = -6,       /* a kernel wait exceeded its limit (device watchdog) */
+  BSA_ERR_PLAN_MISMATCH = -7  /* plan inconsistent with itself or with the inputs */
+} bsa_status;
+
+/* Opaque host handle of a plan.  It holds sizes and a pointer into the
+ * caller's workspace; it stays valid until bsa_plan_destroy or until the
+ * workspace is freed, whichever comes first. */
+typedef struct bsa_plan bsa_plan;
+
+/* Plan geometry and the placement of every plan array inside the workspace
+ * (byte offsets from the workspace base, each 256-byte aligned).  Pure host
+ * arithmetic on sizes. */
+typedef struct bsa_plan_layout {
+  int32_t B, H, Hkv, NQB, NKB, bq, bk, gqa_group;
+  /* mapping: qu = rows per q-unit, rq = q-units per 128-row q-tile,
+   * sq = q-units per logical q-block; ku, rk, sk likewise for keys */
+  int32_t qu, rq, sq, ku, rk, sk;
+  int32_t NQT;          /* q-tiles per head  = Nq / 128 */
+  int32_t NKU;          /* k-units per head  = Nk / ku */
+  int32_t rows;         /* plan rows R = B*H*NQT */
+  int32_t urows;        /* union rows = B*Hkv*NQT when gqa_group > 1, else 0 */
+  int32_t max_row_slots;/* ceil(NKU / rk): most slots one row can need */
+  int32_t segments;     /* row segments used by the schedule sort */
+  int64_t slot_capacity;  /* rows * max_row_slots */
+  int64_t union_capacity; /* urows * NKU */
+  uint64_t off_row_ptr;   /* int32 [rows+1]   CSR row pointer into slots */
+  uint64_t off_slot_ku;   /* int32 [slot_capacity*rk] k-unit of each slot position, -1 = padding */
+  uint64_t off_slot_mask; /* uint32 [slot_capacity] bit i*rk+j: q-unit i attends slot position j */
+  uint64_t off_urow_ptr;  /* int32 [urows+1]  GQA union CSR row pointer */
+  uint64_t off_ukb;       /* int32 [union_capacity] union k-units, ascending */
+  uint64_t off_order;     /* int32 [rows]     longest-row-first schedule */
+  uint64_t off_totals;    /* int64 [4]: slots, selected logical blocks, union entries, 0 */
+  uint64_t off_control;   /* int32 [16]: [0] work counter, [1] status, [2] status detail */
+  uint64_t off_scratch;   /* plan-construction scratch */
+  uint64_t workspace_bytes; /* total bytes the caller must provide */
+} bsa_plan_layout;
+
+/* Plan flags */
+#define BSA_PLAN_NO_UNION 0x1   /* skip the GQA union table even when gqa_group > 1 */
+
+/*
+ * bsa_plan_layout_query -- sizes and workspace layout for a plan.
+ * Arguments: mask geometry B, H (query heads), NQB, NKB; logical block sizes
+ * bq, bk in {32, 64, 128, 256}; gqa_group g >= 1 dividing H; flags as for
+ * bsa_plan_create.  Requires Nq = NQB*bq to be a multiple of 128.
+ * Writes *out; returns BSA_ERR_INVALID_ARG / BSA_ERR_UNSUPPORTED otherwise.
+ * Touches no device.
+ */
+bsa_status bsa_plan_layout_query(int B, int H, int NQB, int NKB, int bq, int bk,
+                                 int gqa_group, int flags, bsa_plan_layout* out);
+
+/*
+ * bsa_plan_create -- build the plan of one logical mask on the GPU.
+ * mask: device, u8 [B][H][NQB][NKB]; any non-zero byte selects the block.
+ * workspace: device, >= layout.workspace_bytes bytes, 256-byte aligned, owned
+ * by the caller and reused by every bsa_forward on this plan (it also holds
+ * the work counter and status word those launches use, so two launches on
+ * one plan must not overlap in time).
+ * Enqueues three kernels on `stream` (no host sync): per-row counts,
+ * prefix sums, then compaction + schedule.  *out receives a new handle.
+ * Errors: BSA_ERR_INVALID_ARG (null/misaligned pointers, bad shapes),
+ * BSA_ERR_UNSUPPORTED, BSA_ERR_WORKSPACE, BSA_ERR_ARCH, BSA_ERR_CUDA.
+ */
+bsa_status bsa_plan_create(const uint8_t* mask, int B, int H, int NQB, int NKB, int bq,
+                           int bk, int gqa_group, void* workspace, size_t workspace_bytes,
+                           int flags, void* stream, bsa_plan** out);
+
+/* Copy the layout of an existing plan into *out. */
+bsa_status bsa_plan_get_layout(const bsa_plan* plan, bsa_plan_layout* out);
+
+/* Device base pointer of the plan's workspace (NULL for a NULL plan). */
+void* bsa_plan_workspace(const bsa_plan* plan);
+
+/* Free the host handle (not the workspace).  NULL is a no-op. */
+void bsa_plan_destroy(bsa_plan* plan);
+
+/*
+ * bsa_forward -- block-sparse attention forward over a plan.
+ * Q: device bf16 [B][Hq][Nq][d]; K, V: device bf16 [B][Hkv][Nk][d];
+ * O: device bf16 [B][Hq][Nq][d] (written); LSE: device fp32 [B][Hq][Nq]
+ * (written; natural log, -inf for rows with no selected key).  All 16-byte
+ * aligned; Q/K/V/O must not alias.  d in {64, 128}.  scale <= 0 selects
+ * 1/sqrt(d).  Nq, Nk, Hkv and the block sizes come from the plan.
+ * Enqueues one memset of the plan's control words and one persistent kernel
+ * on `stream`.  Errors: BSA_ERR_INVALID_ARG, BSA_ERR_UNSUPPORTED,
+ * BSA_ERR_PLAN_MISMATCH (NULL/foreign plan), BSA_ERR_ARCH, BSA_ERR_CUDA.
+ */
+bsa_status bsa_forward(const bsa_plan* plan, const void* Q, const void* K, const void* V,
+                       void* O, float* LSE, int d, float scale, void* stream);
+
+/*
+ * bsa_sync_status -- synchronise `stream`, then report the status word the
+ * last bsa_forward on this plan left: BSA_OK, BSA_ERR_TIMEOUT (a wait in the
+ * kernel ran past the watchdog limit; the kernel stopped cleanly) or
+ * BSA_ERR_PLAN_MISMATCH (an out-of-range plan entry was skipped).  *detail
+ * (may be NULL) receives (block << 8) | wait-site of the first failure.
+ */
+bsa_status bsa_sync_status(const bsa_plan* plan, void* stream, int32_t* detail);
+
+/*
+ * bsa_plan_check -- synchronise `stream`, copy the plan arrays to the host
+ * and verify them (row pointers monotone and within capacity, k-units in
+ * range and ascending, padding only at the end of a row, schedule a
+ * permutation).  Returns BSA_OK or BSA_ERR_PLAN_MISMATCH.  For tests and
+ * debugging; allocates host memory.
+ */
+bsa_status bsa_plan_check(const bsa_plan* plan, void* stream);
+
+/*
+ * bsa_watchdog_selftest -- launch a one-block kernel that waits on a barrier
+ * nothing ever completes, with a limit of `limit_us` microseconds, using the
+ * same bounded wait as the forward kernel; synchronise `stream` and return
+ * the status the kernel recorded (BSA_ERR_TIMEOUT when the watchdog works).
+ * `status` is device int32[4] scratch owned by the caller.
+ */
+bsa_status bsa_watchdog_selftest(int32_t* status, int limit_us, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* bsa_status_string(int status);
+
+/* BSA_VERSION of the compiled library. */
+int bsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSA_H_ */

@@ -25,3 +25,18 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def bsa_lib():
+    """Build libbsa.so in-tree if needed (nvcc cross-compiles without a GPU) and load it."""
+    from block_sparse_attention_plan_gb300 import build as B
+    B.build()
+    import block_sparse_attention_plan_gb300 as bsa
+    return bsa.library()
+
+
+@pytest.fixture(scope="session")
+def bsa(bsa_lib):
+    import block_sparse_attention_plan_gb300 as m
+    return m

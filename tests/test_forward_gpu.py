@@ -1,0 +1,106 @@
+"""GPU forward (tcgen05/TMA kernel, through the C ABI) vs the fp64 oracle on the
+same seeded bf16 inputs."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as OA
+from block_sparse_attention_plan_gb300 import workloads as W
+from compare import assert_attention_close
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(bsa, w, scale=None):
+    p = bsa.plan(w.mask.cuda(), w.bq, w.bk, w.gqa_group)
+    o, lse = bsa.forward(p, w.q.cuda(), w.k.cuda(), w.v.cuda(), scale=scale)
+    st, det = bsa.sync_status(p)
+    assert st == 0, (st, hex(det))
+    return o, lse
+
+
+@pytest.mark.parametrize("name", list(W.SMALL_CONFIGS))
+def test_forward_small_configs(bsa, name):
+    w = W.make_workload(name)
+    o, lse = run_gpu(bsa, w)
+    O, L = OA.block_gather(w.q, w.k, w.v, w.mask, w.bq, w.bk)
+    assert_attention_close(o, lse, O, L, name)
+
+
+@pytest.mark.parametrize("bq,bk,d,g", [
+    (128, 128, 128, 1), (128, 128, 64, 2), (64, 64, 128, 1), (64, 64, 64, 4), (32, 32, 64, 1),
+    (32, 128, 128, 2), (128, 32, 64, 1), (64, 32, 128, 1), (256, 128, 64, 1), (128, 256, 128, 2),
+    (256, 256, 64, 1), (32, 256, 128, 1),
+])
+def test_forward_mappings(bsa, bq, bk, d, g):
+    w = W.random_problem(31 + bq + bk + d, 1, 4, 4 // g, 1024, 1536, d, bq, bk, 0.3)
+    w.mask[0, 1, 0, :] = 0   # an empty logical q-block row
+    o, lse = run_gpu(bsa, w)
+    O, L = OA.block_gather(w.q, w.k, w.v, w.mask, bq, bk)
+    assert_attention_close(o, lse, O, L, f"bq={bq} bk={bk} d={d} g={g}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_forward_all_ones_and_all_zero(bsa, d):
+    w = W.random_problem(5, 1, 2, 2, 512, 768, d, 128, 128, 1.1)
+    o, lse = run_gpu(bsa, w)
+    O, L = OA.block_gather(w.q, w.k, w.v, w.mask, 128, 128)
+    assert_attention_close(o, lse, O, L, "all ones")
+    w.mask.zero_()
+    o, lse = run_gpu(bsa, w)
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_forward_scale_override_and_long_rows(bsa):
+    w = W.random_problem(9, 1, 2, 2, 256, 8192, 128, 128, 128, 0.9)
+    o, lse = run_gpu(bsa, w, scale=0.05)
+    O, L = OA.block_gather(w.q, w.k, w.v, w.mask, 128, 128, scale=0.05)
+    assert_attention_close(o, lse, O, L, "scale")
+
+
+def test_forward_large_logits_rescale(bsa):
+    # Scores growing along the key axis force the running max to move past the
+    # lazy-rescale threshold many times.
+    w = W.random_problem(12, 1, 2, 2, 256, 4096, 128, 128, 128, 1.1)
+    ramp = torch.linspace(0.2, 3.0, 4096).view(1, 1, 4096, 1)
+    w.k = (w.k.float() * ramp).to(torch.bfloat16)
+    w.q = (w.q.float() * 2.0).to(torch.bfloat16)
+    o, lse = run_gpu(bsa, w)
+    O, L = OA.block_gather(w.q, w.k, w.v, w.mask, 128, 128)
+    assert_attention_close(o, lse, O, L, "rescale")
+
+
+def test_forward_repeat_and_plan_reuse(bsa):
+    w = W.make_workload("video_dit_small")
+    p = bsa.plan(w.mask.cuda(), w.bq, w.bk, 1)
+    q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    o1, l1 = bsa.forward(p, q, k, v)
+    o2, l2 = bsa.forward(p, q, k, v)
+    assert bsa.sync_status(p)[0] == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["video_dit", "chunked_prefill", "regular"])
+def test_forward_full_configs(bsa, name):
+    w = W.make_workload(name)
+    o, lse = run_gpu(bsa, w)
+    O, L = OA.block_gather(w.q, w.k, w.v, w.mask, w.bq, w.bk)
+    e = assert_attention_close(o, lse, O, L, name)
+    print(name, e)
+
+
+@pytest.mark.slow
+def test_forward_long_video_sampled(bsa):
+    w = W.make_workload("long_video_dit")
+    o, lse = run_gpu(bsa, w)
+    H, NQB = w.Hq, w.mask.shape[2]
+    samples = [(0, h, qb) for h in range(H) for qb in range(h % 16, NQB, 16)] + [(0, 0, NQB - 1), (0, 39, NQB - 1)]
+    ref = OA.sampled_qblocks(w.q, w.k, w.v, w.mask, w.bq, w.bk, samples)
+    og = torch.cat([o[0, h, qb * 128:(qb + 1) * 128] for (_, h, qb) in samples]).cpu()
+    lg = torch.cat([lse[0, h, qb * 128:(qb + 1) * 128] for (_, h, qb) in samples]).cpu()
+    Oref = np.concatenate([ref[s][0] for s in samples])
+    Lref = np.concatenate([ref[s][1] for s in samples])
+    e = assert_attention_close(og, lg, Oref, Lref, "long_video_dit sampled")
+    print("long_video_dit", e)
+    assert torch.all(o[0, :, -128:] == 0) and torch.all(torch.isneginf(lse[0, :, -128:]))

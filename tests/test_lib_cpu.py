@@ -1,0 +1,102 @@
+"""The C-ABI library builds, loads and exports every symbol of include/bsa.h;
+host-side argument validation and layout arithmetic (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import plan as OP
+from block_sparse_attention_plan_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bsa.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(bsa_[a-z_]+)\s*\(",
+                                 src, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(bsa_lib):
+    names = declared_functions()
+    assert len(names) >= 10, names
+    for n in names:
+        assert hasattr(bsa_lib, n), f"libbsa.so does not export {n}"
+    assert bsa_lib.bsa_version() == 1
+
+
+def test_status_strings(bsa_lib):
+    assert bsa_lib.bsa_status_string(0) == b"BSA_OK"
+    assert bsa_lib.bsa_status_string(-6) == b"BSA_ERR_TIMEOUT"
+    assert bsa_lib.bsa_status_string(-99) == b"BSA_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("name", list(W.CONFIGS))
+def test_layout_matches_mapping_rule(bsa, name):
+    w = W.make_workload(name, data=False)
+    B, H, NQB, NKB = w.mask.shape
+    L = bsa.plan_layout(B, H, NQB, NKB, w.bq, w.bk, w.gqa_group)
+    mp = OP.mapping(w.bq, w.bk)
+    assert (L.qu, L.rq, L.sq, L.ku, L.rk, L.sk) == (mp.qu, mp.rq, mp.sq, mp.ku, mp.rk, mp.sk)
+    assert L.NQT == w.Nq // 128 and L.NKU == w.Nk // mp.ku
+    assert L.rows == B * H * L.NQT
+    assert L.urows == (B * w.Hkv * L.NQT if w.gqa_group > 1 else 0)
+    assert L.max_row_slots == -(-L.NKU // L.rk)
+    offs = [L.off_row_ptr, L.off_slot_ku, L.off_slot_mask, L.off_urow_ptr, L.off_ukb, L.off_order,
+            L.off_totals, L.off_control, L.off_scratch]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    assert L.off_slot_ku - L.off_slot_mask <= 0 and L.workspace_bytes > L.off_scratch
+    assert L.off_slot_mask - L.off_slot_ku >= 4 * L.slot_capacity * L.rk
+
+
+def test_layout_errors(bsa):
+    with pytest.raises(bsa.BsaError) as e:
+        bsa.plan_layout(1, 1, 3, 4, 64, 64)          # Nq = 192, not a multiple of 128
+    assert e.value.status == -1
+    with pytest.raises(bsa.BsaError) as e:
+        bsa.plan_layout(1, 2, 4, 4, 48, 64)          # unsupported block size
+    assert e.value.status == -2
+    with pytest.raises(bsa.BsaError) as e:
+        bsa.plan_layout(1, 3, 4, 4, 64, 64, gqa_group=2)  # H not a multiple of g
+    assert e.value.status == -1
+    with pytest.raises(bsa.BsaError) as e:
+        bsa.plan_layout(1, 1, 4, 200000, 128, 32)    # too many slots per row for the sort
+    assert e.value.status == -2
+
+
+def test_create_and_forward_argument_errors_without_device(bsa_lib, bsa):
+    L = bsa.plan_layout(1, 2, 4, 4, 128, 128)
+    out = ctypes.c_void_p()
+    buf = (ctypes.c_uint8 * 1024)()
+    base = ctypes.addressof(buf)
+    aligned = (base + 255) & ~255
+    # null mask
+    assert bsa_lib.bsa_plan_create(None, 1, 2, 4, 4, 128, 128, 1, ctypes.c_void_p(aligned),
+                                   L.workspace_bytes, 0, None, ctypes.byref(out)) == -1
+    # misaligned workspace
+    assert bsa_lib.bsa_plan_create(ctypes.c_void_p(aligned), 1, 2, 4, 4, 128, 128, 1,
+                                   ctypes.c_void_p(aligned + 16), L.workspace_bytes, 0, None,
+                                   ctypes.byref(out)) == -1
+    # workspace too small
+    assert bsa_lib.bsa_plan_create(ctypes.c_void_p(aligned), 1, 2, 4, 4, 128, 128, 1,
+                                   ctypes.c_void_p(aligned), L.workspace_bytes - 1, 0, None,
+                                   ctypes.byref(out)) == -5
+    # null out-parameter, bad flags
+    assert bsa_lib.bsa_plan_create(ctypes.c_void_p(aligned), 1, 2, 4, 4, 128, 128, 1,
+                                   ctypes.c_void_p(aligned), L.workspace_bytes, 0, None, None) == -1
+    assert bsa_lib.bsa_plan_create(ctypes.c_void_p(aligned), 1, 2, 4, 4, 128, 128, 1,
+                                   ctypes.c_void_p(aligned), L.workspace_bytes, 0x10, None,
+                                   ctypes.byref(out)) == -1
+    # forward: NULL plan, then a foreign object posing as a plan
+    p = ctypes.c_void_p(aligned)
+    assert bsa_lib.bsa_forward(None, p, p, p, p, p, 128, 0.0, None) == -1
+    fake = (ctypes.c_uint32 * 64)()
+    assert bsa_lib.bsa_forward(ctypes.c_void_p(ctypes.addressof(fake)), p, p, p, p, p, 128, 0.0,
+                               None) == -7
+    assert bsa_lib.bsa_sync_status(None, None, None) == -1
+    assert bsa_lib.bsa_plan_check(None, None) == -1
+    assert bsa_lib.bsa_watchdog_selftest(None, 1000, None) == -1
+    bsa_lib.bsa_plan_destroy(None)  # no-op
