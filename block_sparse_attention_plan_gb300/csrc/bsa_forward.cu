@@ -51,7 +51,12 @@ constexpr int kRegsSoftmax = 224;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split");
 __device__ __forceinline__ uint32_t col_s(int w) { return (uint32_t)(w * 128); }
 __device__ __forceinline__ uint32_t col_o(int w) { return (uint32_t)(256 + w * 128); }
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only past 2^8 growth
+constexpr float kRescaleThreshold = 8.0f;
+// Work items (positions in the longest-row-first order) are taken from a
+// global atomic counter by the producer and handed to the other roles through
+// a small ring in shared memory.
+constexpr int kSchedSlots = 4;
+constexpr int kSchedConsumers = 1 + 8;  // MMA thread + one lane per softmax warp  // log2 units: rescale O only past 2^8 growth
 
 template <int D>
 struct Cfg {
@@ -70,9 +75,12 @@ struct Cfg {
   static constexpr int kBarODone = kBarPFull + 2;
   static constexpr int kBarXchg = kBarODone + 2;
   static constexpr int kBarDrain = kBarXchg + 2;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarSchedFull = kBarDrain + 1;
+  static constexpr int kBarSchedEmpty = kBarSchedFull + kSchedSlots;
+  static constexpr int kNumBars = kBarSchedEmpty + kSchedSlots;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
-  static constexpr int kOffML = kOffMisc + 16;             // float [4][128]: mA, mB, lA, lB
+  static constexpr int kOffSched = kOffMisc + 16;          // int [kSchedSlots] work items
+  static constexpr int kOffML = kOffSched + 4 * kSchedSlots;  // float [4][128]: mA, mB, lA, lB
   static constexpr int kSmemBytes = kOffML + 4 * 128 * 4;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -125,6 +133,23 @@ struct Smem {
   }
 };
 
+// Consumer side of the work-item ring: wait for entry t, read it, release it.
+// Returns the item (position in the schedule), -1 at the end, or -2 when the
+// wait gave up.  `lane_arrives`: whether this thread releases the entry.
+template <int D>
+__device__ __forceinline__ int sched_take(const Smem<D>& sm, const uint8_t* smem, uint32_t t,
+                                          bool lane_arrives, bool warp_sync, const Watchdog& wd) {
+  using C = Cfg<D>;
+  const int slot = (int)(t % kSchedSlots);
+  bool ok = mbar_wait(sm.bar(C::kBarSchedFull + slot), (t / kSchedSlots) & 1u, wd, kSiteSched);
+  if (warp_sync) ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return -2;
+  const int item = reinterpret_cast<const volatile int*>(smem + C::kOffSched)[slot];
+  if (warp_sync) __syncwarp();
+  if (lane_arrives) mbar_arrive(sm.bar(C::kBarSchedEmpty + slot));
+  return item;
+}
+
 // Bounded wait used during teardown: ignores the abort flag, short limit.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const Watchdog& wd) {
   volatile int no_abort = 0;
@@ -168,7 +193,7 @@ __device__ __forceinline__ bool load_kv_tile(const FwdParams& p, const Smem<D>& 
 }
 
 template <int D>
-__device__ __noinline__ void producer_role(const FwdParams& p, const Smem<D>& sm,
+__device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, const Smem<D>& sm,
                                            const Watchdog& wd) {
   using C = Cfg<D>;
   tma_prefetch_desc(&p.tmQ);
@@ -178,7 +203,16 @@ __device__ __noinline__ void producer_role(const FwdParams& p, const Smem<D>& sm
   const uint64_t pol_kv = policy_evict_last();
   uint32_t q_it = 0, kv_it = 0;
   bool ok = true;
-  for (int it = blockIdx.x; it < p.rows && ok; it += gridDim.x) {
+  volatile int* sched = reinterpret_cast<volatile int*>(smem + C::kOffSched);
+  for (uint32_t t = 0; ok; ++t) {
+    const int slot = (int)(t % kSchedSlots);
+    if (!mbar_wait(sm.bar(C::kBarSchedEmpty + slot), ((t / kSchedSlots) & 1u) ^ 1u, wd, kSiteSched))
+      break;
+    int it = atomicAdd(p.control + kCtlWorkCounter, 1);
+    if (it >= p.rows) it = -1;
+    sched[slot] = it;
+    mbar_arrive(sm.bar(C::kBarSchedFull + slot));
+    if (it < 0) break;
     const Item m = load_item(p, it, true);
     if (m.n == 0) continue;
     const int qb = (int)(q_it & 1u);
@@ -235,13 +269,15 @@ __device__ __forceinline__ bool issue_s(const Smem<D>& sm, uint32_t tmem, int qb
 }
 
 template <int D>
-__device__ __noinline__ void mma_role(const FwdParams& p, const Smem<D>& sm, uint32_t tmem,
-                                      const Watchdog& wd) {
+__device__ __noinline__ void mma_role(const FwdParams& p, const uint8_t* smem, const Smem<D>& sm,
+                                      uint32_t tmem, const Watchdog& wd) {
   using C = Cfg<D>;
   constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
   uint32_t q_it = 0, kv_it = 0, pc0 = 0, pc1 = 0;
   bool ok = true;
-  for (int it = blockIdx.x; it < p.rows && ok; it += gridDim.x) {
+  for (uint32_t t = 0; ok; ++t) {
+    const int it = sched_take<D>(sm, smem, t, true, false, wd);
+    if (it < 0) break;
     const Item m = load_item(p, it, false);
     if (m.n == 0) continue;
     const int qb = (int)(q_it & 1u);
@@ -306,7 +342,9 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   const uint32_t my_bits_mask = (1u << p.rk) - 1u;
   const float sl2 = p.scale_log2;
   uint32_t sc = 0, oc = 0, xc = 0;
-  for (int it = blockIdx.x; it < p.rows && !*wd.abort_flag; it += gridDim.x) {
+  for (uint32_t t = 0;; ++t) {
+    const int it = sched_take<D>(sm, smem, t, lane == 0, true, wd);
+    if (it < 0) break;
     const Item m = load_item(p, it, false);
     const int nw = (w == 0) ? (m.n + 1) >> 1 : m.n >> 1;
     float m_ref = -INFINITY, l_run = 0.f;
@@ -469,6 +507,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
       mbar_init(sm.bar(C::kBarKvEmpty + s), 1);
     }
     mbar_init(sm.bar(C::kBarDrain), 1);
+    for (int i = 0; i < kSchedSlots; ++i) {
+      mbar_init(sm.bar(C::kBarSchedFull + i), 1);
+      mbar_init(sm.bar(C::kBarSchedEmpty + i), kSchedConsumers);
+    }
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -487,8 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
   } else {
     regs_dec<kRegsControl>();
     if (lane == 0 && !*abort_flag) {
-      if (warp == 0) producer_role<D>(p, sm, wd);
-      else if (warp == 1) mma_role<D>(p, sm, tmem, wd);
+      if (warp == 0) producer_role<D>(p, smem, sm, wd);
+      else if (warp == 1) mma_role<D>(p, smem, sm, tmem, wd);
     }
   }
 

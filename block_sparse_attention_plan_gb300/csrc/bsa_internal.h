@@ -19,7 +19,7 @@ constexpr int kCtlDetail = 2;
 // Wait sites recorded in the status detail word (low 8 bits).
 enum WaitSite : int {
   kSiteQEmpty = 1, kSiteQFull, kSiteKvEmpty, kSiteKvFull, kSiteSFull, kSitePFull,
-  kSiteODone, kSiteXchg, kSiteDrain, kSiteSelftest, kSitePlanRange = 0x40
+  kSiteODone, kSiteXchg, kSiteDrain, kSiteSelftest, kSiteSched, kSitePlanRange = 0x40
 };
 
 // Device views of a plan's workspace.

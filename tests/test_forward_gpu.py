@@ -6,7 +6,7 @@ import torch
 
 from oracle import attention as OA
 from block_sparse_attention_plan_gb300 import workloads as W
-from compare import assert_attention_close
+from compare import assert_attention_close, channel_scale
 
 pytestmark = pytest.mark.gpu
 
@@ -24,7 +24,7 @@ def test_forward_small_configs(bsa, name):
     w = W.make_workload(name)
     o, lse = run_gpu(bsa, w)
     O, L = OA.block_gather(w.q, w.k, w.v, w.mask, w.bq, w.bk)
-    assert_attention_close(o, lse, O, L, name)
+    assert_attention_close(o, lse, O, L, name, scale=channel_scale(w)[None, :, None, :])
 
 
 @pytest.mark.parametrize("bq,bk,d,g", [
@@ -86,7 +86,7 @@ def test_forward_full_configs(bsa, name):
     w = W.make_workload(name)
     o, lse = run_gpu(bsa, w)
     O, L = OA.block_gather(w.q, w.k, w.v, w.mask, w.bq, w.bk)
-    e = assert_attention_close(o, lse, O, L, name)
+    e = assert_attention_close(o, lse, O, L, name, scale=channel_scale(w)[None, :, None, :])
     print(name, e)
 
 
@@ -101,6 +101,8 @@ def test_forward_long_video_sampled(bsa):
     lg = torch.cat([lse[0, h, qb * 128:(qb + 1) * 128] for (_, h, qb) in samples]).cpu()
     Oref = np.concatenate([ref[s][0] for s in samples])
     Lref = np.concatenate([ref[s][1] for s in samples])
-    e = assert_attention_close(og, lg, Oref, Lref, "long_video_dit sampled")
+    cs = channel_scale(w)
+    sc = np.concatenate([np.broadcast_to(cs[h], (128, w.d)) for (_, h, _) in samples])
+    e = assert_attention_close(og, lg, Oref, Lref, "long_video_dit sampled", scale=sc)
     print("long_video_dit", e)
     assert torch.all(o[0, :, -128:] == 0) and torch.all(torch.isneginf(lse[0, :, -128:]))

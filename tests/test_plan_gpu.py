@@ -20,9 +20,12 @@ def gpu_plan_arrays(bsa, mask, bq, bk, g):
 
 
 def assert_plan_equal(a, ref):
+    assert int(a["totals"][3]) == 0  # reserved word
     for k in ("row_ptr", "slot_ku", "slot_mask", "urow_ptr", "ukb", "order", "totals"):
         got = np.asarray(a[k]).astype(np.int64)
         want = np.asarray(ref[k]).astype(np.int64)
+        if k == "totals":
+            got = got[:3]
         assert got.shape == want.shape, (k, got.shape, want.shape)
         if not np.array_equal(got, want):
             bad = np.flatnonzero(got != want)[:10]
