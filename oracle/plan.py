@@ -28,8 +28,12 @@ Per plan row r = (b*H + h)*NQT + qt:
 GQA union (only when g = H/Hkv > 1), per union row (b*Hkv + hk)*NQT + qt:
   uu[y] = OR over the g query heads of the group of u[y]  (intra-group union)
   urow_ptr = exclusive prefix sum of |uu|; ukb = the y with uu[y], ascending
-Schedule: order = rows sorted by slots descending (longest row first), ties by
-  ascending row id (a stable counting sort).
+Schedule (task organisation for data reuse): rows are grouped by KV head --
+  group id = (b*Hkv + hk), i.e. the g*NQT consecutive rows of the g query heads
+  sharing one K/V head -- so that the rows running at one time share the K/V
+  they gather.  Groups come in order of total slots descending (ties by group
+  id); inside a group rows come by slots descending (longest row first), ties
+  by ascending row id.
 Totals: [total slots, selected logical blocks (mask != 0), union entries].
 
 Pins (tests/test_oracle_plan.py): a hand-worked example written out in the
@@ -122,8 +126,15 @@ def build_plan(mask, bq: int, bk: int, gqa_group: int = 1) -> dict:
                 bits |= on.astype(np.uint64) << np.uint64(i * mp.rk + j)
         slot_mask[row_ptr[r]:row_ptr[r] + n] = bits
 
-    # Longest-row-first schedule, ties by ascending row id.
-    order = np.array(sorted(range(R), key=lambda r: (-int(slots[r]), r)), dtype=np.int64)
+    # Schedule: KV-head groups heaviest first; longest row first inside a group.
+    grows = gqa_group * NQT                       # rows per group (contiguous)
+    G = R // grows
+    work = [int(slots[gi * grows:(gi + 1) * grows].sum()) for gi in range(G)]
+    order = []
+    for gi in sorted(range(G), key=lambda x: (-work[x], x)):
+        rows_g = range(gi * grows, (gi + 1) * grows)
+        order.extend(sorted(rows_g, key=lambda r: (-int(slots[r]), r)))
+    order = np.array(order, dtype=np.int64)
 
     # GQA per-group union table.
     if gqa_group > 1:

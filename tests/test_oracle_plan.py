@@ -67,14 +67,25 @@ def check_plan_invariants(mask: np.ndarray, bq: int, bk: int, g: int, p: dict):
                         got[b, h, q0:q0 + qu, y * ku:(y + 1) * ku] = True
                 assert col_on, "a listed k-unit must be selected by some q-unit of the tile"
     np.testing.assert_array_equal(got, want)
-    # schedule: permutation, slots non-increasing, ties by ascending row id
+    # schedule: a permutation; KV-head groups contiguous, heaviest group first
+    # (ties by group id); inside a group slots non-increasing, ties by row id
     order = p["order"].astype(np.int64)
     assert sorted(order.tolist()) == list(range(R))
-    sl = np.diff(rp)[order]
-    assert np.all(np.diff(sl) <= 0)
-    for a, c in zip(order[:-1], order[1:]):
-        if np.diff(rp)[a] == np.diff(rp)[c]:
-            assert a < c
+    nsl = np.diff(rp)
+    Hkv = H // g
+    gid = lambda r: (r // (H * NQT)) * Hkv + ((r // NQT) % H) // g
+    gsz = g * NQT
+    groups = [gid(int(r)) for r in order]
+    seq = [groups[i] for i in range(0, R, gsz)]
+    for i in range(0, R, gsz):
+        assert len(set(groups[i:i + gsz])) == 1            # contiguous
+    work = {gg: int(sum(nsl[r] for r in range(R) if gid(r) == gg)) for gg in set(groups)}
+    for a, c in zip(seq[:-1], seq[1:]):
+        assert work[a] > work[c] or (work[a] == work[c] and a < c)
+    for i in range(0, R, gsz):
+        blk = order[i:i + gsz]
+        for a, c in zip(blk[:-1], blk[1:]):
+            assert nsl[a] > nsl[c] or (nsl[a] == nsl[c] and a < c)
     # GQA union table against Python sets
     if g > 1:
         Hkv = H // g
