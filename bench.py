@@ -224,6 +224,8 @@ def run_gb300(args):
     flop = w.active_flop
 
     def step(ev=None):
+        if ev is not None:
+            ev[2].record(stream)
         p = bsa.plan(mask_d, w.bq, w.bk, w.gqa_group, workspace=wsbuf)
         if ev is not None:
             ev[0].record(stream)
@@ -252,8 +254,7 @@ def run_gb300(args):
         if st != 0:
             raise RuntimeError(f"device status {st} detail {det:#x} during warm-up")
 
-    fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    fev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
@@ -269,7 +270,8 @@ def run_gb300(args):
     if st != 0:
         raise RuntimeError(f"device status {st} detail {det:#x} in the timed region")
     ms = e0.elapsed_time(e1) / args.steps
-    fwd_ms = float(np.mean([a.elapsed_time(b) for a, b in fev]))
+    fwd_ms = float(np.mean([a.elapsed_time(b) for a, b, _ in fev]))
+    plan_ms = float(np.mean([c.elapsed_time(a) for a, _, c in fev]))
     if dist:
         t = torch.tensor([ms, fwd_ms], device=dev, dtype=torch.float64)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -310,6 +312,7 @@ def run_gb300(args):
                      "frac_of_sustained": achieved / peak_sus},
         "e2e": {"value": flop * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+        "plan_ms": plan_ms,
         "gpu_launches": 4 * args.steps,
         "clocks": clk,
     }

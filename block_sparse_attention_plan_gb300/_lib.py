@@ -32,7 +32,7 @@ class Layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "B", "H", "Hkv", "NQB", "NKB", "bq", "bk", "gqa_group",
         "qu", "rq", "sq", "ku", "rk", "sk",
-        "NQT", "NKU", "rows", "urows", "max_row_slots", "segments")] + [
+        "NQT", "NKU", "rows", "urows", "max_row_slots", "groups")] + [
         ("slot_capacity", ctypes.c_int64), ("union_capacity", ctypes.c_int64)] + [
         (n, ctypes.c_uint64) for n in (
             "off_row_ptr", "off_slot_ku", "off_slot_mask", "off_urow_ptr", "off_ukb",

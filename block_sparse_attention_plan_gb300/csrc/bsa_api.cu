@@ -31,7 +31,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255); }
 
 bsa_status compute_layout(int B, int H, int NQB, int NKB, int bq, int bk, int g, int flags,
-                          bsa_plan_layout* L, int* nkeys_out, int* usegs_out) {
+                          bsa_plan_layout* L, int* nkeys_out) {
   if (!L) return BSA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || NQB < 1 || NKB < 1 || g < 1) return BSA_ERR_INVALID_ARG;
   if (!supported_block(bq) || !supported_block(bk)) return BSA_ERR_UNSUPPORTED;
@@ -55,6 +55,7 @@ bsa_status compute_layout(int B, int H, int NQB, int NKB, int bq, int bk, int g,
   const long long max_slots = (NKU + l.rk - 1) / l.rk;
   if (rows > (1ll << 30) || NKU > (1ll << 30)) return BSA_ERR_UNSUPPORTED;
   if (max_slots + 1 > kMaxKeys) return BSA_ERR_UNSUPPORTED;
+  if ((long long)B * (H / g) > kMaxGroups) return BSA_ERR_UNSUPPORTED;
   const long long slot_cap = rows * max_slots;
   const long long union_cap = urows * NKU;
   if (slot_cap * l.rk >= (1ll << 31) || union_cap >= (1ll << 31)) return BSA_ERR_UNSUPPORTED;
@@ -63,11 +64,10 @@ bsa_status compute_layout(int B, int H, int NQB, int NKB, int bq, int bk, int g,
   l.rows = (int)rows;
   l.urows = (int)urows;
   l.max_row_slots = (int)max_slots;
-  l.segments = (int)((rows + kPlanSegRows - 1) / kPlanSegRows);
+  l.groups = B * (H / g);
   l.slot_capacity = slot_cap;
   l.union_capacity = union_cap;
   const int nkeys = (int)max_slots + 1;
-  const int usegs = (int)((urows + kPlanSegRows - 1) / kPlanSegRows);
   uint64_t off = 0;
   l.off_row_ptr = off;   off = align256(off + 4ull * (rows + 1));
   l.off_slot_ku = off;   off = align256(off + 4ull * slot_cap * l.rk);
@@ -81,11 +81,10 @@ bsa_status compute_layout(int B, int H, int NQB, int NKB, int bq, int bk, int g,
   off = align256(off + 4ull * rows);                       // slots
   off = align256(off + 4ull * rows);                       // lcnt
   off = align256(off + 4ull * (urows + 1));                // ucnt
-  off = align256(off + 4ull * (uint64_t)l.segments * nkeys);  // hist / sort bases
+  off = align256(off + 4ull * (uint64_t)l.groups);         // gstart
   l.workspace_bytes = off;
   *L = l;
   if (nkeys_out) *nkeys_out = nkeys;
-  if (usegs_out) *usegs_out = usegs;
   return BSA_OK;
 }
 
@@ -170,7 +169,7 @@ const char* bsa_status_string(int s) {
 
 bsa_status bsa_plan_layout_query(int B, int H, int NQB, int NKB, int bq, int bk, int gqa_group,
                                  int flags, bsa_plan_layout* out) {
-  return compute_layout(B, H, NQB, NKB, bq, bk, gqa_group, flags, out, nullptr, nullptr);
+  return compute_layout(B, H, NQB, NKB, bq, bk, gqa_group, flags, out, nullptr);
 }
 
 bsa_status bsa_plan_create(const uint8_t* mask, int B, int H, int NQB, int NKB, int bq, int bk,
@@ -181,8 +180,8 @@ bsa_status bsa_plan_create(const uint8_t* mask, int B, int H, int NQB, int NKB, 
   if (!mask || !workspace) return BSA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return BSA_ERR_INVALID_ARG;
   bsa_plan_layout L;
-  int nkeys = 0, usegs = 0;
-  bsa_status st = compute_layout(B, H, NQB, NKB, bq, bk, gqa_group, flags, &L, &nkeys, &usegs);
+  int nkeys = 0;
+  bsa_status st = compute_layout(B, H, NQB, NKB, bq, bk, gqa_group, flags, &L, &nkeys);
   if (st != BSA_OK) return st;
   if (workspace_bytes < L.workspace_bytes) return BSA_ERR_WORKSPACE;
   int dev = 0;
@@ -210,11 +209,11 @@ bsa_status bsa_plan_create(const uint8_t* mask, int B, int H, int NQB, int NKB, 
   d.slots = reinterpret_cast<int32_t*>(ws + off); off = align256(off + 4ull * L.rows);
   d.lcnt = reinterpret_cast<int32_t*>(ws + off);  off = align256(off + 4ull * L.rows);
   d.ucnt = reinterpret_cast<int32_t*>(ws + off);  off = align256(off + 4ull * (L.urows + 1));
-  d.hist = reinterpret_cast<int32_t*>(ws + off);
+  d.gstart = reinterpret_cast<int32_t*>(ws + off);
   d.B = B; d.H = H; d.Hkv = L.Hkv; d.g = gqa_group; d.NQB = NQB; d.NKB = NKB;
   d.qu = L.qu; d.rq = L.rq; d.sq = L.sq; d.ku = L.ku; d.rk = L.rk; d.sk = L.sk;
   d.NQT = L.NQT; d.NKU = L.NKU; d.rows = L.rows; d.urows = L.urows;
-  d.nkeys = nkeys; d.segments = L.segments; d.usegments = usegs;
+  d.nkeys = nkeys; d.groups = L.groups;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(d.control, 0, 64, s) != cudaSuccess || launch_plan(d, s) != cudaSuccess) {

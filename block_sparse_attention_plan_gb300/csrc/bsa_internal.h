@@ -10,8 +10,8 @@
 namespace bsa {
 
 constexpr int kTile = 128;            // physical q-tile rows and K/V slot rows
-constexpr int kPlanSegRows = 256;     // rows per segment of the schedule sort
 constexpr int kMaxKeys = 12288;       // bound on (slots per row + 1) for the sort
+constexpr int kMaxGroups = 8192;      // bound on K/V-head groups (B * Hkv)
 constexpr int kCtlWorkCounter = 0;    // control word indices
 constexpr int kCtlStatus = 1;
 constexpr int kCtlDetail = 2;
@@ -36,10 +36,10 @@ struct PlanDev {
   int32_t* slots;   // scratch: slots per row
   int32_t* lcnt;    // scratch: selected logical blocks owned by the row
   int32_t* ucnt;    // scratch: union entries per union row
-  int32_t* hist;    // scratch: [segments][nkeys] histogram, then sort bases
+  int32_t* gstart;  // scratch: first schedule position of each K/V-head group
   int B, H, Hkv, g, NQB, NKB;
   int qu, rq, sq, ku, rk, sk;
-  int NQT, NKU, rows, urows, nkeys, segments, usegments;
+  int NQT, NKU, rows, urows, nkeys, groups;
 };
 
 // Kernel parameters of the forward pass (passed as a __grid_constant__).

@@ -3,20 +3,22 @@
 // Physical mapping ("Decoupling Logical Masks from GPU Execution for Dynamic
 // Block-Sparse Attention" (Tessera), abstract: logical blocks are retained,
 // combined or subdivided into physical tiles) and task organisation (tiles
-// grouped per 128-row q-tile and scheduled longest-row-first), plus the GQA
-// per-group union table ("CompactAttention", summary: Q-block union and
+// grouped per 128-row q-tile; rows scheduled so that rows sharing a K/V head
+// run together, heaviest group first, longest row first inside a group), plus
+// the GQA per-group union table ("CompactAttention", summary: Q-block union and
 // intra-group union).
 //
 // Three launches, no host synchronisation:
-//   count  one warp per plan row: per 32 k-units, each lane ORs the rq
-//          q-unit mask bytes of its k-unit; __ballot_sync + __popc give the
-//          row's unit count.  Per-segment histogram of slots-per-row.
-//   scan   one CTA: exclusive prefix sums (row pointers, union pointers, sort
-//          bases) and totals.
+//   count  one warp per plan row (and per union row): per 32 k-units, each
+//          lane ORs the rq q-unit mask bytes of its k-unit; __ballot_sync +
+//          __popc give the row's unit count.
+//   scan   one CTA: exclusive prefix sums (row pointers, union pointers),
+//          totals, and the rank of every K/V-head group by its total slots.
 //   fill   one warp per row: ballot + prefix-popcount compaction writes the
-//          ascending k-units into slots; sub-mask bits per slot; then a stable
-//          counting-sort scatter of the rows (slots descending, row id
-//          ascending).
+//          ascending k-units into slots, then the per-slot sub-masks; union
+//          rows likewise; and one CTA per K/V-head group places the group's
+//          rows in the schedule with a stable counting sort (slots
+//          descending, row id ascending).
 #include <cstdint>
 
 #include "bsa_internal.h"
@@ -67,58 +69,47 @@ __device__ __forceinline__ int union_unit(const PlanDev& p, int b, int hk, int q
 }
 
 __global__ void __launch_bounds__(kThreads) plan_count_kernel(const PlanDev p) {
-  extern __shared__ int hist_s[];  // [nkeys]
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int cta = blockIdx.x;
-  if (cta < p.segments) {
-    for (int k = threadIdx.x; k < p.nkeys; k += kThreads) hist_s[k] = 0;
-    __syncthreads();
-    for (int i = 0; i < 32; ++i) {
-      const int r = cta * kPlanSegRows + warp * 32 + i;
-      if (r >= p.rows) break;
-      const int bh = r / p.NQT, qt = r % p.NQT;
-      const uint8_t* mbh = p.mask + (size_t)bh * p.NQB * p.NKB;
-      int cnt = 0, own = 0;
-      for (int y0 = 0; y0 < p.NKU; y0 += 32) {
-        const int y = y0 + lane;
-        int u = 0, o = 0;
-        if (y < p.NKU) u = unit_union(mbh, p, qt, y, &o);
-        cnt += __popc(__ballot_sync(0xffffffffu, u));
-        own += o;
-      }
-      for (int s = 16; s > 0; s >>= 1) own += __shfl_xor_sync(0xffffffffu, own, s);
-      if (lane == 0) {
-        const int slots = (cnt + p.rk - 1) / p.rk;
-        p.slots[r] = slots;
-        p.lcnt[r] = own;
-        atomicAdd(&hist_s[slots], 1);
-      }
+  const int row_ctas = (p.rows + kWarps - 1) / kWarps;
+  if ((int)blockIdx.x < row_ctas) {
+    const int r = blockIdx.x * kWarps + warp;
+    if (r >= p.rows) return;
+    const int bh = r / p.NQT, qt = r % p.NQT;
+    const uint8_t* mbh = p.mask + (size_t)bh * p.NQB * p.NKB;
+    int cnt = 0, own = 0;
+    for (int y0 = 0; y0 < p.NKU; y0 += 32) {
+      const int y = y0 + lane;
+      int u = 0, o = 0;
+      if (y < p.NKU) u = unit_union(mbh, p, qt, y, &o);
+      cnt += __popc(__ballot_sync(0xffffffffu, u));
+      own += o;
     }
-    __syncthreads();
-    int* h = p.hist + (size_t)cta * p.nkeys;
-    for (int k = threadIdx.x; k < p.nkeys; k += kThreads) h[k] = hist_s[k];
+    for (int s = 16; s > 0; s >>= 1) own += __shfl_xor_sync(0xffffffffu, own, s);
+    if (lane == 0) {
+      p.slots[r] = (cnt + p.rk - 1) / p.rk;
+      p.lcnt[r] = own;
+    }
   } else {
-    const int useg = cta - p.segments;
-    for (int i = 0; i < 32; ++i) {
-      const int ur = useg * kPlanSegRows + warp * 32 + i;
-      if (ur >= p.urows) break;
-      const int bhk = ur / p.NQT, qt = ur % p.NQT;
-      const int b = bhk / p.Hkv, hk = bhk % p.Hkv;
-      int cnt = 0;
-      for (int y0 = 0; y0 < p.NKU; y0 += 32) {
-        const int y = y0 + lane;
-        const int u = (y < p.NKU) ? union_unit(p, b, hk, qt, y) : 0;
-        cnt += __popc(__ballot_sync(0xffffffffu, u));
-      }
-      if (lane == 0) p.ucnt[ur] = cnt;
+    const int ur = (blockIdx.x - row_ctas) * kWarps + warp;
+    if (ur >= p.urows) return;
+    const int bhk = ur / p.NQT, qt = ur % p.NQT;
+    const int b = bhk / p.Hkv, hk = bhk % p.Hkv;
+    int cnt = 0;
+    for (int y0 = 0; y0 < p.NKU; y0 += 32) {
+      const int y = y0 + lane;
+      const int u = (y < p.NKU) ? union_unit(p, b, hk, qt, y) : 0;
+      cnt += __popc(__ballot_sync(0xffffffffu, u));
     }
+    if (lane == 0) p.ucnt[ur] = cnt;
   }
 }
 
-// Block-wide exclusive scan of one 1024-element chunk; returns the chunk sum.
+// Block-wide exclusive scan of one value per thread (blockDim.x = 32 * nwarps);
+// returns the block total.  Every thread must call it.
 template <typename T>
 __device__ T block_exclusive_scan(T v, T* excl_out, T* warp_sums) {
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  const int nwarps = blockDim.x / 32;
   T x = v;
   for (int s = 1; s < 32; s <<= 1) {
     const T y = __shfl_up_sync(0xffffffffu, x, s);
@@ -127,132 +118,154 @@ __device__ T block_exclusive_scan(T v, T* excl_out, T* warp_sums) {
   if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    T w = warp_sums[lane];
+    T w = lane < nwarps ? warp_sums[lane] : T(0);
     for (int s = 1; s < 32; s <<= 1) {
       const T y = __shfl_up_sync(0xffffffffu, w, s);
       if (lane >= s) w += y;
     }
-    warp_sums[lane] = w;  // inclusive
+    if (lane < nwarps) warp_sums[lane] = w;  // inclusive
   }
   __syncthreads();
   const T before = (warp > 0) ? warp_sums[warp - 1] : T(0);
   *excl_out = before + x - v;
-  const T total = warp_sums[31];
+  const T total = warp_sums[nwarps - 1];
   __syncthreads();
   return total;
 }
 
+// Exclusive prefix sum of in[0..n) into out[0..n] (out[n] = total) by one
+// block: each thread sums a contiguous run, the runs are scanned once, then
+// each thread writes its run's prefixes.
+template <typename TIn>
+__device__ long long block_scan_array(const TIn* in, int32_t* out, int n, long long* wsum) {
+  const int per = (n + blockDim.x - 1) / blockDim.x;
+  const int i0 = threadIdx.x * per;
+  const int i1 = min(i0 + per, n);
+  long long local = 0;
+  for (int i = i0; i < i1; ++i) local += (long long)in[i];
+  long long ex;
+  const long long total = block_exclusive_scan<long long>(local, &ex, wsum);
+  if (out) {
+    long long run = ex;
+    for (int i = i0; i < i1; ++i) {
+      out[i] = (int32_t)run;
+      run += (long long)in[i];
+    }
+    if (threadIdx.x == 0) out[n] = (int32_t)total;
+  }
+  return total;
+}
+
 __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(const PlanDev p) {
-  __shared__ long long wsum64[32];
-  __shared__ int wsum[32];
-  // row pointers
-  int carry = 0;
-  for (int base = 0; base < p.rows; base += kScanThreads) {
-    const int i = base + threadIdx.x;
-    const int v = (i < p.rows) ? p.slots[i] : 0;
-    int ex;
-    const int tot = block_exclusive_scan<int>(v, &ex, wsum);
-    if (i < p.rows) p.row_ptr[i] = carry + ex;
-    carry += tot;
-  }
+  __shared__ long long wsum[32];
+  extern __shared__ int work_s[];  // [groups] total slots per K/V-head group
+  const long long S = block_scan_array<int32_t>(p.slots, p.row_ptr, p.rows, wsum);
+  const long long A = block_scan_array<int32_t>(p.lcnt, nullptr, p.rows, wsum);
+  const long long U = block_scan_array<int32_t>(p.ucnt, p.urow_ptr, p.urows, wsum);
   if (threadIdx.x == 0) {
-    p.row_ptr[p.rows] = carry;
-    p.totals[0] = carry;
-  }
-  // selected logical blocks
-  long long acc = 0;
-  for (int base = 0; base < p.rows; base += kScanThreads) {
-    const int i = base + threadIdx.x;
-    long long ex;
-    acc += block_exclusive_scan<long long>((i < p.rows) ? (long long)p.lcnt[i] : 0ll, &ex, wsum64);
-  }
-  if (threadIdx.x == 0) {
-    p.totals[1] = acc;
+    p.totals[0] = S;
+    p.totals[1] = A;
+    p.totals[2] = U;
     p.totals[3] = 0;
   }
-  // union pointers
-  carry = 0;
-  for (int base = 0; base < p.urows; base += kScanThreads) {
-    const int i = base + threadIdx.x;
-    const int v = (i < p.urows) ? p.ucnt[i] : 0;
-    int ex;
-    const int tot = block_exclusive_scan<int>(v, &ex, wsum);
-    if (i < p.urows) p.urow_ptr[i] = carry + ex;
-    carry += tot;
-  }
-  if (threadIdx.x == 0) {
-    p.urow_ptr[p.urows] = carry;
-    p.totals[2] = carry;
-  }
-  // sort bases: rows with more slots first; within one slot count, earlier
-  // segments first.  Flattened index f = (nkeys-1-key)*segments + seg.
-  const int nf = p.nkeys * p.segments;
-  carry = 0;
-  for (int base = 0; base < nf; base += kScanThreads) {
-    const int f = base + threadIdx.x;
-    int idx = 0, v = 0;
-    if (f < nf) {
-      const int key = p.nkeys - 1 - f / p.segments;
-      const int seg = f % p.segments;
-      idx = seg * p.nkeys + key;
-      v = p.hist[idx];
+  __syncthreads();  // row_ptr visible to the whole block
+  const int gsz = p.g * p.NQT;
+  for (int gi = threadIdx.x; gi < p.groups; gi += blockDim.x)
+    work_s[gi] = p.row_ptr[(gi + 1) * gsz] - p.row_ptr[gi * gsz];
+  __syncthreads();
+  // Groups heaviest first, ties by group id: rank = number of groups before.
+  for (int gi = threadIdx.x; gi < p.groups; gi += blockDim.x) {
+    const int w = work_s[gi];
+    int rank = 0;
+    for (int gj = 0; gj < p.groups; ++gj) {
+      const int x = work_s[gj];
+      rank += (x > w) || (x == w && gj < gi);
     }
-    int ex;
-    const int tot = block_exclusive_scan<int>(v, &ex, wsum);
-    if (f < nf) p.hist[idx] = carry + ex;
-    carry += tot;
+    p.gstart[gi] = rank * gsz;
   }
 }
 
-__global__ void __launch_bounds__(kThreads) plan_fill_kernel(const PlanDev p) {
-  extern __shared__ int start_s[];  // [nkeys]
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int cta = blockIdx.x;
-  if (cta < p.segments) {
-    for (int i = 0; i < 32; ++i) {
-      const int r = cta * kPlanSegRows + warp * 32 + i;
-      if (r >= p.rows) break;
-      const int bh = r / p.NQT, qt = r % p.NQT;
-      const uint8_t* mbh = p.mask + (size_t)bh * p.NQB * p.NKB;
-      const int s0 = p.row_ptr[r];
-      const int n = p.row_ptr[r + 1] - s0;
-      const int cap = n * p.rk;
-      int32_t* out = p.slot_ku + (size_t)s0 * p.rk;
-      int pos = 0;
-      for (int y0 = 0; y0 < p.NKU; y0 += 32) {
-        const int y = y0 + lane;
-        int o;
-        const int u = (y < p.NKU) ? unit_union(mbh, p, qt, y, &o) : 0;
-        const uint32_t bal = __ballot_sync(0xffffffffu, u);
-        if (u) {
-          const int idx = pos + __popc(bal & lanemask_lt());
-          if (idx < cap) out[idx] = y;
-        }
-        pos += __popc(bal);
-      }
-      for (int idx = pos + lane; idx < cap; idx += 32) out[idx] = -1;
-      __threadfence_block();
-      __syncwarp();
-      for (int s = lane; s < n; s += 32) {
-        uint32_t bits = 0;
-        for (int j = 0; j < p.rk; ++j) {
-          const int y = out[s * p.rk + j];
-          if (y < 0) continue;
-          const int kb = y / p.sk;
-          for (int ii = 0; ii < p.rq; ++ii) {
-            const int x = qt * p.rq + ii;
-            if (__ldg(mbh + (size_t)(x / p.sq) * p.NKB + kb) != 0) bits |= 1u << (ii * p.rk + j);
-          }
-        }
-        p.slot_mask[s0 + s] = bits;
+__device__ void fill_row(const PlanDev& p, int r, int lane) {
+  const int bh = r / p.NQT, qt = r % p.NQT;
+  const uint8_t* mbh = p.mask + (size_t)bh * p.NQB * p.NKB;
+  const int s0 = p.row_ptr[r];
+  const int n = p.row_ptr[r + 1] - s0;
+  const int cap = n * p.rk;
+  int32_t* out = p.slot_ku + (size_t)s0 * p.rk;
+  int pos = 0;
+  for (int y0 = 0; y0 < p.NKU; y0 += 32) {
+    const int y = y0 + lane;
+    int o;
+    const int u = (y < p.NKU) ? unit_union(mbh, p, qt, y, &o) : 0;
+    const uint32_t bal = __ballot_sync(0xffffffffu, u);
+    if (u) {
+      const int idx = pos + __popc(bal & lanemask_lt());
+      if (idx < cap) out[idx] = y;
+    }
+    pos += __popc(bal);
+  }
+  for (int idx = pos + lane; idx < cap; idx += 32) out[idx] = -1;
+  __threadfence_block();
+  __syncwarp();
+  for (int s = lane; s < n; s += 32) {
+    uint32_t bits = 0;
+    for (int j = 0; j < p.rk; ++j) {
+      const int y = out[s * p.rk + j];
+      if (y < 0) continue;
+      const int kb = y / p.sk;
+      for (int ii = 0; ii < p.rq; ++ii) {
+        const int x = qt * p.rq + ii;
+        if (__ldg(mbh + (size_t)(x / p.sq) * p.NKB + kb) != 0) bits |= 1u << (ii * p.rk + j);
       }
     }
-    // Stable counting-sort scatter of this segment's rows.
-    for (int k = threadIdx.x; k < p.nkeys; k += kThreads)
-      start_s[k] = p.hist[(size_t)cta * p.nkeys + k];
-    const int r = cta * kPlanSegRows + threadIdx.x;
-    const bool valid = r < p.rows;
-    const int key = valid ? p.slots[r] : -1;
+    p.slot_mask[s0 + s] = bits;
+  }
+}
+
+__device__ void fill_union_row(const PlanDev& p, int ur, int lane) {
+  const int bhk = ur / p.NQT, qt = ur % p.NQT;
+  const int b = bhk / p.Hkv, hk = bhk % p.Hkv;
+  const int s0 = p.urow_ptr[ur];
+  const int cap = p.urow_ptr[ur + 1] - s0;
+  int pos = 0;
+  for (int y0 = 0; y0 < p.NKU; y0 += 32) {
+    const int y = y0 + lane;
+    const int u = (y < p.NKU) ? union_unit(p, b, hk, qt, y) : 0;
+    const uint32_t bal = __ballot_sync(0xffffffffu, u);
+    if (u) {
+      const int idx = pos + __popc(bal & lanemask_lt());
+      if (idx < cap) p.ukb[s0 + idx] = y;
+    }
+    pos += __popc(bal);
+  }
+}
+
+// Stable counting sort of one K/V-head group's rows by slots descending.
+__device__ void order_group(const PlanDev& p, int gi, int* start_s) {
+  __shared__ int wsum[32];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int gsz = p.g * p.NQT;
+  const int r0 = gi * gsz;
+  for (int k = threadIdx.x; k < p.nkeys; k += kThreads) start_s[k] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < gsz; i += kThreads) atomicAdd(&start_s[p.slots[r0 + i]], 1);
+  __syncthreads();
+  // exclusive scan over keys in descending order
+  int carry = 0;
+  for (int base = 0; base < p.nkeys; base += kThreads) {
+    const int key = p.nkeys - 1 - (base + (int)threadIdx.x);
+    const int v = (key >= 0) ? start_s[key] : 0;
+    int ex;
+    const int tot = block_exclusive_scan<int>(v, &ex, wsum);
+    if (key >= 0) start_s[key] = carry + ex;
+    carry += tot;
+    __syncthreads();
+  }
+  const int base_pos = p.gstart[gi];
+  for (int c0 = 0; c0 < gsz; c0 += kThreads) {
+    const int i = c0 + (int)threadIdx.x;
+    const bool valid = i < gsz;
+    const int key = valid ? p.slots[r0 + i] : -1;
     for (int w = 0; w < kWarps; ++w) {
       __syncthreads();
       if (warp == w) {
@@ -261,55 +274,51 @@ __global__ void __launch_bounds__(kThreads) plan_fill_kernel(const PlanDev p) {
         if (valid) pos = start_s[key] + __popc(peers & lanemask_lt());
         __syncwarp();
         if (valid) {
-          p.order[pos] = r;
+          p.order[base_pos + pos] = r0 + i;
           if (lane == __ffs(peers) - 1) start_s[key] += __popc(peers);
         }
       }
     }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) plan_fill_kernel(const PlanDev p) {
+  extern __shared__ int start_s[];  // [nkeys]
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int row_ctas = (p.rows + kWarps - 1) / kWarps;
+  const int union_ctas = (p.urows + kWarps - 1) / kWarps;
+  const int cta = blockIdx.x;
+  if (cta < row_ctas) {
+    const int r = cta * kWarps + warp;
+    if (r < p.rows) fill_row(p, r, lane);
+  } else if (cta < row_ctas + union_ctas) {
+    const int ur = (cta - row_ctas) * kWarps + warp;
+    if (ur < p.urows) fill_union_row(p, ur, lane);
   } else {
-    const int useg = cta - p.segments;
-    for (int i = 0; i < 32; ++i) {
-      const int ur = useg * kPlanSegRows + warp * 32 + i;
-      if (ur >= p.urows) break;
-      const int bhk = ur / p.NQT, qt = ur % p.NQT;
-      const int b = bhk / p.Hkv, hk = bhk % p.Hkv;
-      const int s0 = p.urow_ptr[ur];
-      const int cap = p.urow_ptr[ur + 1] - s0;
-      int pos = 0;
-      for (int y0 = 0; y0 < p.NKU; y0 += 32) {
-        const int y = y0 + lane;
-        const int u = (y < p.NKU) ? union_unit(p, b, hk, qt, y) : 0;
-        const uint32_t bal = __ballot_sync(0xffffffffu, u);
-        if (u) {
-          const int idx = pos + __popc(bal & lanemask_lt());
-          if (idx < cap) p.ukb[s0 + idx] = y;
-        }
-        pos += __popc(bal);
-      }
-    }
+    order_group(p, cta - row_ctas - union_ctas, start_s);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream) {
-  const int grid = p.segments + p.usegments;
-  const size_t smem = (size_t)p.nkeys * sizeof(int);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(plan_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         kMaxKeys * (int)sizeof(int));
-    cudaFuncSetAttribute(plan_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         kMaxKeys * (int)sizeof(int));
-    attr_set = true;
-  }
-  plan_count_kernel<<<grid, kThreads, smem, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  const int row_ctas = (p.rows + kWarps - 1) / kWarps;
+  const int union_ctas = (p.urows + kWarps - 1) / kWarps;
+  const size_t keys_smem = (size_t)p.nkeys * sizeof(int);
+  const size_t groups_smem = (size_t)p.groups * sizeof(int);
+  cudaError_t e = cudaFuncSetAttribute(plan_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kMaxKeys * (int)sizeof(int));
   if (e != cudaSuccess) return e;
-  plan_scan_kernel<<<1, kScanThreads, 0, stream>>>(p);
+  e = cudaFuncSetAttribute(plan_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMaxGroups * (int)sizeof(int));
+  if (e != cudaSuccess) return e;
+  plan_count_kernel<<<row_ctas + union_ctas, kThreads, 0, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  plan_fill_kernel<<<grid, kThreads, smem, stream>>>(p);
+  plan_scan_kernel<<<1, kScanThreads, groups_smem, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  plan_fill_kernel<<<row_ctas + union_ctas + p.groups, kThreads, keys_smem, stream>>>(p);
   return cudaGetLastError();
 }
 

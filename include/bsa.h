@@ -18,8 +18,9 @@
  *                       the Tessera abstract: logical blocks are retained,
  *                       combined or subdivided into 128-row physical tiles,
  *                       and each (batch, head, 128-row q-tile) gets a CSR list
- *                       of the K/V tiles it needs, plus a longest-row-first
- *                       schedule and (for GQA) a per-group union table
+ *                       of the K/V tiles it needs, plus a schedule (rows that
+ *                       share a K/V head together, heaviest group first,
+ *                       longest row first) and (for GQA) a per-group union table
  *                       ("CompactAttention", summary: Q-block union plus
  *                       intra-group union).
  *   bsa_forward      -- runs attention over exactly the tiles of a plan.
@@ -80,7 +81,7 @@ typedef struct bsa_plan_layout {
   int32_t rows;         /* plan rows R = B*H*NQT */
   int32_t urows;        /* union rows = B*Hkv*NQT when gqa_group > 1, else 0 */
   int32_t max_row_slots;/* ceil(NKU / rk): most slots one row can need */
-  int32_t segments;     /* row segments used by the schedule sort */
+  int32_t groups;       /* K/V-head groups of the schedule = B*Hkv */
   int64_t slot_capacity;  /* rows * max_row_slots */
   int64_t union_capacity; /* urows * NKU */
   uint64_t off_row_ptr;   /* int32 [rows+1]   CSR row pointer into slots */
@@ -88,7 +89,7 @@ typedef struct bsa_plan_layout {
   uint64_t off_slot_mask; /* uint32 [slot_capacity] bit i*rk+j: q-unit i attends slot position j */
   uint64_t off_urow_ptr;  /* int32 [urows+1]  GQA union CSR row pointer */
   uint64_t off_ukb;       /* int32 [union_capacity] union k-units, ascending */
-  uint64_t off_order;     /* int32 [rows]     longest-row-first schedule */
+  uint64_t off_order;     /* int32 [rows]     schedule: K/V-head groups heaviest first, rows longest first */
   uint64_t off_totals;    /* int64 [4]: slots, selected logical blocks, union entries, 0 */
   uint64_t off_control;   /* int32 [16]: [0] work counter, [1] status, [2] status detail */
   uint64_t off_scratch;   /* plan-construction scratch */
