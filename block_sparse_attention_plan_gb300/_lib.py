@@ -78,6 +78,8 @@ def library() -> ctypes.CDLL:
     lib.bsa_plan_check.argtypes = [P, VP]
     lib.bsa_watchdog_selftest.restype = I
     lib.bsa_watchdog_selftest.argtypes = [VP, I, VP]
+    lib.bsa_attention_static.restype = I
+    lib.bsa_attention_static.argtypes = [U8P, I, I, I, I, I, I, I, VP, VP, VP, VP, VP, I, F, VP]
     _lib = lib
     return lib
 
@@ -238,6 +240,28 @@ def attention(mask: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Ten
         (stream or torch.cuda.current_stream()).synchronize()
         return o_h, l_h
     return o, lse
+
+
+def attention_static(mask: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                     bq: int, bk: int, out: Optional[torch.Tensor] = None,
+                     lse: Optional[torch.Tensor] = None, scale: Optional[float] = None,
+                     stream: Optional[torch.cuda.Stream] = None):
+    """Plan + forward in one call with the library's built-in scratch area
+    (bsa_attention_static): for callers that cannot allocate device memory.
+    ``out`` and ``lse`` may be supplied so that nothing is allocated here."""
+    B, H, NQB, NKB = mask.shape
+    d = q.shape[3]
+    g = q.shape[1] // k.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    _check(library().bsa_attention_static(
+        ctypes.c_void_p(mask.data_ptr()), B, H, NQB, NKB, bq, bk, g,
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+        ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()), d,
+        0.0 if scale is None else float(scale), _stream_ptr(stream)), "bsa_attention_static")
+    return out, lse
 
 
 def default_scale(d: int) -> float:

@@ -176,6 +176,41 @@ bsa_status bsa_plan_check(const bsa_plan* plan, void* stream);
  */
 bsa_status bsa_watchdog_selftest(int32_t* status, int limit_us, void* stream);
 
+/*
+ * bsa_attention_static -- plan + forward in one call, allocating nothing.
+ * The method's pages have no counterpart of this call; it exists for callers
+ * that cannot allocate device memory (for example an inference-engine plugin
+ * whose execute step must not call cudaMalloc, or a component that only ever
+ * receives device pointers).  Instead of a caller workspace it uses a scratch
+ * area compiled into the library: a file-scope __device__ array of
+ * BSA_STATIC_WORKSPACE_BYTES that every GPU loading the library holds until
+ * the process exits.
+ * Arguments: as bsa_plan_create (mask, geometry, block sizes, gqa_group)
+ * followed by bsa_forward's (Q, K, V, O, LSE, d, scale) and the stream; the
+ * GQA union table is not built.  All pointers are device pointers owned by
+ * the caller.
+ * Limits and behaviour:
+ *   - Returns BSA_ERR_WORKSPACE, before anything is enqueued, when the
+ *     problem's plan needs more than BSA_STATIC_WORKSPACE_BYTES.
+ *   - Calls no cudaMalloc/cudaFree or other allocating routine.  The first
+ *     call on a device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one scratch area and leaves its
+ *     contents behind; the call clears what must start at zero (work counter
+ *     and status words) itself.  Calls whose GPU work overlaps in time (for
+ *     example on two streams) race on the scratch area and must be avoided.
+ *   - Enqueues a memset, the three plan kernels and the forward kernel on
+ *     `stream` without synchronising.  Errors detected by the kernels
+ *     (watchdog expiry, out-of-range plan data) are recorded in the scratch
+ *     area and are not reported by this call; it returns host-detected
+ *     argument errors and launch failures only.
+ */
+#define BSA_STATIC_WORKSPACE_BYTES (16u << 20)
+bsa_status bsa_attention_static(const uint8_t* mask, int B, int H, int NQB, int NKB, int bq,
+                                int bk, int gqa_group, const void* Q, const void* K, const void* V,
+                                void* O, float* LSE, int d, float scale, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* bsa_status_string(int status);
 
