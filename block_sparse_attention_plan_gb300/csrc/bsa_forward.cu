@@ -193,8 +193,8 @@ __device__ __forceinline__ bool load_kv_tile(const FwdParams& p, const Smem<D>& 
 }
 
 template <int D>
-__device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, const Smem<D>& sm,
-                                           const Watchdog& wd) {
+__device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, const Smem<D> sm,
+                                           const Watchdog wd) {
   using C = Cfg<D>;
   tma_prefetch_desc(&p.tmQ);
   tma_prefetch_desc(&p.tmK);
@@ -244,24 +244,53 @@ __device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, co
 }
 
 // ------------------------------------------------------------------ MMA issuer
-// S_w = Q K^T for the next K tile of the ring (both operands K-major, 128B
-// swizzle; 16 columns of d per instruction).
+// Descriptors are built once; per instruction only a compile-time offset is
+// added (the start-address field is the low 14 bits of the descriptor and
+// shared-memory offsets here never carry out of it), so each tcgen05.mma costs
+// the issuing thread a couple of instructions.
 template <int D>
-__device__ __forceinline__ bool issue_s(const Smem<D>& sm, uint32_t tmem, int qb, int w,
-                                        uint32_t& kv_it, const Watchdog& wd) {
+struct MmaDesc {
+  using C = Cfg<D>;
+  uint64_t q[2];   // K-major SW128 descriptor of each Q buffer
+  uint64_t k0;     // K-major SW128 descriptor of ring stage 0 (K tiles)
+  uint64_t v0;     // MN-major SW128 descriptor of ring stage 0 (V tiles)
+  static constexpr uint64_t kStageStep = (uint64_t)(C::kTileBytes >> 4);
+};
+
+// S_w = Q K^T: M=128, N=128, K=16 per instruction, d/16 instructions.
+template <int D>
+__device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc) {
   using C = Cfg<D>;
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = (uint64_t)(((kk / 4) * C::kChunkBytes + (kk % 4) * 32) >> 4);
+    mma_ss(d_tmem, adesc + off, bdesc + off, kIdescS, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O_w (+)= P_w V: M=128, N=d, K=16 keys per instruction, 8 instructions.
+// P columns [8kk, 8kk+8) hold keys [16kk, 16kk+16) as bf16 pairs; V rows
+// [16kk, 16kk+16) start 2048 bytes apart (MN-major: LBO = next 64 columns).
+template <int D>
+__device__ __forceinline__ void mma_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t vdesc,
+                                       uint32_t acc) {
+  constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ts(o_tmem, p_tmem + 8 * kk, vdesc + (uint64_t)(kk * (2048 >> 4)), kIdescPV,
+           (acc || kk > 0) ? 1u : 0u);
+}
+
+template <int D>
+__device__ __forceinline__ bool issue_s(const Smem<D>& sm, const MmaDesc<D>& ds, uint32_t tmem,
+                                        int qb, int w, uint32_t& kv_it, const Watchdog& wd) {
+  using C = Cfg<D>;
   const int stage = (int)(kv_it % C::kStages);
   if (!mbar_wait(sm.bar(C::kBarKvFull + stage), (kv_it / C::kStages) & 1u, wd, kSiteKvFull))
     return false;
   tc_fence_after();
-  const uint32_t qa = sm.q(qb), ka = sm.stage(stage);
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk / 4) * C::kChunkBytes + (kk % 4) * 32;
-    mma_ss(tmem + col_s(w), smem_desc_sw128(qa + off, 16, 1024),
-           smem_desc_sw128(ka + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
-  }
+  mma_qk<D>(tmem + col_s(w), ds.q[qb], ds.k0 + (uint64_t)stage * MmaDesc<D>::kStageStep);
   mma_commit(sm.bar(C::kBarKvEmpty + stage));
   mma_commit(sm.bar(C::kBarSFull + w));
   ++kv_it;
@@ -269,10 +298,14 @@ __device__ __forceinline__ bool issue_s(const Smem<D>& sm, uint32_t tmem, int qb
 }
 
 template <int D>
-__device__ __noinline__ void mma_role(const FwdParams& p, const uint8_t* smem, const Smem<D>& sm,
-                                      uint32_t tmem, const Watchdog& wd) {
+__device__ __noinline__ void mma_role(const FwdParams& p, const uint8_t* smem, const Smem<D> sm,
+                                      uint32_t tmem, const Watchdog wd) {
   using C = Cfg<D>;
-  constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
+  MmaDesc<D> ds;
+  ds.q[0] = smem_desc_sw128(sm.q(0), 16, 1024);
+  ds.q[1] = smem_desc_sw128(sm.q(1), 16, 1024);
+  ds.k0 = smem_desc_sw128(sm.stage(0), 16, 1024);
+  ds.v0 = smem_desc_sw128(sm.stage(0), C::kChunkBytes, 1024);
   uint32_t q_it = 0, kv_it = 0, pc0 = 0, pc1 = 0;
   bool ok = true;
   for (uint32_t t = 0; ok; ++t) {
@@ -283,17 +316,17 @@ __device__ __noinline__ void mma_role(const FwdParams& p, const uint8_t* smem, c
     const int qb = (int)(q_it & 1u);
     if (!mbar_wait(sm.bar(C::kBarQFull + qb), (q_it >> 1) & 1u, wd, kSiteQFull)) break;
     tc_fence_after();
-    ok = issue_s<D>(sm, tmem, qb, 0, kv_it, wd);
-    if (ok && m.n > 1) ok = issue_s<D>(sm, tmem, qb, 1, kv_it, wd);
+    ok = issue_s<D>(sm, ds, tmem, qb, 0, kv_it, wd);
+    if (ok && m.n > 1) ok = issue_s<D>(sm, ds, tmem, qb, 1, kv_it, wd);
     if (ok && m.n <= 2) mma_commit(sm.bar(C::kBarQEmpty + qb));
     for (int j = 0; j < m.n && ok; ++j) {
       const int w = j & 1;
-      uint32_t& pc = w ? pc1 : pc0;
+      const uint32_t pc = w ? pc1 : pc0;
       if (!mbar_wait(sm.bar(C::kBarPFull + w), pc & 1u, wd, kSitePFull)) {
         ok = false;
         break;
       }
-      ++pc;
+      if (w) ++pc1; else ++pc0;
       tc_fence_after();
       const int stage = (int)(kv_it % C::kStages);
       if (!mbar_wait(sm.bar(C::kBarKvFull + stage), (kv_it / C::kStages) & 1u, wd, kSiteKvFull)) {
@@ -301,20 +334,13 @@ __device__ __noinline__ void mma_role(const FwdParams& p, const uint8_t* smem, c
         break;
       }
       tc_fence_after();
-      const uint32_t va = sm.stage(stage);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        // 16 keys per instruction: P columns [8kk, 8kk+8) (bf16 pairs) and V
-        // rows [16kk, 16kk+16) (MN-major: LBO = next 64 columns of d).
-        mma_ts(tmem + col_o(w), tmem + col_s(w) + 8 * kk,
-               smem_desc_sw128(va + kk * 2048, C::kChunkBytes, 1024), kIdescPV,
-               (j >= 2 || kk > 0) ? 1u : 0u);
-      }
+      mma_pv<D>(tmem + col_o(w), tmem + col_s(w),
+                ds.v0 + (uint64_t)stage * MmaDesc<D>::kStageStep, j >= 2 ? 1u : 0u);
       mma_commit(sm.bar(C::kBarKvEmpty + stage));
       ++kv_it;
       if (j + 2 >= m.n) mma_commit(sm.bar(C::kBarODone + w));
       if (j + 2 < m.n) {
-        ok = issue_s<D>(sm, tmem, qb, w, kv_it, wd);
+        ok = issue_s<D>(sm, ds, tmem, qb, w, kv_it, wd);
         if (ok && j + 2 == m.n - 1) mma_commit(sm.bar(C::kBarQEmpty + qb));
       }
     }
@@ -375,11 +401,16 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
           }
         }
       }
+      // row max: four independent chains of three-input max
       float mx4[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) mx4[c] = __uint_as_float(v[c]);
 #pragma unroll
-      for (int e = 4; e < 128; ++e) mx4[e & 3] = fmaxf(mx4[e & 3], __uint_as_float(v[e]));
+      for (int e = 4; e < 128; e += 8) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          mx4[c] = fmax3(mx4[c], __uint_as_float(v[e + 2 * c]), __uint_as_float(v[e + 2 * c + 1]));
+      }
       const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float m_new = fmaxf(m_ref, mx * sl2);
       float factor = 1.f;
@@ -392,21 +423,27 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
       // p = 2^(s*scale*log2e - m_ref), packed as bf16 pairs into the first
       // 64 columns of this group's S region (keys 2c, 2c+1 -> column c).
-      float sum0 = 0.f, sum1 = 0.f;
+      const uint64_t sl2x2 = f2_make(sl2, sl2), nmbx2 = f2_make(-mb, -mb);
+      uint64_t acc2[2] = {0ull, 0ull};  // two packed partial sums (4 chains)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(v[c * 32 + 2 * e]), sl2, -mb));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(v[c * 32 + 2 * e + 1]), sl2, -mb));
-          sum0 += p0;
-          sum1 += p1;
+          const uint64_t sv = f2_make(__uint_as_float(v[c * 32 + 2 * e]),
+                                      __uint_as_float(v[c * 32 + 2 * e + 1]));
+          float x0, x1;
+          f2_split(ffma2(sv, sl2x2, nmbx2), x0, x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          acc2[e & 1] = fadd2(acc2[e & 1], f2_make(p0, p1));
           pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(s_addr + c * 16, pk);
       }
-      const float sum = sum0 + sum1;
+      float s0, s1, s2, s3;
+      f2_split(acc2[0], s0, s1);
+      f2_split(acc2[1], s2, s3);
+      const float sum = (s0 + s1) + (s2 + s3);
       if (__any_sync(0xffffffffu, factor != 1.f)) {
         const uint32_t o_addr = tmem + tl + col_o(w);
 #pragma unroll

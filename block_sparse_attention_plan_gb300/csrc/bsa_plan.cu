@@ -29,6 +29,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kScanThreads = 1024;
+constexpr int kBatch = 4;  // 32-unit chunks whose mask loads are issued together
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
@@ -58,14 +59,14 @@ __device__ __forceinline__ int unit_union(const uint8_t* __restrict__ mbh, const
 __device__ __forceinline__ int union_unit(const PlanDev& p, int b, int hk, int qt, int y) {
   const int kb = y / p.sk;
   int u = 0;
-  for (int hh = 0; hh < p.g && !u; ++hh) {
+  for (int hh = 0; hh < p.g; ++hh) {  // no early exit: the loads are independent
     const uint8_t* mbh = p.mask + ((size_t)(b * p.H + hk * p.g + hh)) * p.NQB * p.NKB;
     for (int i = 0; i < p.rq; ++i) {
       const int x = qt * p.rq + i;
-      u |= __ldg(mbh + (size_t)(x / p.sq) * p.NKB + kb) != 0;
+      u |= __ldg(mbh + (size_t)(x / p.sq) * p.NKB + kb);
     }
   }
-  return u;
+  return u != 0;
 }
 
 __global__ void __launch_bounds__(kThreads) plan_count_kernel(const PlanDev p) {
@@ -77,12 +78,20 @@ __global__ void __launch_bounds__(kThreads) plan_count_kernel(const PlanDev p) {
     const int bh = r / p.NQT, qt = r % p.NQT;
     const uint8_t* mbh = p.mask + (size_t)bh * p.NQB * p.NKB;
     int cnt = 0, own = 0;
-    for (int y0 = 0; y0 < p.NKU; y0 += 32) {
-      const int y = y0 + lane;
-      int u = 0, o = 0;
-      if (y < p.NKU) u = unit_union(mbh, p, qt, y, &o);
-      cnt += __popc(__ballot_sync(0xffffffffu, u));
-      own += o;
+    for (int y0 = 0; y0 < p.NKU; y0 += 32 * kBatch) {
+      int u[kBatch], o[kBatch];
+#pragma unroll
+      for (int c = 0; c < kBatch; ++c) {  // all loads of the batch first
+        const int y = y0 + c * 32 + lane;
+        u[c] = 0;
+        o[c] = 0;
+        if (y < p.NKU) u[c] = unit_union(mbh, p, qt, y, &o[c]);
+      }
+#pragma unroll
+      for (int c = 0; c < kBatch; ++c) {
+        cnt += __popc(__ballot_sync(0xffffffffu, u[c]));
+        own += o[c];
+      }
     }
     for (int s = 16; s > 0; s >>= 1) own += __shfl_xor_sync(0xffffffffu, own, s);
     if (lane == 0) {
@@ -95,10 +104,15 @@ __global__ void __launch_bounds__(kThreads) plan_count_kernel(const PlanDev p) {
     const int bhk = ur / p.NQT, qt = ur % p.NQT;
     const int b = bhk / p.Hkv, hk = bhk % p.Hkv;
     int cnt = 0;
-    for (int y0 = 0; y0 < p.NKU; y0 += 32) {
-      const int y = y0 + lane;
-      const int u = (y < p.NKU) ? union_unit(p, b, hk, qt, y) : 0;
-      cnt += __popc(__ballot_sync(0xffffffffu, u));
+    for (int y0 = 0; y0 < p.NKU; y0 += 32 * kBatch) {
+      int u[kBatch];
+#pragma unroll
+      for (int c = 0; c < kBatch; ++c) {
+        const int y = y0 + c * 32 + lane;
+        u[c] = (y < p.NKU) ? union_unit(p, b, hk, qt, y) : 0;
+      }
+#pragma unroll
+      for (int c = 0; c < kBatch; ++c) cnt += __popc(__ballot_sync(0xffffffffu, u[c]));
     }
     if (lane == 0) p.ucnt[ur] = cnt;
   }
@@ -193,16 +207,23 @@ __device__ void fill_row(const PlanDev& p, int r, int lane) {
   const int cap = n * p.rk;
   int32_t* out = p.slot_ku + (size_t)s0 * p.rk;
   int pos = 0;
-  for (int y0 = 0; y0 < p.NKU; y0 += 32) {
-    const int y = y0 + lane;
-    int o;
-    const int u = (y < p.NKU) ? unit_union(mbh, p, qt, y, &o) : 0;
-    const uint32_t bal = __ballot_sync(0xffffffffu, u);
-    if (u) {
-      const int idx = pos + __popc(bal & lanemask_lt());
-      if (idx < cap) out[idx] = y;
+  for (int y0 = 0; y0 < p.NKU; y0 += 32 * kBatch) {
+    int u[kBatch];
+#pragma unroll
+    for (int c = 0; c < kBatch; ++c) {
+      const int y = y0 + c * 32 + lane;
+      int o;
+      u[c] = (y < p.NKU) ? unit_union(mbh, p, qt, y, &o) : 0;
     }
-    pos += __popc(bal);
+#pragma unroll
+    for (int c = 0; c < kBatch; ++c) {  // ascending k-units: chunk by chunk
+      const uint32_t bal = __ballot_sync(0xffffffffu, u[c]);
+      if (u[c]) {
+        const int idx = pos + __popc(bal & lanemask_lt());
+        if (idx < cap) out[idx] = y0 + c * 32 + lane;
+      }
+      pos += __popc(bal);
+    }
   }
   for (int idx = pos + lane; idx < cap; idx += 32) out[idx] = -1;
   __threadfence_block();
@@ -228,15 +249,22 @@ __device__ void fill_union_row(const PlanDev& p, int ur, int lane) {
   const int s0 = p.urow_ptr[ur];
   const int cap = p.urow_ptr[ur + 1] - s0;
   int pos = 0;
-  for (int y0 = 0; y0 < p.NKU; y0 += 32) {
-    const int y = y0 + lane;
-    const int u = (y < p.NKU) ? union_unit(p, b, hk, qt, y) : 0;
-    const uint32_t bal = __ballot_sync(0xffffffffu, u);
-    if (u) {
-      const int idx = pos + __popc(bal & lanemask_lt());
-      if (idx < cap) p.ukb[s0 + idx] = y;
+  for (int y0 = 0; y0 < p.NKU; y0 += 32 * kBatch) {
+    int u[kBatch];
+#pragma unroll
+    for (int c = 0; c < kBatch; ++c) {
+      const int y = y0 + c * 32 + lane;
+      u[c] = (y < p.NKU) ? union_unit(p, b, hk, qt, y) : 0;
     }
-    pos += __popc(bal);
+#pragma unroll
+    for (int c = 0; c < kBatch; ++c) {
+      const uint32_t bal = __ballot_sync(0xffffffffu, u[c]);
+      if (u[c]) {
+        const int idx = pos + __popc(bal & lanemask_lt());
+        if (idx < cap) p.ukb[s0 + idx] = y0 + c * 32 + lane;
+      }
+      pos += __popc(bal);
+    }
   }
 }
 
