@@ -11,13 +11,15 @@
 //
 // One CTA (384 threads) per SM, looping over plan rows (one 128-row q-tile of
 // one head each) in longest-row-first order:
-//   warp 0      TMA producer: Q tile (double-buffered), then the K and V
-//               tiles of the row's slots into a ring of shared-memory stages
-//               guarded by full/empty mbarriers.  A slot of 128 keys is
+//   warps 0, 2  TMA producers, one per softmax group: each loads the K and V
+//               tiles of its group's slots into its own ring of shared-memory
+//               stages guarded by full/empty mbarriers; warp 0 also takes the
+//               work items and loads each row's Q tile.  A slot of 128 keys is
 //               gathered as rk boxes of ku rows (ku = 128 / rk).
-//   warp 1      MMA issuer (one thread): tcgen05.mma S = Q K^T (both operands
-//               in shared memory) and O += P V (P read from tensor memory).
-//   warp 2      owns the tensor-memory allocation (512 columns).
+//   warps 1, 3  MMA issuers (one thread each, one per softmax group):
+//               tcgen05.mma S = Q K^T (both operands in shared memory) and
+//               O += P V (P read from tensor memory).
+//   warp 2      also owns the tensor-memory allocation (512 columns).
 //   warps 4-7   softmax warpgroup A: even slots of the row.
 //   warps 8-11  softmax warpgroup B: odd slots of the row.
 // Each warpgroup keeps its own running max/sum and its own O accumulator, so
@@ -46,31 +48,39 @@ constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
 // Register split: 384 threads x 168 at launch = 64,512 registers =
 // 128 x kRegsControl (warps 0-3) + 256 x kRegsSoftmax (warps 4-11).
-constexpr int kRegsControl = 56;
-constexpr int kRegsSoftmax = 224;
+constexpr int kRegsControl = 64;
+constexpr int kRegsSoftmax = 216;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split");
 __device__ __forceinline__ uint32_t col_s(int w) { return (uint32_t)(w * 128); }
 __device__ __forceinline__ uint32_t col_o(int w) { return (uint32_t)(256 + w * 128); }
-constexpr float kRescaleThreshold = 8.0f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only past 2^8 growth
 // Work items (positions in the longest-row-first order) are taken from a
 // global atomic counter by the producer and handed to the other roles through
 // a small ring in shared memory.
 constexpr int kSchedSlots = 4;
-constexpr int kSchedConsumers = 1 + 8;  // MMA thread + one lane per softmax warp  // log2 units: rescale O only past 2^8 growth
+constexpr int kSchedConsumers = 1 + 2 + 8;  // ring-B producer, two MMA threads, one lane per softmax warp
 
 template <int D>
 struct Cfg {
   static constexpr int kTileBytes = 128 * D * 2;   // 128 rows x d bf16
   static constexpr int kChunks = D / 64;           // 64-column (128-byte) swizzle blocks
   static constexpr int kChunkBytes = 128 * 128;    // one block of 128 rows
-  static constexpr int kStages = (D == 128) ? 5 : 12;
+  // One K/V ring per softmax group (group A takes the even slots of a row,
+  // group B the odd ones); each ring is consumed in order by one MMA thread.
+  static constexpr int kStagesA = (D == 128) ? 3 : 6;
+  static constexpr int kStagesB = (D == 128) ? 3 : 6;
+  static constexpr int kQBufs = (D == 128) ? 1 : 2;  // Q tile buffers
   static constexpr int kOffQ = 0;
-  static constexpr int kOffRing = 2 * kTileBytes;
-  static constexpr int kOffBar = kOffRing + kStages * kTileBytes;
+  static constexpr int kOffRingA = kQBufs * kTileBytes;
+  static constexpr int kOffRingB = kOffRingA + kStagesA * kTileBytes;
+  static constexpr int kOffBar = kOffRingB + kStagesB * kTileBytes;
   // barriers
-  static constexpr int kBarQFull = 0, kBarQEmpty = 2, kBarKvFull = 4;
-  static constexpr int kBarKvEmpty = kBarKvFull + kStages;
-  static constexpr int kBarSFull = kBarKvEmpty + kStages;
+  static constexpr int kBarQFull = 0, kBarQEmpty = 2;
+  static constexpr int kBarKvFullA = 4;
+  static constexpr int kBarKvEmptyA = kBarKvFullA + kStagesA;
+  static constexpr int kBarKvFullB = kBarKvEmptyA + kStagesA;
+  static constexpr int kBarKvEmptyB = kBarKvFullB + kStagesB;
+  static constexpr int kBarSFull = kBarKvEmptyB + kStagesB;
   static constexpr int kBarPFull = kBarSFull + 2;
   static constexpr int kBarODone = kBarPFull + 2;
   static constexpr int kBarXchg = kBarODone + 2;
@@ -83,7 +93,17 @@ struct Cfg {
   static constexpr int kOffML = kOffSched + 4 * kSchedSlots;  // float [4][128]: mA, mB, lA, lB
   static constexpr int kSmemBytes = kOffML + 4 * 128 * 4;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  __host__ __device__ static constexpr int stages(int w) { return w ? kStagesB : kStagesA; }
+  __host__ __device__ static constexpr int bar_full(int w) { return w ? kBarKvFullB : kBarKvFullA; }
+  __host__ __device__ static constexpr int bar_empty(int w) { return w ? kBarKvEmptyB : kBarKvEmptyA; }
+  __host__ __device__ static constexpr int ring(int w) { return w ? kOffRingB : kOffRingA; }
 };
+
+// Q buffer index and phase parity of the q_it-th non-empty row of a CTA.
+template <int D>
+__device__ __forceinline__ int q_buf(uint32_t q_it) { return (int)(q_it % Cfg<D>::kQBufs); }
+template <int D>
+__device__ __forceinline__ uint32_t q_par(uint32_t q_it) { return (q_it / Cfg<D>::kQBufs) & 1u; }
 
 struct Item {
   int n;       // slots of the row (0 = empty or rejected)
@@ -128,8 +148,8 @@ struct Smem {
   uint32_t base;
   __device__ __forceinline__ uint32_t bar(int i) const { return base + C::kOffBar + 8u * (uint32_t)i; }
   __device__ __forceinline__ uint32_t q(int qb) const { return base + C::kOffQ + qb * C::kTileBytes; }
-  __device__ __forceinline__ uint32_t stage(int s) const {
-    return base + C::kOffRing + (uint32_t)s * C::kTileBytes;
+  __device__ __forceinline__ uint32_t stage(int w, int s) const {
+    return base + C::ring(w) + (uint32_t)s * C::kTileBytes;
   }
 };
 
@@ -161,12 +181,14 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 template <int D>
 __device__ __forceinline__ bool load_kv_tile(const FwdParams& p, const Smem<D>& sm,
                                              const CUtensorMap* map, const Item& m, int j,
-                                             uint32_t& kv_it, uint64_t pol, const Watchdog& wd) {
+                                             uint32_t (&kv_it)[2], uint64_t pol, const Watchdog& wd) {
   using C = Cfg<D>;
-  const int stage = (int)(kv_it % C::kStages);
-  const uint32_t ph = (kv_it / C::kStages) & 1u;
-  if (!mbar_wait(sm.bar(C::kBarKvEmpty + stage), ph ^ 1u, wd, kSiteKvEmpty)) return false;
-  const uint32_t full = sm.bar(C::kBarKvFull + stage);
+  const int w = j & 1;  // ring of the softmax group that owns slot j
+  const int nst = C::stages(w);
+  const int stage = (int)(kv_it[w] % nst);
+  const uint32_t ph = (kv_it[w] / nst) & 1u;
+  if (!mbar_wait(sm.bar(C::bar_empty(w) + stage), ph ^ 1u, wd, kSiteKvEmpty)) return false;
+  const uint32_t full = sm.bar(C::bar_full(w) + stage);
   mbar_arrive_expect_tx(full, C::kTileBytes);
   const int32_t* ent = p.slot_ku + (size_t)(m.s0 + j) * p.rk;
   int first = __ldg(ent);
@@ -174,7 +196,7 @@ __device__ __forceinline__ bool load_kv_tile(const FwdParams& p, const Smem<D>& 
     record_status(p.control, -7, kSitePlanRange + 2);
     first = 0;
   }
-  const uint32_t dst0 = sm.stage(stage);
+  const uint32_t dst0 = sm.stage(w, stage);
   for (int u = 0; u < p.rk; ++u) {
     int y = __ldg(ent + u);
     if (y < 0) {
@@ -188,58 +210,72 @@ __device__ __forceinline__ bool load_kv_tile(const FwdParams& p, const Smem<D>& 
     for (int c = 0; c < C::kChunks; ++c)
       tma_load_2d(dst0 + c * C::kChunkBytes + u * p.ku * 128, map, c * 64, row, full, pol);
   }
-  ++kv_it;
+  ++kv_it[w];
   return true;
 }
 
+// Producer of ring w.  The ring-A producer (w = 0) also takes work items from
+// the global counter, publishes them, and loads each row's Q tile; the ring-B
+// producer (w = 1) reads the published items.  Each loads, in consumption
+// order, the K and V tiles of its group's slots j = w, w+2, ...
 template <int D>
 __device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, const Smem<D> sm,
-                                           const Watchdog wd) {
+                                           const Watchdog wd, int w) {
   using C = Cfg<D>;
-  tma_prefetch_desc(&p.tmQ);
+  if (w == 0) tma_prefetch_desc(&p.tmQ);
   tma_prefetch_desc(&p.tmK);
   tma_prefetch_desc(&p.tmV);
   const uint64_t pol_q = policy_evict_first();
   const uint64_t pol_kv = policy_evict_last();
-  uint32_t q_it = 0, kv_it = 0;
+  uint32_t q_it = 0, kv_it[2] = {0u, 0u};
   bool ok = true;
   volatile int* sched = reinterpret_cast<volatile int*>(smem + C::kOffSched);
   for (uint32_t t = 0; ok; ++t) {
-    const int slot = (int)(t % kSchedSlots);
-    if (!mbar_wait(sm.bar(C::kBarSchedEmpty + slot), ((t / kSchedSlots) & 1u) ^ 1u, wd, kSiteSched))
-      break;
-    int it = atomicAdd(p.control + kCtlWorkCounter, 1);
-    if (it >= p.rows) it = -1;
-    sched[slot] = it;
-    mbar_arrive(sm.bar(C::kBarSchedFull + slot));
+    int it;
+    if (w == 0) {
+      const int slot = (int)(t % kSchedSlots);
+      if (!mbar_wait(sm.bar(C::kBarSchedEmpty + slot), ((t / kSchedSlots) & 1u) ^ 1u, wd,
+                     kSiteSched))
+        break;
+      it = atomicAdd(p.control + kCtlWorkCounter, 1);
+      if (it >= p.rows) it = -1;
+      sched[slot] = it;
+      mbar_arrive(sm.bar(C::kBarSchedFull + slot));
+    } else {
+      it = sched_take<D>(sm, smem, t, true, false, wd);
+    }
     if (it < 0) break;
-    const Item m = load_item(p, it, true);
+    const Item m = load_item(p, it, w == 0);
     if (m.n == 0) continue;
-    const int qb = (int)(q_it & 1u);
-    if (!mbar_wait(sm.bar(C::kBarQEmpty + qb), ((q_it >> 1) & 1u) ^ 1u, wd, kSiteQEmpty)) break;
-    mbar_arrive_expect_tx(sm.bar(C::kBarQFull + qb), C::kTileBytes);
-    const int qrow = m.bh * p.Nq + m.qt * 128;
+    if (w == 0) {
+      const int qb = q_buf<D>(q_it);
+      if (!mbar_wait(sm.bar(C::kBarQEmpty + qb), q_par<D>(q_it) ^ 1u, wd, kSiteQEmpty)) break;
+      mbar_arrive_expect_tx(sm.bar(C::kBarQFull + qb), C::kTileBytes);
+      const int qrow = m.bh * p.Nq + m.qt * 128;
 #pragma unroll
-    for (int c = 0; c < C::kChunks; ++c)
-      tma_load_2d(sm.q(qb) + c * C::kChunkBytes, &p.tmQ, c * 64, qrow, sm.bar(C::kBarQFull + qb),
-                  pol_q);
-    ++q_it;
-    // Ring order = MMA consumption order: K0, K1, then V_j, K_{j+2} for each j.
-    ok = load_kv_tile<D>(p, sm, &p.tmK, m, 0, kv_it, pol_kv, wd);
-    if (ok && m.n > 1) ok = load_kv_tile<D>(p, sm, &p.tmK, m, 1, kv_it, pol_kv, wd);
-    for (int j = 0; j < m.n && ok; ++j) {
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_load_2d(sm.q(qb) + c * C::kChunkBytes, &p.tmQ, c * 64, qrow,
+                    sm.bar(C::kBarQFull + qb), pol_q);
+      ++q_it;
+    }
+    // Ring w in consumption order: K_w, then V_j, K_{j+2} for j = w, w+2, ...
+    if (w < m.n) ok = load_kv_tile<D>(p, sm, &p.tmK, m, w, kv_it, pol_kv, wd);
+    for (int j = w; j < m.n && ok; j += 2) {
       ok = load_kv_tile<D>(p, sm, &p.tmV, m, j, kv_it, pol_kv, wd);
       if (ok && j + 2 < m.n) ok = load_kv_tile<D>(p, sm, &p.tmK, m, j + 2, kv_it, pol_kv, wd);
     }
   }
   if (*wd.abort_flag) {
     // Let copies already issued land before the CTA's shared memory goes away.
-    const uint32_t nk = kv_it < (uint32_t)C::kStages ? kv_it : (uint32_t)C::kStages;
-    for (uint32_t t = kv_it - nk; t < kv_it; ++t)
-      drain_wait(sm.bar(C::kBarKvFull + (int)(t % C::kStages)), (t / C::kStages) & 1u, wd);
-    const uint32_t nq = q_it < 2u ? q_it : 2u;
-    for (uint32_t t = q_it - nq; t < q_it; ++t)
-      drain_wait(sm.bar(C::kBarQFull + (int)(t & 1u)), (t >> 1) & 1u, wd);
+    const uint32_t nst = (uint32_t)C::stages(w);
+    const uint32_t nk = kv_it[w] < nst ? kv_it[w] : nst;
+    for (uint32_t t = kv_it[w] - nk; t < kv_it[w]; ++t)
+      drain_wait(sm.bar(C::bar_full(w) + (int)(t % nst)), (t / nst) & 1u, wd);
+    if (w == 0) {
+      const uint32_t nq = q_it < (uint32_t)C::kQBufs ? q_it : (uint32_t)C::kQBufs;
+      for (uint32_t t = q_it - nq; t < q_it; ++t)
+        drain_wait(sm.bar(C::kBarQFull + q_buf<D>(t)), q_par<D>(t), wd);
+    }
   }
 }
 
@@ -252,8 +288,8 @@ template <int D>
 struct MmaDesc {
   using C = Cfg<D>;
   uint64_t q[2];   // K-major SW128 descriptor of each Q buffer
-  uint64_t k0;     // K-major SW128 descriptor of ring stage 0 (K tiles)
-  uint64_t v0;     // MN-major SW128 descriptor of ring stage 0 (V tiles)
+  uint64_t kv0;    // K-major SW128 descriptor of stage 0 of this thread's ring (K tiles)
+  uint64_t v0;     // MN-major SW128 descriptor of the same stage (V tiles)
   static constexpr uint64_t kStageStep = (uint64_t)(C::kTileBytes >> 4);
 };
 
@@ -284,69 +320,80 @@ __device__ __forceinline__ void mma_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_
 
 template <int D>
 __device__ __forceinline__ bool issue_s(const Smem<D>& sm, const MmaDesc<D>& ds, uint32_t tmem,
-                                        int qb, int w, uint32_t& kv_it, const Watchdog& wd) {
+                                        int qb, int w, uint32_t& kv, const Watchdog& wd) {
   using C = Cfg<D>;
-  const int stage = (int)(kv_it % C::kStages);
-  if (!mbar_wait(sm.bar(C::kBarKvFull + stage), (kv_it / C::kStages) & 1u, wd, kSiteKvFull))
+  const int stage = (int)(kv % C::stages(w));
+  if (!mbar_wait(sm.bar(C::bar_full(w) + stage), (kv / C::stages(w)) & 1u, wd, kSiteKvFull))
     return false;
   tc_fence_after();
-  mma_qk<D>(tmem + col_s(w), ds.q[qb], ds.k0 + (uint64_t)stage * MmaDesc<D>::kStageStep);
-  mma_commit(sm.bar(C::kBarKvEmpty + stage));
+  mma_qk<D>(tmem + col_s(w), ds.q[qb], ds.kv0 + (uint64_t)stage * MmaDesc<D>::kStageStep);
+  mma_commit(sm.bar(C::bar_empty(w) + stage));
   mma_commit(sm.bar(C::kBarSFull + w));
-  ++kv_it;
+  ++kv;
   return true;
 }
 
+// MMA issuer of softmax group w (slots j = w, w+2, ... of each row), fed by
+// ring w.  Two of these run in separate warps: tcgen05.mma issue is close to
+// synchronous with execution, so while one thread is held issuing, the other
+// does its barrier waits and has its next group of MMAs ready, keeping the
+// tensor pipe fed.
 template <int D>
 __device__ __noinline__ void mma_role(const FwdParams& p, const uint8_t* smem, const Smem<D> sm,
-                                      uint32_t tmem, const Watchdog wd) {
+                                      uint32_t tmem, const Watchdog wd, int w) {
   using C = Cfg<D>;
   MmaDesc<D> ds;
   ds.q[0] = smem_desc_sw128(sm.q(0), 16, 1024);
-  ds.q[1] = smem_desc_sw128(sm.q(1), 16, 1024);
-  ds.k0 = smem_desc_sw128(sm.stage(0), 16, 1024);
-  ds.v0 = smem_desc_sw128(sm.stage(0), C::kChunkBytes, 1024);
-  uint32_t q_it = 0, kv_it = 0, pc0 = 0, pc1 = 0;
+  ds.q[1] = smem_desc_sw128(sm.q(C::kQBufs - 1), 16, 1024);
+  ds.kv0 = smem_desc_sw128(sm.stage(w, 0), 16, 1024);
+  ds.v0 = smem_desc_sw128(sm.stage(w, 0), C::kChunkBytes, 1024);
+  uint32_t q_it = 0, kv = 0, pc = 0;
   bool ok = true;
   for (uint32_t t = 0; ok; ++t) {
     const int it = sched_take<D>(sm, smem, t, true, false, wd);
     if (it < 0) break;
     const Item m = load_item(p, it, false);
-    if (m.n == 0) continue;
-    const int qb = (int)(q_it & 1u);
-    if (!mbar_wait(sm.bar(C::kBarQFull + qb), (q_it >> 1) & 1u, wd, kSiteQFull)) break;
+    const int n = m.n;
+    if (n == 0) continue;
+    const int qb = q_buf<D>(q_it);
+    const uint32_t q_empty = sm.bar(C::kBarQEmpty + qb);
+    // Every MMA thread waits for the row's Q before releasing it, so neither
+    // can arrive on q_empty twice within one phase.
+    if (!mbar_wait(sm.bar(C::kBarQFull + qb), q_par<D>(q_it), wd, kSiteQFull)) break;
     tc_fence_after();
-    ok = issue_s<D>(sm, ds, tmem, qb, 0, kv_it, wd);
-    if (ok && m.n > 1) ok = issue_s<D>(sm, ds, tmem, qb, 1, kv_it, wd);
-    if (ok && m.n <= 2) mma_commit(sm.bar(C::kBarQEmpty + qb));
-    for (int j = 0; j < m.n && ok; ++j) {
-      const int w = j & 1;
-      const uint32_t pc = w ? pc1 : pc0;
-      if (!mbar_wait(sm.bar(C::kBarPFull + w), pc & 1u, wd, kSitePFull)) {
-        ok = false;
-        break;
-      }
-      if (w) ++pc1; else ++pc0;
-      tc_fence_after();
-      const int stage = (int)(kv_it % C::kStages);
-      if (!mbar_wait(sm.bar(C::kBarKvFull + stage), (kv_it / C::kStages) & 1u, wd, kSiteKvFull)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      mma_pv<D>(tmem + col_o(w), tmem + col_s(w),
-                ds.v0 + (uint64_t)stage * MmaDesc<D>::kStageStep, j >= 2 ? 1u : 0u);
-      mma_commit(sm.bar(C::kBarKvEmpty + stage));
-      ++kv_it;
-      if (j + 2 >= m.n) mma_commit(sm.bar(C::kBarODone + w));
-      if (j + 2 < m.n) {
-        ok = issue_s<D>(sm, ds, tmem, qb, w, kv_it, wd);
-        if (ok && j + 2 == m.n - 1) mma_commit(sm.bar(C::kBarQEmpty + qb));
+    if (w >= n) {
+      mbar_arrive(q_empty);  // this group has no slot in the row
+    } else {
+      ok = issue_s<D>(sm, ds, tmem, qb, w, kv, wd);
+      if (ok && w + 2 >= n) mma_commit(q_empty);
+      for (int j = w; j < n && ok; j += 2) {
+        if (!mbar_wait(sm.bar(C::kBarPFull + w), pc & 1u, wd, kSitePFull)) {
+          ok = false;
+          break;
+        }
+        ++pc;
+        tc_fence_after();
+        const int stage = (int)(kv % C::stages(w));
+        if (!mbar_wait(sm.bar(C::bar_full(w) + stage), (kv / C::stages(w)) & 1u, wd, kSiteKvFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        mma_pv<D>(tmem + col_o(w), tmem + col_s(w),
+                  ds.v0 + (uint64_t)stage * MmaDesc<D>::kStageStep, j >= 2 ? 1u : 0u);
+        mma_commit(sm.bar(C::bar_empty(w) + stage));
+        ++kv;
+        if (j + 2 >= n) {
+          mma_commit(sm.bar(C::kBarODone + w));
+        } else {
+          ok = issue_s<D>(sm, ds, tmem, qb, w, kv, wd);
+          if (ok && j + 4 >= n) mma_commit(q_empty);
+        }
       }
     }
     ++q_it;
   }
-  // Drain: every MMA issued so far has completed once this arrives.
+  // Drain: every MMA this thread issued has completed once its commit arrives.
   mma_commit(sm.bar(C::kBarDrain));
   drain_wait(sm.bar(C::kBarDrain), 0, wd);
 }
@@ -365,6 +412,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   const uint32_t s_addr = tmem + tl + col_s(w);
   const int qi = rloc / p.qu;
   const bool submask = (p.rq * p.rk) > 1;
+  const int ku_shift = p.ku == 32 ? 0 : (p.ku == 64 ? 1 : 2);  // log2(ku / 32)
   const uint32_t my_bits_mask = (1u << p.rk) - 1u;
   const float sl2 = p.scale_log2;
   uint32_t sc = 0, oc = 0, xc = 0;
@@ -392,10 +440,11 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       tmem_ld32_at<96>(s_addr + 96, v);
       tmem_wait_ld();
       if (submask) {
+        // 32-column chunk c lies in k-unit c >> ku_shift; a warp's rows share
+        // one q-unit, so the branch is warp-uniform.
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const int unit = (c * 32) / p.ku;
-          if (!((bits >> unit) & 1u)) {
+          if (!((bits >> (c >> ku_shift)) & 1u)) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[c * 32 + e] = __float_as_uint(-INFINITY);
           }
@@ -485,15 +534,15 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     const size_t orow = (size_t)m.bh * p.Nq + (size_t)m.qt * 128 + rloc;
     uint4* optr = reinterpret_cast<uint4*>(p.O + orow * D);
 #pragma unroll
-    for (int c = 0; c < D / 64; ++c) {
-      const int col0 = w * (D / 2) + c * 32;
-      uint32_t a[32], bb[32];
-      if (nA > 0) tmem_ld32(tmem + tl + col_o(0) + col0, a);
-      if (nB > 0) tmem_ld32(tmem + tl + col_o(1) + col0, bb);
+    for (int c = 0; c < D / 32; ++c) {  // this group's half of the columns, 16 at a time
+      const int col0 = w * (D / 2) + c * 16;
+      uint32_t a[16], bb[16];
+      if (nA > 0) tmem_ld16(tmem + tl + col_o(0) + col0, a);
+      if (nB > 0) tmem_ld16(tmem + tl + col_o(1) + col0, bb);
       tmem_wait_ld();
-      uint32_t pk[16];
+      uint32_t pk[8];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
+      for (int e = 0; e < 8; ++e) {
         float o0 = 0.f, o1 = 0.f;
         if (nA > 0) {
           o0 = __uint_as_float(a[2 * e]) * fA;
@@ -505,9 +554,8 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         }
         pk[e] = pack_bf16x2(o0 * inv, o1 * inv);
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        optr[col0 / 8 + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      optr[col0 / 8] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      optr[col0 / 8 + 1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
     }
     if (w == 0) p.LSE[orow] = (L > 0.f) ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
     tc_fence_before();
@@ -533,17 +581,21 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
     if (sm.base & 1023u) record_failure(wd, -4, 0);  // layout assumption violated
     for (int i = 0; i < 2; ++i) {
       mbar_init(sm.bar(C::kBarQFull + i), 1);
-      mbar_init(sm.bar(C::kBarQEmpty + i), 1);
+      mbar_init(sm.bar(C::kBarQEmpty + i), 2);  // one arrival per MMA thread
       mbar_init(sm.bar(C::kBarSFull + i), 1);
       mbar_init(sm.bar(C::kBarPFull + i), 128);
       mbar_init(sm.bar(C::kBarODone + i), 1);
       mbar_init(sm.bar(C::kBarXchg + i), 256);
     }
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(sm.bar(C::kBarKvFull + s), 1);
-      mbar_init(sm.bar(C::kBarKvEmpty + s), 1);
+    for (int s = 0; s < C::kStagesA; ++s) {
+      mbar_init(sm.bar(C::kBarKvFullA + s), 1);
+      mbar_init(sm.bar(C::kBarKvEmptyA + s), 1);
     }
-    mbar_init(sm.bar(C::kBarDrain), 1);
+    for (int s = 0; s < C::kStagesB; ++s) {
+      mbar_init(sm.bar(C::kBarKvFullB + s), 1);
+      mbar_init(sm.bar(C::kBarKvEmptyB + s), 1);
+    }
+    mbar_init(sm.bar(C::kBarDrain), 2);
     for (int i = 0; i < kSchedSlots; ++i) {
       mbar_init(sm.bar(C::kBarSchedFull + i), 1);
       mbar_init(sm.bar(C::kBarSchedEmpty + i), kSchedConsumers);
@@ -566,8 +618,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
   } else {
     regs_dec<kRegsControl>();
     if (lane == 0 && !*abort_flag) {
-      if (warp == 0) producer_role<D>(p, smem, sm, wd);
-      else if (warp == 1) mma_role<D>(p, smem, sm, tmem, wd);
+      if (warp == 0) producer_role<D>(p, smem, sm, wd, 0);
+      else if (warp == 1) mma_role<D>(p, smem, sm, tmem, wd, 0);
+      else if (warp == 2) producer_role<D>(p, smem, sm, wd, 1);
+      else mma_role<D>(p, smem, sm, tmem, wd, 1);
     }
   }
 
