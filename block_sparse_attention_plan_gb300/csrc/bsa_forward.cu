@@ -415,6 +415,50 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   const int ku_shift = p.ku == 32 ? 0 : (p.ku == 64 ? 1 : 2);  // log2(ku / 32)
   const uint32_t my_bits_mask = (1u << p.rk) - 1u;
   const float sl2 = p.scale_log2;
+  const uint64_t sl2x2 = f2_make(sl2, sl2);
+  uint32_t bits = 0xffffffffu;  // this row's sub-mask bits for the current slot
+  // S row of the current slot -> registers (masked columns -> -inf).
+  auto load_s = [&](uint32_t (&v)[128]) {
+    tmem_ld32_at<0>(s_addr + 0, v);
+    tmem_ld32_at<32>(s_addr + 32, v);
+    tmem_ld32_at<64>(s_addr + 64, v);
+    tmem_ld32_at<96>(s_addr + 96, v);
+    tmem_wait_ld();
+    if (submask) {
+      // 32-column chunk c lies in k-unit c >> ku_shift; a warp's rows share
+      // one q-unit, so the branch is warp-uniform.
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (!((bits >> (c >> ku_shift)) & 1u)) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[c * 32 + e] = __float_as_uint(-INFINITY);
+        }
+      }
+    }
+  };
+  // p = 2^(s*scale*log2e - m), packed in place as bf16 pairs into v[0..64);
+  // returns the row sum of p; with `mx` also returns the max of the raw row.
+  auto exp_pack = [&](uint32_t (&v)[128], float m, float* mx) -> float {
+    const float mb = (m == -INFINITY) ? 0.f : m;
+    const uint64_t nmbx2 = f2_make(-mb, -mb);
+    uint64_t acc2[2] = {0ull, 0ull};
+    float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int e = 0; e < 64; ++e) {
+      const float a0 = __uint_as_float(v[2 * e]), a1 = __uint_as_float(v[2 * e + 1]);
+      if (mx) mx4[e & 3] = fmax3(mx4[e & 3], a0, a1);
+      float x0, x1;
+      f2_split(ffma2(f2_make(a0, a1), sl2x2, nmbx2), x0, x1);
+      const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+      acc2[e & 1] = fadd2(acc2[e & 1], f2_make(p0, p1));
+      v[e] = pack_bf16x2(p0, p1);
+    }
+    if (mx) *mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+    float s0, s1, s2, s3;
+    f2_split(acc2[0], s0, s1);
+    f2_split(acc2[1], s2, s3);
+    return (s0 + s1) + (s2 + s3);
+  };
   uint32_t sc = 0, oc = 0, xc = 0;
   for (uint32_t t = 0;; ++t) {
     const int it = sched_take<D>(sm, smem, t, lane == 0, true, wd);
@@ -425,7 +469,6 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     bool ok = true;
     for (int k = 0; k < nw; ++k) {
       const int slot = m.s0 + 2 * k + w;
-      uint32_t bits = 0xffffffffu;
       if (submask) bits = (__ldg(p.slot_mask + slot) >> (qi * p.rk)) & my_bits_mask;
       if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarSFull + w), sc & 1u, wd, kSiteSFull))) {
         ok = false;
@@ -434,65 +477,49 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       ++sc;
       tc_fence_after();
       uint32_t v[128];
-      tmem_ld32_at<0>(s_addr + 0, v);
-      tmem_ld32_at<32>(s_addr + 32, v);
-      tmem_ld32_at<64>(s_addr + 64, v);
-      tmem_ld32_at<96>(s_addr + 96, v);
-      tmem_wait_ld();
-      if (submask) {
-        // 32-column chunk c lies in k-unit c >> ku_shift; a warp's rows share
-        // one q-unit, so the branch is warp-uniform.
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (!((bits >> (c >> ku_shift)) & 1u)) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[c * 32 + e] = __float_as_uint(-INFINITY);
+      load_s(v);
+      float factor = 1.f, sum;
+      if (!__any_sync(0xffffffffu, m_ref == -INFINITY)) {
+        // Fused pass: exponentials relative to the current reference max while
+        // the slot's own max is tracked alongside (it no longer gates them).
+        float mxr;
+        sum = exp_pack(v, m_ref, &mxr);
+        const float m_new = fmaxf(m_ref, mxr * sl2);
+        const bool grow = m_new > m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, grow)) {
+          // Rare: the max grew past the threshold; redo the slot against it.
+          if (grow) {
+            factor = ex2_approx(m_ref - m_new);
+            m_ref = m_new;
           }
+          load_s(v);
+          sum = exp_pack(v, m_ref, nullptr);
         }
-      }
-      // row max: four independent chains of three-input max
-      float mx4[4];
+      } else {
+        // First slot with a finite score for some row of the warp: max first.
+        float mx4[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) mx4[c] = __uint_as_float(v[c]);
+        for (int c = 0; c < 4; ++c) mx4[c] = __uint_as_float(v[c]);
 #pragma unroll
-      for (int e = 4; e < 128; e += 8) {
+        for (int e = 4; e < 128; e += 8) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          mx4[c] = fmax3(mx4[c], __uint_as_float(v[e + 2 * c]), __uint_as_float(v[e + 2 * c + 1]));
-      }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      const float m_new = fmaxf(m_ref, mx * sl2);
-      float factor = 1.f;
-      if (m_ref == -INFINITY) {
-        m_ref = m_new;  // nothing weighted accumulated yet: O holds zeros
-      } else if (m_new > m_ref + kRescaleThreshold) {
-        factor = ex2_approx(m_ref - m_new);
-        m_ref = m_new;
-      }
-      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // p = 2^(s*scale*log2e - m_ref), packed as bf16 pairs into the first
-      // 64 columns of this group's S region (keys 2c, 2c+1 -> column c).
-      const uint64_t sl2x2 = f2_make(sl2, sl2), nmbx2 = f2_make(-mb, -mb);
-      uint64_t acc2[2] = {0ull, 0ull};  // two packed partial sums (4 chains)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint64_t sv = f2_make(__uint_as_float(v[c * 32 + 2 * e]),
-                                      __uint_as_float(v[c * 32 + 2 * e + 1]));
-          float x0, x1;
-          f2_split(ffma2(sv, sl2x2, nmbx2), x0, x1);
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          acc2[e & 1] = fadd2(acc2[e & 1], f2_make(p0, p1));
-          pk[e] = pack_bf16x2(p0, p1);
+          for (int c = 0; c < 4; ++c)
+            mx4[c] = fmax3(mx4[c], __uint_as_float(v[e + 2 * c]), __uint_as_float(v[e + 2 * c + 1]));
         }
-        tmem_st16(s_addr + c * 16, pk);
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        const float m_new = fmaxf(m_ref, mx * sl2);
+        if (m_ref == -INFINITY) {
+          m_ref = m_new;  // nothing weighted accumulated yet: O holds zeros
+        } else if (m_new > m_ref + kRescaleThreshold) {
+          factor = ex2_approx(m_ref - m_new);
+          m_ref = m_new;
+        }
+        sum = exp_pack(v, m_ref, nullptr);
       }
-      float s0, s1, s2, s3;
-      f2_split(acc2[0], s0, s1);
-      f2_split(acc2[1], s2, s3);
-      const float sum = (s0 + s1) + (s2 + s3);
+      // P = packed bf16 pairs into the first 64 columns of this group's S
+      // region (keys 2c, 2c+1 -> column c).
+      tmem_st32_at<0>(s_addr + 0, v);
+      tmem_st32_at<32>(s_addr + 32, v);
       if (__any_sync(0xffffffffu, factor != 1.f)) {
         const uint32_t o_addr = tmem + tl + col_o(w);
 #pragma unroll
@@ -508,7 +535,8 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       tmem_wait_st();
       l_run = l_run * factor + sum;
       tc_fence_before();
-      mbar_arrive(sm.bar(C::kBarPFull + w));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.bar(C::kBarPFull + w));  // one arrival per warp
     }
     if (!ok) break;
     // ------------------------------------------------------------ epilogue
@@ -520,7 +548,8 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     ml[w * 128 + rloc] = m_ref;
     ml[(2 + w) * 128 + rloc] = l_run;
     tc_fence_before();
-    mbar_arrive(sm.bar(C::kBarXchg + 0));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.bar(C::kBarXchg + 0));
     if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarXchg + 0), xc & 1u, wd, kSiteXchg))) break;
     tc_fence_after();
     const float mA = ml[rloc], mB = ml[128 + rloc];
@@ -559,7 +588,8 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     }
     if (w == 0) p.LSE[orow] = (L > 0.f) ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
     tc_fence_before();
-    mbar_arrive(sm.bar(C::kBarXchg + 1));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.bar(C::kBarXchg + 1));
     if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarXchg + 1), xc & 1u, wd, kSiteXchg))) break;
     ++xc;
   }
@@ -583,9 +613,9 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
       mbar_init(sm.bar(C::kBarQFull + i), 1);
       mbar_init(sm.bar(C::kBarQEmpty + i), 2);  // one arrival per MMA thread
       mbar_init(sm.bar(C::kBarSFull + i), 1);
-      mbar_init(sm.bar(C::kBarPFull + i), 128);
+      mbar_init(sm.bar(C::kBarPFull + i), 4);    // one arrival per softmax warp
       mbar_init(sm.bar(C::kBarODone + i), 1);
-      mbar_init(sm.bar(C::kBarXchg + i), 256);
+      mbar_init(sm.bar(C::kBarXchg + i), 8);     // one arrival per softmax warp of both groups
     }
     for (int s = 0; s < C::kStagesA; ++s) {
       mbar_init(sm.bar(C::kBarKvFullA + s), 1);
