@@ -29,7 +29,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kScanThreads = 1024;
-constexpr int kBatch = 4;  // 32-unit chunks whose mask loads are issued together
+constexpr int kBatch = 8;  // 32-unit chunks whose mask loads are issued together
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
@@ -37,36 +37,61 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-// Whether k-unit y is selected by any q-unit of q-tile qt of mask plane mbh
-// ([NQB][NKB] of one (b, h)).  `own` counts the logical blocks whose first
-// q-unit and first k-unit fall here (so every selected logical block is
-// counted exactly once over the whole plan).
-__device__ __forceinline__ int unit_union(const uint8_t* __restrict__ mbh, const PlanDev& p, int qt,
-                                          int y, int* own) {
-  const int kb = y / p.sk;
-  const bool first_k = (y % p.sk) == 0;
-  int u = 0, o = 0;
-  for (int i = 0; i < p.rq; ++i) {
-    const int x = qt * p.rq + i;
-    const int v = __ldg(mbh + (size_t)(x / p.sq) * p.NKB + kb) != 0;
-    u |= v;
-    o += (v && first_k && (x % p.sq) == 0);
-  }
-  *own = o;
-  return u;
-}
+// Mask bytes of kBatch consecutive 32-unit chunks (k-units y0 + c*32 + lane)
+// for the rq q-units of q-tile qt of mask plane mbh ([NQB][NKB] of one
+// (b, h)).  Every load of the batch is issued before any is used (fully
+// unrolled, predicated on rq <= 4), so a warp waits for one round trip per
+// batch instead of one per byte.
+struct UnitBatch {
+  int u[kBatch];    // k-unit selected by some q-unit of the tile
+  int own[kBatch];  // logical blocks first-owned here (see count kernel)
+};
 
-__device__ __forceinline__ int union_unit(const PlanDev& p, int b, int hk, int qt, int y) {
-  const int kb = y / p.sk;
-  int u = 0;
-  for (int hh = 0; hh < p.g; ++hh) {  // no early exit: the loads are independent
-    const uint8_t* mbh = p.mask + ((size_t)(b * p.H + hk * p.g + hh)) * p.NQB * p.NKB;
-    for (int i = 0; i < p.rq; ++i) {
+__device__ __forceinline__ UnitBatch unit_batch(const uint8_t* __restrict__ mbh, const PlanDev& p,
+                                                int qt, int y0, int lane) {
+  const int sk_sh = p.sk >> 1, sq_sh = p.sq >> 1;  // sk, sq are 1 or 2
+  uint8_t v[kBatch][4];
+#pragma unroll
+  for (int c = 0; c < kBatch; ++c) {
+    const int y = y0 + c * 32 + lane;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
       const int x = qt * p.rq + i;
-      u |= __ldg(mbh + (size_t)(x / p.sq) * p.NKB + kb);
+      v[c][i] = (i < p.rq && y < p.NKU) ? __ldg(mbh + (size_t)(x >> sq_sh) * p.NKB + (y >> sk_sh))
+                                        : (uint8_t)0;
     }
   }
-  return u != 0;
+  UnitBatch r;
+#pragma unroll
+  for (int c = 0; c < kBatch; ++c) {
+    const int y = y0 + c * 32 + lane;
+    const bool first_k = (y & sk_sh) == 0;
+    int u = 0, o = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int x = qt * p.rq + i;
+      const int sel = v[c][i] != 0;
+      u |= sel;
+      o += (sel && first_k && (x & sq_sh) == 0);
+    }
+    r.u[c] = u;
+    r.own[c] = o;
+  }
+  return r;
+}
+
+// GQA union over the g query heads of K/V head hk: for each head the same
+// hoisted batch of loads, OR-ed together.
+__device__ __forceinline__ void union_batch(const PlanDev& p, int b, int hk, int qt, int y0,
+                                            int lane, int (&u)[kBatch]) {
+#pragma unroll
+  for (int c = 0; c < kBatch; ++c) u[c] = 0;
+  for (int hh = 0; hh < p.g; ++hh) {
+    const uint8_t* mbh = p.mask + ((size_t)(b * p.H + hk * p.g + hh)) * p.NQB * p.NKB;
+    const UnitBatch r = unit_batch(mbh, p, qt, y0, lane);
+#pragma unroll
+    for (int c = 0; c < kBatch; ++c) u[c] |= r.u[c];
+  }
 }
 
 __global__ void __launch_bounds__(kThreads) plan_count_kernel(const PlanDev p) {
@@ -79,18 +104,11 @@ __global__ void __launch_bounds__(kThreads) plan_count_kernel(const PlanDev p) {
     const uint8_t* mbh = p.mask + (size_t)bh * p.NQB * p.NKB;
     int cnt = 0, own = 0;
     for (int y0 = 0; y0 < p.NKU; y0 += 32 * kBatch) {
-      int u[kBatch], o[kBatch];
-#pragma unroll
-      for (int c = 0; c < kBatch; ++c) {  // all loads of the batch first
-        const int y = y0 + c * 32 + lane;
-        u[c] = 0;
-        o[c] = 0;
-        if (y < p.NKU) u[c] = unit_union(mbh, p, qt, y, &o[c]);
-      }
+      const UnitBatch r = unit_batch(mbh, p, qt, y0, lane);
 #pragma unroll
       for (int c = 0; c < kBatch; ++c) {
-        cnt += __popc(__ballot_sync(0xffffffffu, u[c]));
-        own += o[c];
+        cnt += __popc(__ballot_sync(0xffffffffu, r.u[c]));
+        own += r.own[c];
       }
     }
     for (int s = 16; s > 0; s >>= 1) own += __shfl_xor_sync(0xffffffffu, own, s);
@@ -106,11 +124,7 @@ __global__ void __launch_bounds__(kThreads) plan_count_kernel(const PlanDev p) {
     int cnt = 0;
     for (int y0 = 0; y0 < p.NKU; y0 += 32 * kBatch) {
       int u[kBatch];
-#pragma unroll
-      for (int c = 0; c < kBatch; ++c) {
-        const int y = y0 + c * 32 + lane;
-        u[c] = (y < p.NKU) ? union_unit(p, b, hk, qt, y) : 0;
-      }
+      union_batch(p, b, hk, qt, y0, lane, u);
 #pragma unroll
       for (int c = 0; c < kBatch; ++c) cnt += __popc(__ballot_sync(0xffffffffu, u[c]));
     }
@@ -148,22 +162,35 @@ __device__ T block_exclusive_scan(T v, T* excl_out, T* warp_sums) {
 }
 
 // Exclusive prefix sum of in[0..n) into out[0..n] (out[n] = total) by one
-// block: each thread sums a contiguous run, the runs are scanned once, then
-// each thread writes its run's prefixes.
+// block: each thread sums a contiguous run (loads issued kRun at a time), the
+// run sums are scanned once, then each thread writes its run's prefixes.
+constexpr int kRun = 16;
 template <typename TIn>
 __device__ long long block_scan_array(const TIn* in, int32_t* out, int n, long long* wsum) {
   const int per = (n + blockDim.x - 1) / blockDim.x;
   const int i0 = threadIdx.x * per;
   const int i1 = min(i0 + per, n);
   long long local = 0;
-  for (int i = i0; i < i1; ++i) local += (long long)in[i];
+  for (int b = i0; b < i1; b += kRun) {
+    TIn t[kRun];
+#pragma unroll
+    for (int k = 0; k < kRun; ++k) t[k] = (b + k < i1) ? in[b + k] : TIn(0);
+#pragma unroll
+    for (int k = 0; k < kRun; ++k) local += (long long)t[k];
+  }
   long long ex;
   const long long total = block_exclusive_scan<long long>(local, &ex, wsum);
   if (out) {
     long long run = ex;
-    for (int i = i0; i < i1; ++i) {
-      out[i] = (int32_t)run;
-      run += (long long)in[i];
+    for (int b = i0; b < i1; b += kRun) {
+      TIn t[kRun];
+#pragma unroll
+      for (int k = 0; k < kRun; ++k) t[k] = (b + k < i1) ? in[b + k] : TIn(0);
+#pragma unroll
+      for (int k = 0; k < kRun; ++k) {
+        if (b + k < i1) out[b + k] = (int32_t)run;
+        run += (long long)t[k];
+      }
     }
     if (threadIdx.x == 0) out[n] = (int32_t)total;
   }
@@ -208,17 +235,11 @@ __device__ void fill_row(const PlanDev& p, int r, int lane) {
   int32_t* out = p.slot_ku + (size_t)s0 * p.rk;
   int pos = 0;
   for (int y0 = 0; y0 < p.NKU; y0 += 32 * kBatch) {
-    int u[kBatch];
-#pragma unroll
-    for (int c = 0; c < kBatch; ++c) {
-      const int y = y0 + c * 32 + lane;
-      int o;
-      u[c] = (y < p.NKU) ? unit_union(mbh, p, qt, y, &o) : 0;
-    }
+    const UnitBatch r = unit_batch(mbh, p, qt, y0, lane);
 #pragma unroll
     for (int c = 0; c < kBatch; ++c) {  // ascending k-units: chunk by chunk
-      const uint32_t bal = __ballot_sync(0xffffffffu, u[c]);
-      if (u[c]) {
+      const uint32_t bal = __ballot_sync(0xffffffffu, r.u[c]);
+      if (r.u[c]) {
         const int idx = pos + __popc(bal & lanemask_lt());
         if (idx < cap) out[idx] = y0 + c * 32 + lane;
       }
@@ -233,10 +254,10 @@ __device__ void fill_row(const PlanDev& p, int r, int lane) {
     for (int j = 0; j < p.rk; ++j) {
       const int y = out[s * p.rk + j];
       if (y < 0) continue;
-      const int kb = y / p.sk;
+      const int kb = y >> (p.sk >> 1);
       for (int ii = 0; ii < p.rq; ++ii) {
         const int x = qt * p.rq + ii;
-        if (__ldg(mbh + (size_t)(x / p.sq) * p.NKB + kb) != 0) bits |= 1u << (ii * p.rk + j);
+        if (__ldg(mbh + (size_t)(x >> (p.sq >> 1)) * p.NKB + kb) != 0) bits |= 1u << (ii * p.rk + j);
       }
     }
     p.slot_mask[s0 + s] = bits;
@@ -251,11 +272,7 @@ __device__ void fill_union_row(const PlanDev& p, int ur, int lane) {
   int pos = 0;
   for (int y0 = 0; y0 < p.NKU; y0 += 32 * kBatch) {
     int u[kBatch];
-#pragma unroll
-    for (int c = 0; c < kBatch; ++c) {
-      const int y = y0 + c * 32 + lane;
-      u[c] = (y < p.NKU) ? union_unit(p, b, hk, qt, y) : 0;
-    }
+    union_batch(p, b, hk, qt, y0, lane, u);
 #pragma unroll
     for (int c = 0; c < kBatch; ++c) {
       const uint32_t bal = __ballot_sync(0xffffffffu, u[c]);
@@ -268,7 +285,6 @@ __device__ void fill_union_row(const PlanDev& p, int ur, int lane) {
   }
 }
 
-// Stable counting sort of one K/V-head group's rows by slots descending.
 __device__ void order_group(const PlanDev& p, int gi, int* start_s) {
   __shared__ int wsum[32];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
