@@ -17,8 +17,8 @@
 //               work items and loads each row's Q tile.  A slot of 128 keys is
 //               gathered as rk boxes of ku rows (ku = 128 / rk).
 //   warps 1, 3  MMA issuers (one thread each, one per softmax group):
-//               tcgen05.mma S = Q K^T (both operands in shared memory) and
-//               O += P V (P read from tensor memory).
+//               tcgen05.mma S = Q K^T and O += P V, all operands in shared
+//               memory, accumulators in tensor memory.
 //   warp 2      also owns the tensor-memory allocation (512 columns).
 //   warps 4-7   softmax warpgroup A: even slots of the row.
 //   warps 8-11  softmax warpgroup B: odd slots of the row.
@@ -27,8 +27,10 @@
 // softmax; the two partial results are merged in the epilogue.
 //
 // Tensor memory (512 fp32 columns x 128 lanes; lane = q-tile row):
-//   [0,128) S_A (P_A packed bf16 in [0,64))   [128,256) S_B / P_B
-//   [256,256+d) O_A                           [384,384+d) O_B
+//   [0,128) S_A   [128,256) S_B   [256,256+d) O_A   [384,384+d) O_B
+// P (bf16) goes through shared memory, one 32 KB buffer per softmax group, so
+// a group's S buffer is free as soon as its softmax has read it: the MMA
+// thread computes the next S while the softmax is still computing P.
 //
 // Every wait is bounded (watchdog): on expiry the CTA records
 // BSA_ERR_TIMEOUT in the plan's status word, lets its in-flight copies and
@@ -48,8 +50,8 @@ constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
 // Register split: 384 threads x 168 at launch = 64,512 registers =
 // 128 x kRegsControl (warps 0-3) + 256 x kRegsSoftmax (warps 4-11).
-constexpr int kRegsControl = 64;
-constexpr int kRegsSoftmax = 216;
+constexpr int kRegsControl = 72;
+constexpr int kRegsSoftmax = 208;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split");
 __device__ __forceinline__ uint32_t col_s(int w) { return (uint32_t)(w * 128); }
 __device__ __forceinline__ uint32_t col_o(int w) { return (uint32_t)(256 + w * 128); }
@@ -65,13 +67,15 @@ struct Cfg {
   static constexpr int kTileBytes = 128 * D * 2;   // 128 rows x d bf16
   static constexpr int kChunks = D / 64;           // 64-column (128-byte) swizzle blocks
   static constexpr int kChunkBytes = 128 * 128;    // one block of 128 rows
+  static constexpr int kPBytes = 128 * 128 * 2;    // P: 128 rows x 128 keys bf16
   // One K/V ring per softmax group (group A takes the even slots of a row,
   // group B the odd ones); each ring is consumed in order by one MMA thread.
-  static constexpr int kStagesA = (D == 128) ? 3 : 6;
-  static constexpr int kStagesB = (D == 128) ? 3 : 6;
+  static constexpr int kStagesA = (D == 128) ? 2 : 4;
+  static constexpr int kStagesB = (D == 128) ? 2 : 4;
   static constexpr int kQBufs = (D == 128) ? 1 : 2;  // Q tile buffers
   static constexpr int kOffQ = 0;
-  static constexpr int kOffRingA = kQBufs * kTileBytes;
+  static constexpr int kOffP = kQBufs * kTileBytes;           // P of group A, then B
+  static constexpr int kOffRingA = kOffP + 2 * kPBytes;
   static constexpr int kOffRingB = kOffRingA + kStagesA * kTileBytes;
   static constexpr int kOffBar = kOffRingB + kStagesB * kTileBytes;
   // barriers
@@ -81,8 +85,10 @@ struct Cfg {
   static constexpr int kBarKvFullB = kBarKvEmptyA + kStagesA;
   static constexpr int kBarKvEmptyB = kBarKvFullB + kStagesB;
   static constexpr int kBarSFull = kBarKvEmptyB + kStagesB;
-  static constexpr int kBarPFull = kBarSFull + 2;
-  static constexpr int kBarODone = kBarPFull + 2;
+  static constexpr int kBarSFree = kBarSFull + 2;
+  static constexpr int kBarPFull = kBarSFree + 2;
+  static constexpr int kBarPFree = kBarPFull + 2;
+  static constexpr int kBarODone = kBarPFree + 2;
   static constexpr int kBarXchg = kBarODone + 2;
   static constexpr int kBarDrain = kBarXchg + 2;
   static constexpr int kBarSchedFull = kBarDrain + 1;
@@ -148,6 +154,7 @@ struct Smem {
   uint32_t base;
   __device__ __forceinline__ uint32_t bar(int i) const { return base + C::kOffBar + 8u * (uint32_t)i; }
   __device__ __forceinline__ uint32_t q(int qb) const { return base + C::kOffQ + qb * C::kTileBytes; }
+  __device__ __forceinline__ uint32_t pbuf(int w) const { return base + C::kOffP + w * C::kPBytes; }
   __device__ __forceinline__ uint32_t stage(int w, int s) const {
     return base + C::ring(w) + (uint32_t)s * C::kTileBytes;
   }
@@ -258,11 +265,12 @@ __device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, co
                     sm.bar(C::kBarQFull + qb), pol_q);
       ++q_it;
     }
-    // Ring w in consumption order: K_w, then V_j, K_{j+2} for j = w, w+2, ...
+    // Ring w in consumption order: K_w, then K_{j+2}, V_j for j = w, w+2, ...
+    // (the MMA thread computes S of slot j+2 while slot j's softmax runs).
     if (w < m.n) ok = load_kv_tile<D>(p, sm, &p.tmK, m, w, kv_it, pol_kv, wd);
     for (int j = w; j < m.n && ok; j += 2) {
-      ok = load_kv_tile<D>(p, sm, &p.tmV, m, j, kv_it, pol_kv, wd);
-      if (ok && j + 2 < m.n) ok = load_kv_tile<D>(p, sm, &p.tmK, m, j + 2, kv_it, pol_kv, wd);
+      if (j + 2 < m.n) ok = load_kv_tile<D>(p, sm, &p.tmK, m, j + 2, kv_it, pol_kv, wd);
+      if (ok) ok = load_kv_tile<D>(p, sm, &p.tmV, m, j, kv_it, pol_kv, wd);
     }
   }
   if (*wd.abort_flag) {
@@ -306,48 +314,69 @@ __device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint64_t adesc, uint64_t
 }
 
 // O_w (+)= P_w V: M=128, N=d, K=16 keys per instruction, 8 instructions.
-// P columns [8kk, 8kk+8) hold keys [16kk, 16kk+16) as bf16 pairs; V rows
-// [16kk, 16kk+16) start 2048 bytes apart (MN-major: LBO = next 64 columns).
+// P (shared memory, K-major 128B swizzle like Q) advances like Q does in
+// mma_qk; V rows [16kk, 16kk+16) start 2048 bytes apart (MN-major: LBO = next
+// 64 columns).
 template <int D>
-__device__ __forceinline__ void mma_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t vdesc,
+__device__ __forceinline__ void mma_pv(uint32_t o_tmem, uint64_t pdesc, uint64_t vdesc,
                                        uint32_t acc) {
   constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk)
-    mma_ts(o_tmem, p_tmem + 8 * kk, vdesc + (uint64_t)(kk * (2048 >> 4)), kIdescPV,
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint64_t off = (uint64_t)(((kk / 4) * (128 * 128) + (kk % 4) * 32) >> 4);
+    mma_ss(o_tmem, pdesc + off, vdesc + (uint64_t)(kk * (2048 >> 4)), kIdescPV,
            (acc || kk > 0) ? 1u : 0u);
+  }
 }
 
+// State of one MMA issuer (softmax group w).
 template <int D>
-__device__ __forceinline__ bool issue_s(const Smem<D>& sm, const MmaDesc<D>& ds, uint32_t tmem,
-                                        int qb, int w, uint32_t& kv, const Watchdog& wd) {
+struct MmaState {
+  MmaDesc<D> ds;
+  uint64_t pdesc;    // K-major SW128 descriptor of this group's P buffer
+  uint32_t kv = 0;   // tiles consumed from ring w
+  uint32_t ns = 0;   // S tiles issued (the n-th waits for s_free completion n-1)
+  uint32_t pc = 0;   // P tiles consumed
+};
+
+// S_w = Q K^T into this group's S buffer, once the softmax has read the
+// previous S out of it.
+template <int D>
+__device__ __forceinline__ bool issue_s(const Smem<D>& sm, MmaState<D>& st, uint32_t tmem, int qb,
+                                        int w, const Watchdog& wd) {
   using C = Cfg<D>;
-  const int stage = (int)(kv % C::stages(w));
-  if (!mbar_wait(sm.bar(C::bar_full(w) + stage), (kv / C::stages(w)) & 1u, wd, kSiteKvFull))
+  if (st.ns > 0 &&
+      !mbar_wait(sm.bar(C::kBarSFree + w), (st.ns - 1) & 1u, wd, kSiteSFull))
+    return false;
+  const int stage = (int)(st.kv % C::stages(w));
+  if (!mbar_wait(sm.bar(C::bar_full(w) + stage), (st.kv / C::stages(w)) & 1u, wd, kSiteKvFull))
     return false;
   tc_fence_after();
-  mma_qk<D>(tmem + col_s(w), ds.q[qb], ds.kv0 + (uint64_t)stage * MmaDesc<D>::kStageStep);
+  mma_qk<D>(tmem + col_s(w), st.ds.q[qb], st.ds.kv0 + (uint64_t)stage * MmaDesc<D>::kStageStep);
   mma_commit(sm.bar(C::bar_empty(w) + stage));
   mma_commit(sm.bar(C::kBarSFull + w));
-  ++kv;
+  ++st.kv;
+  ++st.ns;
   return true;
 }
 
 // MMA issuer of softmax group w (slots j = w, w+2, ... of each row), fed by
 // ring w.  Two of these run in separate warps: tcgen05.mma issue is close to
 // synchronous with execution, so while one thread is held issuing, the other
-// does its barrier waits and has its next group of MMAs ready, keeping the
-// tensor pipe fed.
+// does its barrier waits and has its next group of MMAs ready.  Within a
+// group, S of slot j+2 is issued before P V of slot j, so it runs while slot
+// j's softmax is still computing P.
 template <int D>
 __device__ __noinline__ void mma_role(const FwdParams& p, const uint8_t* smem, const Smem<D> sm,
                                       uint32_t tmem, const Watchdog wd, int w) {
   using C = Cfg<D>;
-  MmaDesc<D> ds;
-  ds.q[0] = smem_desc_sw128(sm.q(0), 16, 1024);
-  ds.q[1] = smem_desc_sw128(sm.q(C::kQBufs - 1), 16, 1024);
-  ds.kv0 = smem_desc_sw128(sm.stage(w, 0), 16, 1024);
-  ds.v0 = smem_desc_sw128(sm.stage(w, 0), C::kChunkBytes, 1024);
-  uint32_t q_it = 0, kv = 0, pc = 0;
+  MmaState<D> st;
+  st.ds.q[0] = smem_desc_sw128(sm.q(0), 16, 1024);
+  st.ds.q[1] = smem_desc_sw128(sm.q(C::kQBufs - 1), 16, 1024);
+  st.ds.kv0 = smem_desc_sw128(sm.stage(w, 0), 16, 1024);
+  st.ds.v0 = smem_desc_sw128(sm.stage(w, 0), C::kChunkBytes, 1024);
+  st.pdesc = smem_desc_sw128(sm.pbuf(w), 16, 1024);
+  uint32_t q_it = 0;
   bool ok = true;
   for (uint32_t t = 0; ok; ++t) {
     const int it = sched_take<D>(sm, smem, t, true, false, wd);
@@ -364,31 +393,33 @@ __device__ __noinline__ void mma_role(const FwdParams& p, const uint8_t* smem, c
     if (w >= n) {
       mbar_arrive(q_empty);  // this group has no slot in the row
     } else {
-      ok = issue_s<D>(sm, ds, tmem, qb, w, kv, wd);
+      ok = issue_s<D>(sm, st, tmem, qb, w, wd);
       if (ok && w + 2 >= n) mma_commit(q_empty);
       for (int j = w; j < n && ok; j += 2) {
-        if (!mbar_wait(sm.bar(C::kBarPFull + w), pc & 1u, wd, kSitePFull)) {
-          ok = false;
-          break;
-        }
-        ++pc;
-        tc_fence_after();
-        const int stage = (int)(kv % C::stages(w));
-        if (!mbar_wait(sm.bar(C::bar_full(w) + stage), (kv / C::stages(w)) & 1u, wd, kSiteKvFull)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        mma_pv<D>(tmem + col_o(w), tmem + col_s(w),
-                  ds.v0 + (uint64_t)stage * MmaDesc<D>::kStageStep, j >= 2 ? 1u : 0u);
-        mma_commit(sm.bar(C::bar_empty(w) + stage));
-        ++kv;
-        if (j + 2 >= n) {
-          mma_commit(sm.bar(C::kBarODone + w));
-        } else {
-          ok = issue_s<D>(sm, ds, tmem, qb, w, kv, wd);
+        if (j + 2 < n) {
+          ok = issue_s<D>(sm, st, tmem, qb, w, wd);
           if (ok && j + 4 >= n) mma_commit(q_empty);
+          if (!ok) break;
         }
+        if (!mbar_wait(sm.bar(C::kBarPFull + w), st.pc & 1u, wd, kSitePFull)) {
+          ok = false;
+          break;
+        }
+        ++st.pc;
+        tc_fence_after();
+        const int stage = (int)(st.kv % C::stages(w));
+        if (!mbar_wait(sm.bar(C::bar_full(w) + stage), (st.kv / C::stages(w)) & 1u, wd,
+                       kSiteKvFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        mma_pv<D>(tmem + col_o(w), st.pdesc, st.ds.v0 + (uint64_t)stage * MmaDesc<D>::kStageStep,
+                  j >= 2 ? 1u : 0u);
+        mma_commit(sm.bar(C::bar_empty(w) + stage));
+        mma_commit(sm.bar(C::kBarPFree + w));
+        ++st.kv;
+        if (j + 2 >= n) mma_commit(sm.bar(C::kBarODone + w));
       }
     }
     ++q_it;
@@ -459,7 +490,8 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     f2_split(acc2[1], s2, s3);
     return (s0 + s1) + (s2 + s3);
   };
-  uint32_t sc = 0, oc = 0, xc = 0;
+  uint32_t sc = 0, oc = 0, xc = 0, np = 0;
+  const uint32_t p_row = sm.pbuf(w) + (uint32_t)rloc * 128;  // this row in P chunk 0
   for (uint32_t t = 0;; ++t) {
     const int it = sched_take<D>(sm, smem, t, lane == 0, true, wd);
     if (it < 0) break;
@@ -478,48 +510,50 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       tc_fence_after();
       uint32_t v[128];
       load_s(v);
-      float factor = 1.f, sum;
-      if (!__any_sync(0xffffffffu, m_ref == -INFINITY)) {
-        // Fused pass: exponentials relative to the current reference max while
-        // the slot's own max is tracked alongside (it no longer gates them).
-        float mxr;
-        sum = exp_pack(v, m_ref, &mxr);
-        const float m_new = fmaxf(m_ref, mxr * sl2);
-        const bool grow = m_new > m_ref + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, grow)) {
-          // Rare: the max grew past the threshold; redo the slot against it.
-          if (grow) {
-            factor = ex2_approx(m_ref - m_new);
-            m_ref = m_new;
-          }
-          load_s(v);
-          sum = exp_pack(v, m_ref, nullptr);
-        }
-      } else {
-        // First slot with a finite score for some row of the warp: max first.
-        float mx4[4];
+      // The S row is in registers: hand the S buffer back for the next S MMA.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.bar(C::kBarSFree + w));
+      // Row max, then exponentials against the reference max.
+      float mx4[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) mx4[c] = __uint_as_float(v[c]);
+      for (int c = 0; c < 4; ++c) mx4[c] = __uint_as_float(v[c]);
 #pragma unroll
-        for (int e = 4; e < 128; e += 8) {
+      for (int e = 4; e < 128; e += 8) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            mx4[c] = fmax3(mx4[c], __uint_as_float(v[e + 2 * c]), __uint_as_float(v[e + 2 * c + 1]));
-        }
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        const float m_new = fmaxf(m_ref, mx * sl2);
-        if (m_ref == -INFINITY) {
-          m_ref = m_new;  // nothing weighted accumulated yet: O holds zeros
-        } else if (m_new > m_ref + kRescaleThreshold) {
-          factor = ex2_approx(m_ref - m_new);
-          m_ref = m_new;
-        }
-        sum = exp_pack(v, m_ref, nullptr);
+        for (int c = 0; c < 4; ++c)
+          mx4[c] = fmax3(mx4[c], __uint_as_float(v[e + 2 * c]), __uint_as_float(v[e + 2 * c + 1]));
       }
-      // P = packed bf16 pairs into the first 64 columns of this group's S
-      // region (keys 2c, 2c+1 -> column c).
-      tmem_st32_at<0>(s_addr + 0, v);
-      tmem_st32_at<32>(s_addr + 32, v);
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      const float m_new = fmaxf(m_ref, mx * sl2);
+      float factor = 1.f;
+      if (m_ref == -INFINITY) {
+        m_ref = m_new;  // nothing weighted accumulated yet: O holds zeros
+      } else if (m_new > m_ref + kRescaleThreshold) {
+        factor = ex2_approx(m_ref - m_new);
+        m_ref = m_new;
+      }
+      const float sum = exp_pack(v, m_ref, nullptr);
+      // The previous P V of this group must be done with the P buffer (and
+      // with O) before P is overwritten or O rescaled.
+      if (np > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + w), (np - 1) & 1u, wd,
+                                                       kSitePFull))) {
+        ok = false;
+        break;
+      }
+      ++np;
+      // P -> shared memory in the K-major 128B-swizzled layout the MMA reads:
+      // row r, keys [64c + 8u, +8) at chunk c, 16-byte unit u ^ (r % 8).
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t addr = p_row + c * (128 * 128) + ((u ^ (rloc & 7)) << 4);
+          st_shared_v4(addr, v[c * 32 + u * 4], v[c * 32 + u * 4 + 1], v[c * 32 + u * 4 + 2],
+                       v[c * 32 + u * 4 + 3]);
+        }
+      }
+      fence_proxy_async_smem();  // make the stores visible to the tensor core
       if (__any_sync(0xffffffffu, factor != 1.f)) {
         const uint32_t o_addr = tmem + tl + col_o(w);
 #pragma unroll
@@ -613,7 +647,9 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
       mbar_init(sm.bar(C::kBarQFull + i), 1);
       mbar_init(sm.bar(C::kBarQEmpty + i), 2);  // one arrival per MMA thread
       mbar_init(sm.bar(C::kBarSFull + i), 1);
+      mbar_init(sm.bar(C::kBarSFree + i), 4);    // one arrival per softmax warp
       mbar_init(sm.bar(C::kBarPFull + i), 4);    // one arrival per softmax warp
+      mbar_init(sm.bar(C::kBarPFree + i), 1);
       mbar_init(sm.bar(C::kBarODone + i), 1);
       mbar_init(sm.bar(C::kBarXchg + i), 8);     // one arrival per softmax warp of both groups
     }
