@@ -185,10 +185,25 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 }
 
 // ------------------------------------------------------------------ producer
+// K/V units of one slot as the plan lists them (rk <= 4 entries, -1 = padding).
+// The producer reads them a slot ahead, so the global-load latency overlaps
+// its stage waits instead of sitting between a stage freeing and its copy.
+struct SlotKeys {
+  int y[4];
+};
+__device__ __forceinline__ SlotKeys fetch_keys(const FwdParams& p, const Item& m, int j) {
+  SlotKeys k;
+  const int32_t* ent = p.slot_ku + (size_t)(m.s0 + j) * p.rk;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) k.y[u] = (u < p.rk) ? __ldg(ent + u) : -1;
+  return k;
+}
+
 template <int D>
 __device__ __forceinline__ bool load_kv_tile(const FwdParams& p, const Smem<D>& sm,
                                              const CUtensorMap* map, const Item& m, int j,
-                                             uint32_t (&kv_it)[2], uint64_t pol, const Watchdog& wd) {
+                                             const SlotKeys& keys, uint32_t (&kv_it)[2],
+                                             uint64_t pol, const Watchdog& wd) {
   using C = Cfg<D>;
   const int w = j & 1;  // ring of the softmax group that owns slot j
   const int nst = C::stages(w);
@@ -197,15 +212,16 @@ __device__ __forceinline__ bool load_kv_tile(const FwdParams& p, const Smem<D>& 
   if (!mbar_wait(sm.bar(C::bar_empty(w) + stage), ph ^ 1u, wd, kSiteKvEmpty)) return false;
   const uint32_t full = sm.bar(C::bar_full(w) + stage);
   mbar_arrive_expect_tx(full, C::kTileBytes);
-  const int32_t* ent = p.slot_ku + (size_t)(m.s0 + j) * p.rk;
-  int first = __ldg(ent);
+  int first = keys.y[0];
   if (first < 0 || first >= p.NKU) {
     record_status(p.control, -7, kSitePlanRange + 2);
     first = 0;
   }
   const uint32_t dst0 = sm.stage(w, stage);
-  for (int u = 0; u < p.rk; ++u) {
-    int y = __ldg(ent + u);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    if (u >= p.rk) break;
+    int y = keys.y[u];
     if (y < 0) {
       y = first;  // padding position: load real rows, the sub-mask hides them
     } else if (y >= p.NKU) {
@@ -267,10 +283,19 @@ __device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, co
     }
     // Ring w in consumption order: K_w, then K_{j+2}, V_j for j = w, w+2, ...
     // (the MMA thread computes S of slot j+2 while slot j's softmax runs).
-    if (w < m.n) ok = load_kv_tile<D>(p, sm, &p.tmK, m, w, kv_it, pol_kv, wd);
+    // V_j reuses the units read for K_j; slot j+4's are read before the waits
+    // of K_{j+2} and V_j.
+    if (w >= m.n) continue;
+    SlotKeys kc = fetch_keys(p, m, w), kn = kc;
+    if (w + 2 < m.n) kn = fetch_keys(p, m, w + 2);
+    ok = load_kv_tile<D>(p, sm, &p.tmK, m, w, kc, kv_it, pol_kv, wd);
     for (int j = w; j < m.n && ok; j += 2) {
-      if (j + 2 < m.n) ok = load_kv_tile<D>(p, sm, &p.tmK, m, j + 2, kv_it, pol_kv, wd);
-      if (ok) ok = load_kv_tile<D>(p, sm, &p.tmV, m, j, kv_it, pol_kv, wd);
+      SlotKeys kn2 = kn;
+      if (j + 4 < m.n) kn2 = fetch_keys(p, m, j + 4);
+      if (j + 2 < m.n) ok = load_kv_tile<D>(p, sm, &p.tmK, m, j + 2, kn, kv_it, pol_kv, wd);
+      if (ok) ok = load_kv_tile<D>(p, sm, &p.tmV, m, j, kc, kv_it, pol_kv, wd);
+      kc = kn;
+      kn = kn2;
     }
   }
   if (*wd.abort_flag) {
@@ -517,9 +542,9 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       // Row max, then exponentials against the reference max.
       float mx4[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) mx4[c] = __uint_as_float(v[c]);
+      for (int c = 0; c < 4; ++c) mx4[c] = fmaxf(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]));
 #pragma unroll
-      for (int e = 4; e < 128; e += 8) {
+      for (int e = 8; e < 128; e += 8) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           mx4[c] = fmax3(mx4[c], __uint_as_float(v[e + 2 * c]), __uint_as_float(v[e + 2 * c + 1]));
