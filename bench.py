@@ -346,13 +346,17 @@ def run_gb300(args):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
                      "traffic": args.traffic if args.traffic is not None else _traffic(w.name),
-                     "kernel": "bsa_fwd_kernel<128>" if w.d == 128 else "bsa_fwd_kernel<64>",
+                     # forward_ms spans the whole bsa_forward call: key-norm and
+                     # row-bound passes, the bounded pass (the dominant kernel)
+                     # and the exact pass over queued rows.
+                     "kernel": "bsa_fwd_kernel<%d, bounded>" % w.d,
                      "forward_ms": fwd_ms, "peak_source": f"{peak_src} bf16 burst",
                      "frac_of_sustained": achieved / peak_sus},
         "e2e": {"value": flop * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
         "plan_ms": plan_ms,
-        "gpu_launches": 4 * args.steps,
+        # per step: 3 plan kernels + key norms, row bounds, bounded pass, exact pass
+        "gpu_launches": 7 * args.steps,
         "clocks": clk,
     }
     if cpu is not None:

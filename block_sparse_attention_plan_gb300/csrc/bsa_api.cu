@@ -28,7 +28,6 @@ struct PlanImpl {
 
 inline bool supported_block(int b) { return b == 32 || b == 64 || b == 128 || b == 256; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-inline uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255); }
 
 bsa_status compute_layout(int B, int H, int NQB, int NKB, int bq, int bk, int g, int flags,
                           bsa_plan_layout* L, int* nkeys_out) {
@@ -78,11 +77,7 @@ bsa_status compute_layout(int B, int H, int NQB, int NKB, int bq, int bk, int g,
   l.off_totals = off;    off = align256(off + 8ull * 4);
   l.off_control = off;   off = align256(off + 4ull * 16);
   l.off_scratch = off;
-  off = align256(off + 4ull * rows);                       // slots
-  off = align256(off + 4ull * rows);                       // lcnt
-  off = align256(off + 4ull * (urows + 1));                // ucnt
-  off = align256(off + 4ull * (uint64_t)l.groups);         // gstart
-  l.workspace_bytes = off;
+  l.workspace_bytes = fwd_scratch(l).end;  // plan scratch, then forward scratch
   *L = l;
   if (nkeys_out) *nkeys_out = nkeys;
   return BSA_OK;
@@ -276,9 +271,15 @@ bsa_status bsa_forward(const bsa_plan* plan, const void* Q, const void* K, const
   fp.control = pd.control;
   fp.O = static_cast<uint16_t*>(O);
   fp.LSE = LSE;
+  fp.K = static_cast<const uint16_t*>(K);
+  const FwdScratch fs = fwd_scratch(L);
+  fp.kmax = reinterpret_cast<float*>(p->ws + fs.off_kmax);
+  fp.rowk = reinterpret_cast<float*>(p->ws + fs.off_rowk);
+  fp.fb_flag = reinterpret_cast<int32_t*>(p->ws + fs.off_fb_flag);
+  fp.fb_list = reinterpret_cast<int32_t*>(p->ws + fs.off_fb_list);
   fp.slot_capacity = L.slot_capacity;
   fp.watchdog_ns = env_ll("BSA_WATCHDOG_MS", 1000) * 1000000ll;
-  fp.H = L.H; fp.Hkv = L.Hkv; fp.g = L.gqa_group; fp.NQT = L.NQT; fp.NKU = L.NKU;
+  fp.B = L.B; fp.H = L.H; fp.Hkv = L.Hkv; fp.g = L.gqa_group; fp.NQT = L.NQT; fp.NKU = L.NKU;
   fp.Nq = (int)Nq; fp.Nk = (int)Nk; fp.rq = L.rq; fp.rk = L.rk; fp.qu = L.qu; fp.ku = L.ku;
   fp.rows = L.rows;
   const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)d);

@@ -38,6 +38,7 @@
 // BSA_ERR_TIMEOUT in the plan's status word, lets its in-flight copies and
 // MMAs land, frees tensor memory and exits.
 #include <cstdint>
+#include <type_traits>
 #include <cuda_bf16.h>
 
 #include "bsa_device.cuh"
@@ -58,7 +59,18 @@ static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "regist
 constexpr uint32_t kColS = 0;    // S buffer b at kColS + 128 b
 constexpr uint32_t kColO = 256;  // O accumulator, d columns
 constexpr uint32_t kColP = 384;  // P buffer b at kColP + 64 b
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only past 2^8 growth
+// Lazy rescale: O and the row sums keep the reference maximum m of the row
+// until some score exceeds it by more than kRescaleThreshold (log2 units),
+// so weights stay <= 2^16 (bf16 and fp32 hold them exactly as well as 1).
+// A half-row whose weight sum is <= 2^16 cannot hold such a score, which
+// is what is checked per slot; only then are the exact maxima compared.
+constexpr float kRescaleThreshold = 16.0f;
+constexpr float kRescaleSumBound = 65536.0f;  // 2^kRescaleThreshold
+// Bounded pass: weights below 2^-126 are flushed to zero, so a row of at most
+// n keys whose weights sum to at least n * 2^-102 loses under 2^-24 of its
+// total weight (fp32 precision); a row below that (while it has selected
+// keys) is recomputed by the exact pass.
+constexpr float kFallbackPerKey = 0x1p-102f;
 // Work items (positions in the longest-row-first order) are taken from a
 // global atomic counter by the K producer and handed to the other roles
 // through a small ring in shared memory.
@@ -95,8 +107,8 @@ struct Cfg {
   static constexpr int kBarSchedEmpty = kBarSchedFull + kSchedSlots;
   static constexpr int kNumBars = kBarSchedEmpty + kSchedSlots;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
-  static constexpr int kOffSched = kOffMisc + 16;          // int [kSchedSlots] work items
-  static constexpr int kOffX = kOffSched + 4 * kSchedSlots;  // float [2 parities][2 halves][128 rows]
+  static constexpr int kOffSched = kOffMisc + 16;          // int [kSchedSlots][8] work items
+  static constexpr int kOffX = kOffSched + 32 * kSchedSlots;  // float [2 parities][2 halves][128 rows]
   static constexpr int kSmemBytes = kOffX + 2 * 2 * 128 * 4;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -114,6 +126,9 @@ struct Item {
   int qt;      // q-tile
   int kvrow0;  // first K/V row of the head's sequence in the [B*Hkv*Nk, d] view
   bool valid;  // the schedule entry named a plan row
+  int row;     // plan row
+  int it;      // schedule position; < 0: no more work (-2: a wait gave up)
+  float kb;    // largest key norm over the row's K units
 };
 
 __device__ __forceinline__ void record_status(int32_t* ctl, int code, int site) {
@@ -124,13 +139,14 @@ __device__ __forceinline__ void record_status(int32_t* ctl, int code, int site) 
 // Decode one schedule entry, rejecting out-of-range plan data (the row is then
 // treated as empty and BSA_ERR_PLAN_MISMATCH is recorded).
 __device__ __forceinline__ Item load_item(const FwdParams& p, int it, bool report) {
-  Item m{0, 0, 0, 0, 0, false};
+  Item m{0, 0, 0, 0, 0, false, 0, it, 0.f};
   const int row = __ldg(p.order + it);
   if (row < 0 || row >= p.rows) {
     if (report) record_status(p.control, -7, kSitePlanRange);
     return m;
   }
   m.valid = true;
+  m.row = row;
   const int s0 = __ldg(p.row_ptr + row), s1 = __ldg(p.row_ptr + row + 1);
   m.bh = row / p.NQT;
   m.qt = row % p.NQT;
@@ -156,21 +172,47 @@ struct Smem {
   __device__ __forceinline__ uint32_t vst(int s) const { return base + C::kOffV + s * C::kTileBytes; }
 };
 
-// Consumer side of the work-item ring: wait for entry t, read it, release it.
-// Returns the item (position in the schedule), -1 at the end, or -2 when the
-// wait gave up.  `lane_arrives`: whether this thread releases the entry.
+// The work-item ring: the K producer decodes each schedule entry once (its
+// global loads run ahead of everyone else) and publishes the whole item, 8
+// words, so that no other role touches global memory at a row start.
 template <int D>
-__device__ __forceinline__ int sched_take(const Smem<D>& sm, const uint8_t* smem, uint32_t t,
-                                          bool lane_arrives, bool warp_sync, const Watchdog& wd) {
+__device__ __forceinline__ void sched_publish(uint8_t* smem, int slot, const Item& m) {
+  volatile int* e = reinterpret_cast<volatile int*>(smem + Cfg<D>::kOffSched) + slot * 8;
+  e[0] = m.it;
+  e[1] = m.n;
+  e[2] = m.s0;
+  e[3] = m.bh;
+  e[4] = m.qt;
+  e[5] = m.kvrow0;
+  e[6] = m.valid ? m.row : -1;
+  e[7] = __float_as_int(m.kb);
+}
+
+// Consumer side: wait for entry t, read it, release it (`lane_arrives`: this
+// thread releases the entry).  it = -2 when the wait gave up.
+template <int D>
+__device__ __forceinline__ Item sched_take(const Smem<D>& sm, const uint8_t* smem, uint32_t t,
+                                           bool lane_arrives, bool warp_sync, const Watchdog& wd) {
   using C = Cfg<D>;
+  Item m{0, 0, 0, 0, 0, false, 0, -2, 0.f};
   const int slot = (int)(t % kSchedSlots);
   bool ok = mbar_wait(sm.bar(C::kBarSchedFull + slot), (t / kSchedSlots) & 1u, wd, kSiteSched);
   if (warp_sync) ok = __all_sync(0xffffffffu, ok);
-  if (!ok) return -2;
-  const int item = reinterpret_cast<const volatile int*>(smem + C::kOffSched)[slot];
+  if (!ok) return m;
+  const volatile int* e = reinterpret_cast<const volatile int*>(smem + C::kOffSched) + slot * 8;
+  m.it = e[0];
+  m.n = e[1];
+  m.s0 = e[2];
+  m.bh = e[3];
+  m.qt = e[4];
+  m.kvrow0 = e[5];
+  const int row = e[6];
+  m.valid = row >= 0;
+  m.row = m.valid ? row : 0;
+  m.kb = __int_as_float(e[7]);
   if (warp_sync) __syncwarp();
   if (lane_arrives) mbar_arrive(sm.bar(C::kBarSchedEmpty + slot));
-  return item;
+  return m;
 }
 
 // Bounded wait used during teardown: ignores the abort flag, short limit.
@@ -256,23 +298,29 @@ __device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, co
                        : Ring{sm.vst(0), sm.bar(C::kBarVFull), sm.bar(C::kBarVEmpty), C::kStagesV};
   uint32_t q_it = 0, kv_it = 0;
   bool ok = true;
-  volatile int* sched = reinterpret_cast<volatile int*>(smem + C::kOffSched);
+  const int nwork =
+      p.work_count ? *reinterpret_cast<const volatile int32_t*>(p.work_count) : p.rows;
   for (uint32_t t = 0; ok; ++t) {
-    int it;
+    Item m;
     if (kside) {
       const int slot = (int)(t % kSchedSlots);
       if (!mbar_wait(sm.bar(C::kBarSchedEmpty + slot), ((t / kSchedSlots) & 1u) ^ 1u, wd,
                      kSiteSched))
         break;
-      it = atomicAdd(p.control + kCtlWorkCounter, 1);
-      if (it >= p.rows) it = -1;
-      sched[slot] = it;
+      int it = atomicAdd(p.work_counter, 1);
+      if (it >= nwork) it = -1;
+      if (it >= 0) {
+        m = load_item(p, it, true);
+        if (m.n > 0) m.kb = __ldg(p.rowk + m.row);
+      } else {
+        m = Item{0, 0, 0, 0, 0, false, 0, -1, 0.f};
+      }
+      sched_publish<D>(smem, slot, m);
       mbar_arrive(sm.bar(C::kBarSchedFull + slot));
     } else {
-      it = sched_take<D>(sm, smem, t, true, false, wd);
+      m = sched_take<D>(sm, smem, t, true, false, wd);
     }
-    if (it < 0) break;
-    const Item m = load_item(p, it, kside);
+    if (m.it < 0) break;
     if (m.n == 0) continue;
     if (kside) {
       const int qb = q_buf<D>(q_it);
@@ -382,9 +430,8 @@ __device__ __noinline__ void s_issuer_role(const FwdParams& p, const uint8_t* sm
   uint32_t q_it = 0;
   bool ok = true;
   for (uint32_t t = 0; ok; ++t) {
-    const int it = sched_take<D>(sm, smem, t, true, false, wd);
-    if (it < 0) break;
-    const Item m = load_item(p, it, false);
+    const Item m = sched_take<D>(sm, smem, t, true, false, wd);
+    if (m.it < 0) break;
     if (m.n == 0) continue;
     const int qb = q_buf<D>(q_it);
     if (!mbar_wait(sm.bar(C::kBarQFull + qb), q_par<D>(q_it), wd, kSiteQFull)) break;
@@ -410,9 +457,8 @@ __device__ __noinline__ void pv_issuer_role(const FwdParams& p, const uint8_t* s
   uint32_t rows = 0;
   bool ok = true;
   for (uint32_t t = 0; ok; ++t) {
-    const int it = sched_take<D>(sm, smem, t, true, false, wd);
-    if (it < 0) break;
-    const Item m = load_item(p, it, false);
+    const Item m = sched_take<D>(sm, smem, t, true, false, wd);
+    if (m.it < 0) break;
     const int n = m.n;
     if (n == 0) continue;
     for (int j = 0; j < n && ok; ++j) {
@@ -447,7 +493,15 @@ __device__ __noinline__ void pv_issuer_role(const FwdParams& p, const uint8_t* s
 }
 
 // ------------------------------------------------------------------ softmax
-template <int D>
+// Bounded pass (kExact = false): every row takes as its reference maximum the
+// Cauchy-Schwarz bound |q| * max|k| * scale * log2(e) over the K units of its
+// slots, which no score of the row exceeds, so each weight is <= 1, no
+// rescale is ever due and the two threads of a row need no exchange until
+// the epilogue.  A row whose weights then sum to less than 2^-64 (the bound
+// was far above its scores) is queued for the exact pass.
+// Exact pass (kExact = true): the running row maximum, agreed between the
+// two threads of a row, with a lazy rescale of O.
+template <int D, bool kExact>
 __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, const Smem<D>& sm,
                                              uint32_t tmem, const Watchdog& wd) {
   using C = Cfg<D>;
@@ -464,21 +518,30 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   const float sl2 = p.scale_log2;
   const uint64_t sl2x2 = f2_make(sl2, sl2);
   float* xbuf = reinterpret_cast<float*>(smem + C::kOffX);
-  uint32_t sg = 0, rows = 0, xc = 0;
+  uint32_t sg = 0, rows = 0, xc = 0, q_it = 0;
   uint32_t bits = 0xffffffffu;  // this row's sub-mask bits for the current slot
 
   // One float per row with the thread of the other key half that owns the
   // same row (warp quad + 4 <-> quad + 8); double-buffered by round parity.
-  auto exchange = [&](float mine, float& theirs) -> bool {
+  // post() hands this thread's value over; collect() waits for the
+  // partner's value of the same round.
+  auto post = [&](float mine) {
     const int par = (int)(xc & 1u);
     xbuf[(par * 2 + h) * 128 + rloc] = mine;
     __syncwarp();
+    if (lane == 0) mbar_arrive(sm.bar(C::kBarXchg + quad * 2 + par));
+  };
+  auto collect = [&](float& theirs) -> bool {
+    const int par = (int)(xc & 1u);
     const uint32_t bar = sm.bar(C::kBarXchg + quad * 2 + par);
-    if (lane == 0) mbar_arrive(bar);
     const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, (xc >> 1) & 1u, wd, kSiteXchg));
     if (ok) theirs = xbuf[(par * 2 + (h ^ 1)) * 128 + rloc];
     ++xc;
     return ok;
+  };
+  auto exchange = [&](float mine, float& theirs) -> bool {
+    post(mine);
+    return collect(theirs);
   };
   // This thread's 64 scores of the slot in S buffer `sbuf` (masked -> -inf).
   auto load_s = [&](uint32_t sbuf, uint32_t (&v)[64]) {
@@ -497,21 +560,33 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       }
     }
   };
-  // p = 2^(s*scale*log2e - m), packed in place as bf16 pairs into v[0..32);
-  // returns the sum of the 64 values of p.
-  auto exp_pack = [&](uint32_t (&v)[64], float m) -> float {
+  // p = 2^(s*scale*log2e - m) as bf16 pairs into pk (keys 2e, 2e+1 -> pk[e]).
+  // Returns the sum of the 64 values of p; *sum_w gets the sum of the same
+  // values as rounded to bf16, i.e. of the weights the P V product applies
+  // (O is divided by that sum, so exactly those weights are normalised; the
+  // log-sum-exp uses the exact one).  With kMax, also the maximum of the raw
+  // scores in *mx.
+  auto exp_pack = [&](const uint32_t (&v)[64], uint32_t (&pk)[32], float m, auto with_max,
+                      float* mx, float* sum_w) -> float {
+    constexpr bool kMax = decltype(with_max)::value;
     const float mb = (m == -INFINITY) ? 0.f : m;
     const uint64_t nmbx2 = f2_make(-mb, -mb);
     uint64_t acc2[2] = {0ull, 0ull};
+    float accw[4] = {0.f, 0.f, 0.f, 0.f};
+    float mx2[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
+      const float a0 = __uint_as_float(v[2 * e]), a1 = __uint_as_float(v[2 * e + 1]);
+      if (kMax) mx2[e & 1] = fmax3(mx2[e & 1], a0, a1);
       float x0, x1;
-      f2_split(ffma2(f2_make(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sl2x2, nmbx2),
-               x0, x1);
+      f2_split(ffma2(f2_make(a0, a1), sl2x2, nmbx2), x0, x1);
       const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+      pk[e] = pack_bf16x2(p0, p1);
       acc2[e & 1] = fadd2(acc2[e & 1], f2_make(p0, p1));
-      v[e] = pack_bf16x2(p0, p1);
+      add_bf16x2_f32(accw[2 * (e & 1)], accw[2 * (e & 1) + 1], pk[e]);
     }
+    if (kMax) *mx = fmaxf(mx2[0], mx2[1]);
+    *sum_w = (accw[0] + accw[1]) + (accw[2] + accw[3]);
     float s0, s1, s2, s3;
     f2_split(acc2[0], s0, s1);
     f2_split(acc2[1], s2, s3);
@@ -519,9 +594,8 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   };
 
   for (uint32_t t = 0;; ++t) {
-    const int it = sched_take<D>(sm, smem, t, lane == 0, true, wd);
-    if (it < 0) break;
-    const Item m = load_item(p, it, false);
+    const Item m = sched_take<D>(sm, smem, t, lane == 0, true, wd);
+    if (m.it < 0) break;
     if (!m.valid) continue;
     const size_t orow = (size_t)m.bh * p.Nq + (size_t)m.qt * 128 + rloc;
     uint4* optr = reinterpret_cast<uint4*>(p.O + orow * D + h * (D / 2));
@@ -531,7 +605,38 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       if (h == 0) p.LSE[orow] = -INFINITY;
       continue;
     }
-    float m_ref = -INFINITY, l_run = 0.f;
+    // The row's Q tile: (bounded pass) this row's query norm; then release
+    // it (with the S issuer's commit, the buffer can be refilled).
+    const int qb = q_buf<D>(q_it);
+    if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarQFull + qb), q_par<D>(q_it), wd, kSiteQFull)))
+      break;
+    float m_ref = -INFINITY;
+    if constexpr (!kExact) {
+      // |q|^2 from the 128B-swizzled tile: 16-byte unit u of row r in a
+      // 64-column chunk sits at unit position u ^ (r % 8).
+      float q2a = 0.f, q2b = 0.f;
+      const uint32_t qrow = sm.q(qb) + (uint32_t)rloc * 128u;
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+#pragma unroll
+        for (int u4 = 0; u4 < 8; ++u4) {
+          const uint4 x = ld_shared_v4(qrow + (uint32_t)(c * C::kChunkBytes) + ((u4 ^ (rloc & 7)) << 4));
+          const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
+            q2a = fmaf(lo, lo, q2a);
+            q2b = fmaf(hi, hi, q2b);
+          }
+        }
+      }
+      m_ref = sqrtf(q2a + q2b) * m.kb * sl2;  // m.kb: largest key norm of the row's K units
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.bar(C::kBarQEmpty + qb));
+    ++q_it;
+    float l_run = 0.f, lw_run = 0.f;  // exact and bf16-weight row sums
+    bool has_keys = !submask;         // (bounded pass) some key of the row is selected
     bool ok = true;
     for (int j = 0; j < m.n; ++j) {
       const int b = (int)(sg & 1u);
@@ -548,62 +653,110 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.bar(C::kBarSFree + b));
-      // Max of this half-row, then of the whole row with the partner's half.
-      float mx4[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) mx4[c] = fmaxf(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]));
-#pragma unroll
-      for (int e = 8; e < 64; e += 8) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          mx4[c] = fmax3(mx4[c], __uint_as_float(v[e + 2 * c]), __uint_as_float(v[e + 2 * c + 1]));
-      }
-      float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      float mo = -INFINITY;
-      if (!exchange(mx, mo)) {
-        ok = false;
-        break;
-      }
-      mx = fmaxf(mx, mo);
-      // Both threads of a row see the same maximum, so they keep the same
-      // reference and take the same rescale decisions.
-      const float m_new = fmaxf(m_ref, mx * sl2);
-      float factor = 1.f;
-      if (m_ref == -INFINITY) {
-        m_ref = m_new;  // nothing weighted accumulated yet
-      } else if (m_new > m_ref + kRescaleThreshold) {
-        factor = ex2_approx(m_ref - m_new);
-        m_ref = m_new;
-      }
-      const float sum = exp_pack(v, m_ref);
-      // P buffer b was last read by the P V of slot g - 2.
-      if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
-        ok = false;
-        break;
-      }
-      if (__any_sync(0xffffffffu, factor != 1.f)) {
-        // O changes scale: the P V of slot g - 1 must have finished with it
-        // (the one of slot g starts only after this slot's P is published).
-        const uint32_t g1 = sg - 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + (int)(g1 & 1u)), (g1 >> 1) & 1u, wd, kSitePFull))) {
+      uint32_t pk[32];
+      float sum, sum_w, factor = 1.f;
+      const uint32_t pcol = tmem + tl + kColP + 64u * (uint32_t)b + 32u * (uint32_t)h;
+      if constexpr (!kExact) {
+        if (submask) has_keys |= (bits != 0u);
+        sum = exp_pack(v, pk, m_ref, std::false_type{}, nullptr, &sum_w);
+        // P buffer b was last read by the P V of slot g - 2.
+        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t o_addr = tmem + tl + kColO + (uint32_t)(h * (D / 2));
+        tmem_st32(pcol, pk);
+      } else if (m_ref == -INFINITY) {
+        // No reference yet in this row: the whole-row maximum first (both
+        // threads of a row get the same value and so the same reference).
+        float mx4[4];
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t o[32];
-          tmem_ld32(o_addr + c * 32, o);
-          tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) mx4[c] = fmaxf(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]));
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
-          tmem_st32(o_addr + c * 32, o);
+        for (int e = 8; e < 64; e += 8) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            mx4[c] = fmax3(mx4[c], __uint_as_float(v[e + 2 * c]), __uint_as_float(v[e + 2 * c + 1]));
+        }
+        float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        float mo = -INFINITY;
+        if (!exchange(mx, mo)) {
+          ok = false;
+          break;
+        }
+        m_ref = fmaxf(mx, mo) * sl2;  // stays -inf while every key so far is masked
+        sum = exp_pack(v, pk, m_ref, std::false_type{}, nullptr, &sum_w);
+        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
+          ok = false;
+          break;
+        }
+        tmem_st32(pcol, pk);
+      } else {
+        // Exponentials against the current reference right away; whether a
+        // rescale is due is settled while P is being written.
+        sum = exp_pack(v, pk, m_ref, std::false_type{}, nullptr, &sum_w);
+        post(sum_w);
+        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
+          ok = false;
+          break;
+        }
+        tmem_st32(pcol, pk);
+        float sw_other = 0.f;
+        if (!collect(sw_other)) {
+          ok = false;
+          break;
+        }
+        // Both threads of a row see the same two sums, and the two warps of a
+        // lane quadrant hold the same rows: they take this branch together.
+        if (__any_sync(0xffffffffu, sum_w > kRescaleSumBound || sw_other > kRescaleSumBound)) {
+          float mx4[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) mx4[c] = fmaxf(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]));
+#pragma unroll
+          for (int e = 8; e < 64; e += 8) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              mx4[c] = fmax3(mx4[c], __uint_as_float(v[e + 2 * c]), __uint_as_float(v[e + 2 * c + 1]));
+          }
+          const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+          float mo = -INFINITY;
+          if (!exchange(mx, mo)) {
+            ok = false;
+            break;
+          }
+          const float m_new = fmaxf(mx, mo) * sl2;
+          if (__any_sync(0xffffffffu, m_new > m_ref + kRescaleThreshold)) {
+            if (m_new > m_ref + kRescaleThreshold) {
+              factor = ex2_approx(m_ref - m_new);
+              m_ref = m_new;
+            }
+            sum = exp_pack(v, pk, m_ref, std::false_type{}, nullptr, &sum_w);
+            // O changes scale: the P V of slot g - 1 must have finished with
+            // it (the one of slot g starts only after this slot's P is
+            // published).
+            const uint32_t g1 = sg - 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + (int)(g1 & 1u)), (g1 >> 1) & 1u, wd, kSitePFull))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            tmem_wait_st();
+            tmem_st32(pcol, pk);
+            const uint32_t o_addr = tmem + tl + kColO + (uint32_t)(h * (D / 2));
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+              uint32_t o[32];
+              tmem_ld32(o_addr + c * 32, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+              tmem_st32(o_addr + c * 32, o);
+            }
+          }
         }
       }
-      tmem_st32_at<0>(tmem + tl + kColP + 64u * (uint32_t)b + 32u * (uint32_t)h, v);
       tmem_wait_st();
       l_run = l_run * factor + sum;
+      lw_run = lw_run * factor + sum_w;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.bar(C::kBarPFull + b));  // one arrival per warp
@@ -613,10 +766,19 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     // ------------------------------------------------------------ epilogue
     if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarOFull), rows & 1u, wd, kSiteODone))) break;
     tc_fence_after();
-    float l_other = 0.f;
+    float l_other = 0.f, lw_other = 0.f;
     if (!exchange(l_run, l_other)) break;
-    const float L = l_run + l_other;
-    const float inv = (L > 0.f) ? 1.f / L : 0.f;
+    if (!exchange(lw_run, lw_other)) break;
+    const float L = l_run + l_other, Lw = lw_run + lw_other;
+    const float inv = (Lw > 0.f) ? 1.f / Lw : 0.f;
+    if constexpr (!kExact) {
+      // Both threads of a row compute the same L and has_keys.
+      const bool need = has_keys && !(Lw >= kFallbackPerKey * (float)(m.n * 128));
+      if (__any_sync(0xffffffffu, need) && lane == 0) {
+        if (atomicExch(p.fb_flag + m.row, 1) == 0)
+          p.fb_list[atomicAdd(p.control + kCtlFallbackCount, 1)] = m.row;
+      }
+    }
     const uint32_t o_addr = tmem + tl + kColO + (uint32_t)(h * (D / 2));
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {  // this thread's half of the row, 32 columns at a time
@@ -640,7 +802,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   }
 }
 
-template <int D>
+template <int D, bool kExact>
 __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -656,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
     if (sm.base & 1023u) record_failure(wd, -4, 0);  // layout assumption violated
     for (int i = 0; i < 2; ++i) {
       mbar_init(sm.bar(C::kBarQFull + i), 1);
-      mbar_init(sm.bar(C::kBarQEmpty + i), 1);
+      mbar_init(sm.bar(C::kBarQEmpty + i), 1 + 8);  // S issuer commit + softmax warps
       mbar_init(sm.bar(C::kBarSFull + i), 1);
       mbar_init(sm.bar(C::kBarSFree + i), 8);  // one arrival per softmax warp
       mbar_init(sm.bar(C::kBarPFull + i), 8);  // one arrival per softmax warp
@@ -692,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
 
   if (warp >= 4) {
     regs_inc<kRegsSoftmax>();
-    softmax_role<D>(p, smem, sm, tmem, wd);
+    softmax_role<D, kExact>(p, smem, sm, tmem, wd);
   } else {
     regs_dec<kRegsControl>();
     if (lane == 0 && !*abort_flag) {
@@ -725,14 +887,94 @@ __global__ void watchdog_selftest_kernel(int32_t* status, long long limit_ns) {
   if (mbar_wait(bar, 0, wd, kSiteSelftest)) status[3] = 1;
 }
 
-template <int D>
+template <int D, bool kExact>
 cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t stream) {
   const int smem = Cfg<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(bsa_fwd_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(bsa_fwd_kernel<D, kExact>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  bsa_fwd_kernel<D><<<grid, kThreads, smem, stream>>>(p);
+  bsa_fwd_kernel<D, kExact><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
+}
+
+// Largest key norm of every K unit (ku rows) of every K/V head, i.e. a bound
+// on |k| for the Cauchy-Schwarz reference of the bounded pass; also clears
+// the fallback flags.  One warp per unit; d/8 lanes read one 16-byte part
+// each of a row, so a warp reads 32 x 16 contiguous bytes per load.
+template <int D>
+__global__ void __launch_bounds__(256) kmax_kernel(const uint16_t* __restrict__ K,
+                                                   float* __restrict__ kmax, int units, int ku,
+                                                   int32_t* __restrict__ fb_flag, int rows) {
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerStep = 32 / kLanesPerRow;
+  const int tid = blockIdx.x * blockDim.x + threadIdx.x;
+  for (int i = tid; i < rows; i += gridDim.x * blockDim.x) fb_flag[i] = 0;
+  const int unit = tid >> 5, lane = threadIdx.x & 31;
+  if (unit >= units) return;
+  const int sub = lane / kLanesPerRow, part = lane % kLanesPerRow;
+  // K units are contiguous in the [B*Hkv*Nk, d] view: unit i covers rows [i*ku, (i+1)*ku).
+  const uint4* base = reinterpret_cast<const uint4*>(K + (size_t)unit * ku * D) + part;
+  float best = 0.f;
+  for (int r = sub; r < ku; r += kRowsPerStep) {
+    const uint4 x = __ldg(base + (size_t)r * (D / 8));
+    const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+    float s2 = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
+      s2 = fmaf(lo, lo, fmaf(hi, hi, s2));
+    }
+#pragma unroll
+    for (int o = kLanesPerRow / 2; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+    best = fmaxf(best, s2);
+  }
+#pragma unroll
+  for (int o = 16; o >= kLanesPerRow; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
+  if (lane == 0) kmax[unit] = sqrtf(best);
+}
+
+// Largest key norm over the K units of each plan row's slots (one warp per
+// row), the |k| factor of the row's Cauchy-Schwarz reference.
+__global__ void __launch_bounds__(256) rowbound_kernel(const FwdParams p) {
+  const int row = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+  if (row >= p.rows) return;
+  const int s0 = __ldg(p.row_ptr + row), s1 = __ldg(p.row_ptr + row + 1);
+  float km = 0.f;
+  if (s0 >= 0 && s1 >= s0 && (long long)s1 <= p.slot_capacity) {  // else the forward reports it
+    const int bh = row / p.NQT, b = bh / p.H, h = bh % p.H;
+    const float* kh = p.kmax + (size_t)(b * p.Hkv + h / p.g) * p.NKU;
+    for (long long i = (long long)s0 * p.rk + lane; i < (long long)s1 * p.rk; i += 32) {
+      const int y = __ldg(p.slot_ku + i);
+      if (y >= 0 && y < p.NKU) km = fmaxf(km, __ldg(kh + y));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, o));
+  if (lane == 0) p.rowk[row] = km;
+}
+
+template <int D>
+cudaError_t launch_passes(const FwdParams& p, int grid, cudaStream_t stream) {
+  const long long units = (long long)p.B * p.Hkv * p.NKU;
+  const long long blocks = (units + 7) / 8;
+  kmax_kernel<D><<<(unsigned)(blocks > 0 ? blocks : 1), 256, 0, stream>>>(p.K, p.kmax, (int)units,
+                                                                        p.ku, p.fb_flag, p.rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  rowbound_kernel<<<(unsigned)((p.rows + 7) / 8), 256, 0, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  FwdParams a = p;
+  a.work_counter = p.control + kCtlWorkCounter;
+  a.work_count = nullptr;
+  e = launch_d<D, false>(a, grid, stream);
+  if (e != cudaSuccess) return e;
+  // Exact pass over the queued rows (exits at once when none was queued).
+  FwdParams x = p;
+  x.order = p.fb_list;
+  x.work_counter = p.control + kCtlFallbackWork;
+  x.work_count = p.control + kCtlFallbackCount;
+  return launch_d<D, true>(x, grid, stream);
 }
 
 }  // namespace
@@ -740,8 +982,8 @@ cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t stream) {
 int forward_smem_bytes(int d) { return d == 64 ? Cfg<64>::kSmemBytes : Cfg<128>::kSmemBytes; }
 
 cudaError_t launch_forward(const FwdParams& p, int d, int grid, cudaStream_t stream) {
-  if (d == 64) return launch_d<64>(p, grid, stream);
-  return launch_d<128>(p, grid, stream);
+  if (d == 64) return launch_passes<64>(p, grid, stream);
+  return launch_passes<128>(p, grid, stream);
 }
 
 cudaError_t launch_watchdog_selftest(int32_t* status, long long limit_ns, cudaStream_t stream) {

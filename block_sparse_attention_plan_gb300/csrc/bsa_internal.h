@@ -15,6 +15,8 @@ constexpr int kMaxGroups = 8192;      // bound on K/V-head groups (B * Hkv)
 constexpr int kCtlWorkCounter = 0;    // control word indices
 constexpr int kCtlStatus = 1;
 constexpr int kCtlDetail = 2;
+constexpr int kCtlFallbackCount = 3;  // rows queued for the exact second pass
+constexpr int kCtlFallbackWork = 4;   // work counter of that pass
 
 // Wait sites recorded in the status detail word (low 8 bits).
 enum WaitSite : int {
@@ -42,6 +44,30 @@ struct PlanDev {
   int NQT, NKU, rows, urows, nkeys, groups;
 };
 
+inline uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255); }
+
+// Forward-pass scratch inside a plan workspace, after the plan-construction
+// scratch: the largest key norm of every K unit (float[B*Hkv*NKU]), that of
+// every plan row's selected units (float[rows]), a fallback flag per plan row
+// and the list of rows queued for the exact pass (int32[rows] each).
+struct FwdScratch {
+  uint64_t off_kmax, off_rowk, off_fb_flag, off_fb_list, end;
+};
+inline FwdScratch fwd_scratch(const bsa_plan_layout& L) {
+  uint64_t off = L.off_scratch;
+  off = align256(off + 4ull * (uint64_t)L.rows);          // plan scratch: slots
+  off = align256(off + 4ull * (uint64_t)L.rows);          // lcnt
+  off = align256(off + 4ull * ((uint64_t)L.urows + 1));   // ucnt
+  off = align256(off + 4ull * (uint64_t)L.groups);        // gstart
+  FwdScratch f;
+  f.off_kmax = off;    off = align256(off + 4ull * (uint64_t)L.B * L.Hkv * L.NKU);
+  f.off_rowk = off;    off = align256(off + 4ull * (uint64_t)L.rows);
+  f.off_fb_flag = off; off = align256(off + 4ull * (uint64_t)L.rows);
+  f.off_fb_list = off; off = align256(off + 4ull * (uint64_t)L.rows);
+  f.end = off;
+  return f;
+}
+
 // Kernel parameters of the forward pass (passed as a __grid_constant__).
 struct FwdParams {
   CUtensorMap tmQ;   // Q viewed as [B*Hq*Nq, d], box {64, 128}, 128B swizzle
@@ -54,13 +80,22 @@ struct FwdParams {
   int32_t* control;
   uint16_t* O;       // bf16 bits
   float* LSE;
+  const uint16_t* K;     // bf16 bits, [B*Hkv*Nk, d] (read by the key-norm pass)
+  float* kmax;           // largest key norm per K unit
+  float* rowk;           // largest key norm over each plan row's K units
+  int32_t* fb_flag;      // per plan row: queued for the exact pass
+  int32_t* fb_list;      // plan rows queued for the exact pass
+  int32_t* work_counter;         // set by launch_forward: the pass's work counter
+  const int32_t* work_count;     // number of work items (nullptr: rows)
   long long slot_capacity;
   long long watchdog_ns;
-  int H, Hkv, g, NQT, NKU, Nq, Nk, rq, rk, qu, ku, rows;
+  int B, H, Hkv, g, NQT, NKU, Nq, Nk, rq, rk, qu, ku, rows;
   float scale_log2;  // scale * log2(e)
 };
 
 cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream);
+// Key-norm pass, bounded-reference pass over every plan row, then the exact
+// pass over the rows the first one queued (see bsa_forward.cu).
 cudaError_t launch_forward(const FwdParams& p, int d, int grid, cudaStream_t stream);
 int forward_smem_bytes(int d);
 cudaError_t launch_watchdog_selftest(int32_t* status, long long limit_ns, cudaStream_t stream);

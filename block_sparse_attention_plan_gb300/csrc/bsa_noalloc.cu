@@ -76,7 +76,6 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t rows, int d, int box_r
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-inline uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255); }
 
 }  // namespace
 
@@ -144,8 +143,15 @@ extern "C" bsa_status bsa_attention_static(const uint8_t* mask, int B, int H, in
   fp.control = pd.control;
   fp.O = static_cast<uint16_t*>(O);
   fp.LSE = LSE;
+  fp.K = static_cast<const uint16_t*>(K);
+  const FwdScratch fs = fwd_scratch(L);
+  fp.kmax = reinterpret_cast<float*>(ws + fs.off_kmax);
+  fp.rowk = reinterpret_cast<float*>(ws + fs.off_rowk);
+  fp.fb_flag = reinterpret_cast<int32_t*>(ws + fs.off_fb_flag);
+  fp.fb_list = reinterpret_cast<int32_t*>(ws + fs.off_fb_list);
   fp.slot_capacity = L.slot_capacity;
   fp.watchdog_ns = 1000ll * 1000000ll;
+  fp.B = B;
   fp.H = H; fp.Hkv = L.Hkv; fp.g = gqa_group; fp.NQT = L.NQT; fp.NKU = L.NKU;
   fp.Nq = (int)Nq; fp.Nk = (int)Nk; fp.rq = L.rq; fp.rk = L.rk; fp.qu = L.qu; fp.ku = L.ku;
   fp.rows = L.rows;

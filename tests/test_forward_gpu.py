@@ -59,15 +59,55 @@ def test_forward_scale_override_and_long_rows(bsa):
 
 
 def test_forward_large_logits_rescale(bsa):
-    # Scores growing along the key axis force the running max to move past the
-    # lazy-rescale threshold many times.
+    # Scores growing along the key axis (by about 60 in log2 units over the
+    # sequence) force the running max past the lazy-rescale threshold (16 log2
+    # units) several times.
     w = W.random_problem(12, 1, 2, 2, 256, 4096, 128, 128, 128, 1.1)
     ramp = torch.linspace(0.2, 3.0, 4096).view(1, 1, 4096, 1)
     w.k = (w.k.float() * ramp).to(torch.bfloat16)
-    w.q = (w.q.float() * 2.0).to(torch.bfloat16)
+    w.q = (w.q.float() * 4.0).to(torch.bfloat16)
     o, lse = run_gpu(bsa, w)
     O, L = OA.block_gather(w.q, w.k, w.v, w.mask, 128, 128)
     assert_attention_close(o, lse, O, L, "rescale")
+
+
+# Control word holding the number of plan rows the bounded pass queued for
+# the exact pass (index 3 of the plan's control words).
+FALLBACK_COUNT = 3
+
+
+def test_forward_loose_bound_rows_take_exact_pass(bsa):
+    # Heads 0-1 (K/V head 0): a large query component on channel 0 and a large
+    # key component on channel 1 make |q||k| (the row bound) exceed every
+    # score by thousands of log2 units, so the bounded pass underflows there
+    # and must hand those rows to the exact pass; heads 2-3 stay ordinary.
+    w = W.random_problem(21, 1, 4, 2, 512, 1024, 128, 128, 128, 0.7)
+    q, k = w.q.float(), w.k.float()
+    q[:, :2, :, 0] = 150.0
+    k[:, :1, :, 1] = 150.0
+    w.q, w.k = q.to(torch.bfloat16), k.to(torch.bfloat16)
+    p = bsa.plan(w.mask.cuda(), w.bq, w.bk, w.gqa_group)
+    o, lse = bsa.forward(p, w.q.cuda(), w.k.cuda(), w.v.cuda())
+    st, det = bsa.sync_status(p)
+    assert st == 0, (st, hex(det))
+    queued = int(p.control()[FALLBACK_COUNT].item())
+    rows_h01 = 2 * (512 // 128)
+    nonempty_h01 = int((w.mask[0, :2].reshape(2, 4, -1).sum(-1) > 0).sum())
+    assert nonempty_h01 <= queued <= rows_h01, (queued, nonempty_h01)
+    O, L = OA.block_gather(w.q, w.k, w.v, w.mask, 128, 128)
+    assert_attention_close(o, lse, O, L, "loose bound")
+
+
+@pytest.mark.parametrize("name", ["video_dit_small", "chunked_prefill_small", "regular_small",
+                                  "long_video_dit_small"])
+def test_forward_bounded_pass_queues_nothing_on_workloads(bsa, name):
+    # On the benchmark-shaped inputs the row bound stays close enough to the
+    # scores that no row should need the exact pass.
+    w = W.make_workload(name)
+    p = bsa.plan(w.mask.cuda(), w.bq, w.bk, w.gqa_group)
+    bsa.forward(p, w.q.cuda(), w.k.cuda(), w.v.cuda())
+    assert bsa.sync_status(p)[0] == 0
+    assert int(p.control()[FALLBACK_COUNT].item()) == 0
 
 
 def test_forward_repeat_and_plan_reuse(bsa):
