@@ -899,37 +899,38 @@ cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t stream) {
 
 // Largest key norm of every K unit (ku rows) of every K/V head, i.e. a bound
 // on |k| for the Cauchy-Schwarz reference of the bounded pass; also clears
-// the fallback flags.  One warp per unit; d/8 lanes read one 16-byte part
-// each of a row, so a warp reads 32 x 16 contiguous bytes per load.
+// the fallback flags.  One warp per unit, one row per lane at a time with the
+// row's d/8 16-byte loads all in flight; one reduction at the end.
 template <int D>
 __global__ void __launch_bounds__(256) kmax_kernel(const uint16_t* __restrict__ K,
                                                    float* __restrict__ kmax, int units, int ku,
                                                    int32_t* __restrict__ fb_flag, int rows) {
-  constexpr int kLanesPerRow = D / 8;
-  constexpr int kRowsPerStep = 32 / kLanesPerRow;
   const int tid = blockIdx.x * blockDim.x + threadIdx.x;
   for (int i = tid; i < rows; i += gridDim.x * blockDim.x) fb_flag[i] = 0;
   const int unit = tid >> 5, lane = threadIdx.x & 31;
   if (unit >= units) return;
-  const int sub = lane / kLanesPerRow, part = lane % kLanesPerRow;
   // K units are contiguous in the [B*Hkv*Nk, d] view: unit i covers rows [i*ku, (i+1)*ku).
-  const uint4* base = reinterpret_cast<const uint4*>(K + (size_t)unit * ku * D) + part;
   float best = 0.f;
-  for (int r = sub; r < ku; r += kRowsPerStep) {
-    const uint4 x = __ldg(base + (size_t)r * (D / 8));
-    const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-    float s2 = 0.f;
+  for (int r = lane; r < ku; r += 32) {
+    const uint4* src = reinterpret_cast<const uint4*>(K + ((size_t)unit * ku + r) * D);
+    uint4 x[D / 8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
-      s2 = fmaf(lo, lo, fmaf(hi, hi, s2));
+    for (int c = 0; c < D / 8; ++c) x[c] = __ldg(src + c);
+    float s2a = 0.f, s2b = 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      const uint32_t w4[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
+        s2a = fmaf(lo, lo, s2a);
+        s2b = fmaf(hi, hi, s2b);
+      }
     }
-#pragma unroll
-    for (int o = kLanesPerRow / 2; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-    best = fmaxf(best, s2);
+    best = fmaxf(best, s2a + s2b);
   }
 #pragma unroll
-  for (int o = 16; o >= kLanesPerRow; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
+  for (int o = 16; o > 0; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
   if (lane == 0) kmax[unit] = sqrtf(best);
 }
 
