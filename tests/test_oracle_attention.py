@@ -150,3 +150,59 @@ def test_sampled_rows_match_full_gather():
         np.testing.assert_array_equal(l, L[b, h, qb * 128:(qb + 1) * 128])
     # the all-padding block selects nothing: empty rows
     assert np.all(np.isneginf(L[0, :, 10 * 128:]))
+
+
+# ---------------------------------------------------------------- element mask
+def test_causal_equals_sdpa_is_causal():
+    # Nq = Nk, all-ones block mask: the element mask is plain causal attention.
+    w = _problem(41, 1, 2, 2, 128, 128, 32, 32, 32, 1.0)
+    ones = torch.ones(1, 2, 4, 4, dtype=torch.uint8)
+    O, L = OA.dense_masked(w.q, w.k, w.v, ones, 32, 32, causal=True)
+    ref = F.scaled_dot_product_attention(w.q.double(), w.k.double(), w.v.double(), is_causal=True)
+    np.testing.assert_allclose(O, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_causal_offset_equals_shifted_tril_mask():
+    # Nq < Nk: queries are the last Nq positions, so query i sees keys j <= i + Nk - Nq;
+    # the mask here is built with torch.tril's diagonal offset.
+    w = _problem(42, 1, 2, 1, 64, 192, 32, 32, 32, 1.0)
+    ones = torch.ones(1, 2, 2, 6, dtype=torch.uint8)
+    O, L = OA.dense_masked(w.q, w.k, w.v, ones, 32, 32, causal=True)
+    tm = torch.ones(64, 192, dtype=torch.bool).tril(diagonal=192 - 64)
+    k64 = w.k.double().repeat_interleave(2, dim=1)
+    v64 = w.v.double().repeat_interleave(2, dim=1)
+    ref = F.scaled_dot_product_attention(w.q.double(), k64, v64, attn_mask=tm)
+    np.testing.assert_allclose(O, ref.numpy(), rtol=0, atol=1e-12)
+    s = (w.q.double() @ k64.transpose(-1, -2)) / math.sqrt(32)
+    lse = torch.logsumexp(s.masked_fill(~tm, float("-inf")), dim=-1)
+    np.testing.assert_allclose(L, lse.numpy(), rtol=0, atol=1e-12)
+
+
+def test_kv_lens_equal_sdpa_on_sliced_keys():
+    w = _problem(43, 2, 2, 2, 64, 128, 32, 32, 32, 1.0)
+    ones = torch.ones(2, 2, 2, 4, dtype=torch.uint8)
+    lens = [77, 128]
+    O, L = OA.dense_masked(w.q, w.k, w.v, ones, 32, 32, kv_lens=lens)
+    for b, n in enumerate(lens):
+        ref = F.scaled_dot_product_attention(w.q[b:b + 1].double(), w.k[b:b + 1, :, :n].double(),
+                                             w.v[b:b + 1, :, :n].double())
+        np.testing.assert_allclose(O[b:b + 1], ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_kv_len_zero_gives_empty_rows():
+    w = _problem(44, 1, 1, 1, 32, 64, 32, 32, 32, 1.0)
+    ones = torch.ones(1, 1, 1, 2, dtype=torch.uint8)
+    O, L = OA.block_gather(w.q, w.k, w.v, ones, 32, 32, kv_lens=[0])
+    assert np.all(O == 0.0) and np.all(np.isneginf(L))
+
+
+@pytest.mark.parametrize("bq,bk", [(32, 32), (64, 32), (32, 64)])
+def test_element_mask_forms_agree(bq, bk):
+    w = _problem(45, 2, 2, 1, 128, 256, 32, bq, bk, 0.6)
+    lens = [200, 131]
+    O1, L1 = OA.dense_masked(w.q, w.k, w.v, w.mask, bq, bk, causal=True, kv_lens=lens)
+    O2, L2 = OA.block_gather(w.q, w.k, w.v, w.mask, bq, bk, causal=True, kv_lens=lens)
+    np.testing.assert_allclose(O1, O2, rtol=0, atol=1e-12)
+    assert np.array_equal(np.isneginf(L1), np.isneginf(L2))
+    fin = np.isfinite(L1)
+    np.testing.assert_allclose(L1[fin], L2[fin], rtol=0, atol=1e-12)
