@@ -19,6 +19,13 @@ STATUS_NAMES = {
     -4: "BSA_ERR_CUDA", -5: "BSA_ERR_WORKSPACE", -6: "BSA_ERR_TIMEOUT", -7: "BSA_ERR_PLAN_MISMATCH",
 }
 PLAN_NO_UNION = 0x1
+FWD_CAUSAL = 0x1
+
+
+class KVPagesC(ctypes.Structure):
+    """Mirror of bsa_kv_pages (include/bsa.h)."""
+    _fields_ = [("block_table", ctypes.c_void_p), ("max_pages", ctypes.c_int),
+                ("page_size", ctypes.c_int), ("num_pages", ctypes.c_int)]
 
 
 class BsaError(RuntimeError):
@@ -72,6 +79,8 @@ def library() -> ctypes.CDLL:
     lib.bsa_plan_destroy.argtypes = [P]
     lib.bsa_forward.restype = I
     lib.bsa_forward.argtypes = [P, VP, VP, VP, VP, VP, I, F, VP]
+    lib.bsa_forward_ex.restype = I
+    lib.bsa_forward_ex.argtypes = [P, VP, VP, VP, ctypes.POINTER(KVPagesC), VP, I, VP, VP, I, F, VP]
     lib.bsa_sync_status.restype = I
     lib.bsa_sync_status.argtypes = [P, VP, ctypes.POINTER(ctypes.c_int32)]
     lib.bsa_plan_check.restype = I
@@ -177,26 +186,56 @@ def plan(mask: torch.Tensor, bq: int, bk: int, gqa_group: int = 1, flags: int = 
 def forward(p: Plan, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
             scale: Optional[float] = None,
-            stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Block-sparse attention over plan ``p`` (bsa_forward).  Returns (O, LSE)."""
+            stream: Optional[torch.cuda.Stream] = None,
+            block_table: Optional[torch.Tensor] = None,
+            kv_lens: Optional[torch.Tensor] = None,
+            causal: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Block-sparse attention over plan ``p``.  Returns (O, LSE).
+
+    Contiguous K/V: k, v [B, Hkv, Nk, d].  Paged K/V (``block_table`` given,
+    int32 CUDA [B, max_pages]): k, v are pools [num_pages, Hkv, page_size, d].
+    ``kv_lens`` (int32 CUDA [B]) and ``causal`` mask keys inside the selected
+    blocks (bsa_forward_ex)."""
     L = p.layout
     for name, t in (("q", q), ("k", k), ("v", v)):
         if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
-            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor [B, H, N, d]")
+            raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor with 4 dimensions")
     B, Hq, Nq, d = q.shape
     if (B, Hq, Nq) != (L.B, L.H, L.NQB * L.bq):
         raise ValueError("q shape does not match the plan")
-    if tuple(k.shape) != (L.B, L.Hkv, L.NKB * L.bk, d) or k.shape != v.shape:
-        raise ValueError("k/v shape does not match the plan")
+    if k.shape != v.shape:
+        raise ValueError("k and v shapes differ")
+    pages = None
+    if block_table is None:
+        if tuple(k.shape) != (L.B, L.Hkv, L.NKB * L.bk, d):
+            raise ValueError("k/v shape does not match the plan")
+    else:
+        if (block_table.dtype != torch.int32 or not block_table.is_cuda or block_table.dim() != 2
+                or not block_table.is_contiguous() or block_table.shape[0] != L.B):
+            raise ValueError("block_table must be a contiguous CUDA int32 tensor [B, max_pages]")
+        if k.shape[1] != L.Hkv or k.shape[3] != d:
+            raise ValueError("k/v pools must be [num_pages, Hkv, page_size, d]")
+        pages = KVPagesC(block_table.data_ptr(), block_table.shape[1], k.shape[2], k.shape[0])
+    if kv_lens is not None and (kv_lens.dtype != torch.int32 or not kv_lens.is_cuda
+                                or tuple(kv_lens.shape) != (L.B,)):
+        raise ValueError("kv_lens must be a CUDA int32 tensor [B]")
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device)
     sc = 0.0 if scale is None else float(scale)
-    _check(library().bsa_forward(
-        p.handle, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
-        ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
-        ctypes.c_void_p(lse.data_ptr()), d, sc, _stream_ptr(stream)), "bsa_forward")
+    if pages is None and kv_lens is None and not causal:
+        _check(library().bsa_forward(
+            p.handle, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+            ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+            ctypes.c_void_p(lse.data_ptr()), d, sc, _stream_ptr(stream)), "bsa_forward")
+    else:
+        _check(library().bsa_forward_ex(
+            p.handle, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+            ctypes.c_void_p(v.data_ptr()), ctypes.byref(pages) if pages is not None else None,
+            ctypes.c_void_p(kv_lens.data_ptr()) if kv_lens is not None else None,
+            FWD_CAUSAL if causal else 0, ctypes.c_void_p(out.data_ptr()),
+            ctypes.c_void_p(lse.data_ptr()), d, sc, _stream_ptr(stream)), "bsa_forward_ex")
     return out, lse
 
 

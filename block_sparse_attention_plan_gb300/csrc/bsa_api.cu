@@ -240,10 +240,18 @@ void bsa_plan_destroy(bsa_plan* plan) {
 
 bsa_status bsa_forward(const bsa_plan* plan, const void* Q, const void* K, const void* V, void* O,
                        float* LSE, int d, float scale, void* stream) {
+  return bsa_forward_ex(plan, Q, K, V, nullptr, nullptr, 0, O, LSE, d, scale, stream);
+}
+
+bsa_status bsa_forward_ex(const bsa_plan* plan, const void* Q, const void* K, const void* V,
+                          const bsa_kv_pages* pages, const int32_t* kv_lens, int flags,
+                          void* O, float* LSE, int d, float scale, void* stream) {
   const PlanImpl* p = as_impl(plan);
   if (!plan) return BSA_ERR_INVALID_ARG;
   if (!p) return BSA_ERR_PLAN_MISMATCH;
   if (!Q || !K || !V || !O || !LSE) return BSA_ERR_INVALID_ARG;
+  if (flags & ~BSA_FWD_CAUSAL) return BSA_ERR_INVALID_ARG;
+  if (kv_lens && (reinterpret_cast<uintptr_t>(kv_lens) & 3u)) return BSA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
     return BSA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return BSA_ERR_UNSUPPORTED;
@@ -254,7 +262,16 @@ bsa_status bsa_forward(const bsa_plan* plan, const void* Q, const void* K, const
   if (dev != p->device) return BSA_ERR_PLAN_MISMATCH;
   const bsa_plan_layout& L = p->L;
   const long long Nq = (long long)L.NQB * L.bq, Nk = (long long)L.NKB * L.bk;
-  const long long qrows = (long long)L.B * L.H * Nq, kvrows = (long long)L.B * L.Hkv * Nk;
+  const long long qrows = (long long)L.B * L.H * Nq;
+  long long kvrows = (long long)L.B * L.Hkv * Nk;
+  if (pages) {
+    if (!pages->block_table || pages->max_pages < 1 || pages->page_size < 1 || pages->num_pages < 1)
+      return BSA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(pages->block_table) & 3u) return BSA_ERR_INVALID_ARG;
+    if (pages->page_size % L.ku) return BSA_ERR_UNSUPPORTED;
+    if ((long long)pages->max_pages * pages->page_size < Nk) return BSA_ERR_INVALID_ARG;
+    kvrows = (long long)pages->num_pages * L.Hkv * pages->page_size;
+  }
   if (qrows >= (1ll << 31) || kvrows >= (1ll << 31)) return BSA_ERR_UNSUPPORTED;
 
   FwdParams fp;
@@ -279,6 +296,16 @@ bsa_status bsa_forward(const bsa_plan* plan, const void* Q, const void* K, const
   fp.fb_list = reinterpret_cast<int32_t*>(p->ws + fs.off_fb_list);
   fp.slot_capacity = L.slot_capacity;
   fp.watchdog_ns = env_ll("BSA_WATCHDOG_MS", 1000) * 1000000ll;
+  if (pages) {
+    fp.block_table = pages->block_table;
+    fp.max_pages = pages->max_pages;
+    fp.page_size = pages->page_size;
+    fp.num_pages = pages->num_pages;
+  }
+  fp.kv_lens = kv_lens;
+  fp.causal = (flags & BSA_FWD_CAUSAL) ? 1 : 0;
+  fp.causal_off = (int)(Nk - Nq);
+  fp.elem_mask = (fp.causal || kv_lens) ? 1 : 0;
   fp.B = L.B; fp.H = L.H; fp.Hkv = L.Hkv; fp.g = L.gqa_group; fp.NQT = L.NQT; fp.NKU = L.NKU;
   fp.Nq = (int)Nq; fp.Nk = (int)Nk; fp.rq = L.rq; fp.rk = L.rk; fp.qu = L.qu; fp.ku = L.ku;
   fp.rows = L.rows;

@@ -223,6 +223,25 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 }
 
 // ------------------------------------------------------------------ producers
+// Row of K unit y of the item's K/V head in the TMA view of the paged pools
+// [num_pages*Hkv*page_size, d] (contiguous K/V use kvrow0 + y*ku).  A page
+// outside the table is an error only when the unit holds keys within the
+// sequence's key length (beyond it the keys are masked, so any valid page
+// serves).
+__device__ __forceinline__ int unit_row(const FwdParams& p, const Item& m, int y) {
+  if (p.block_table == nullptr) return m.kvrow0 + y * p.ku;
+  const int b = m.bh / p.H, hkv = (m.bh % p.H) / p.g;
+  const int key = y * p.ku;
+  const int lp = key / p.page_size, off = key % p.page_size;
+  int phys = (lp < p.max_pages) ? __ldg(p.block_table + (size_t)b * p.max_pages + lp) : -1;
+  if (phys < 0 || phys >= p.num_pages) {
+    const bool live = p.kv_lens == nullptr || key < __ldg(p.kv_lens + b);
+    if (live) record_status(p.control, -7, kSitePlanRange + 4);
+    phys = 0;
+  }
+  return (phys * p.Hkv + hkv) * p.page_size + off;
+}
+
 // K/V units of one slot as the plan lists them (rk <= 4 entries, -1 = padding).
 // A producer reads them two slots ahead, so the global-load latency overlaps
 // its stage waits instead of sitting between a stage freeing and its copy.
@@ -246,7 +265,7 @@ struct Ring {
 };
 
 // Gather the 128 keys of one slot into the next stage of `r`.
-template <int D>
+template <int D, bool kGeneral>
 __device__ __forceinline__ bool load_tile(const FwdParams& p, const CUtensorMap* map, const Ring& r,
                                           const Item& m, const SlotKeys& keys, uint32_t& it,
                                           uint64_t pol, const Watchdog& wd) {
@@ -272,7 +291,7 @@ __device__ __forceinline__ bool load_tile(const FwdParams& p, const CUtensorMap*
       record_status(p.control, -7, kSitePlanRange + 3);
       y = first;
     }
-    const int row = m.kvrow0 + y * p.ku;
+    const int row = kGeneral ? unit_row(p, m, y) : m.kvrow0 + y * p.ku;
 #pragma unroll
     for (int c = 0; c < C::kChunks; ++c)
       tma_load_2d(dst0 + c * C::kChunkBytes + u * p.ku * 128, map, c * 64, row, full, pol);
@@ -285,7 +304,7 @@ __device__ __forceinline__ bool load_tile(const FwdParams& p, const CUtensorMap*
 // them, loads each row's Q tile and the K tile of every slot.  V producer:
 // reads the published items and loads the V tile of every slot.  Both load in
 // slot order, which is the order the MMA thread consumes each ring in.
-template <int D>
+template <int D, bool kGeneral>
 __device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, const Smem<D> sm,
                                            const Watchdog wd, bool kside) {
   using C = Cfg<D>;
@@ -338,7 +357,7 @@ __device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, co
     for (int j = 0; j < m.n && ok; ++j) {
       SlotKeys k2 = k1;
       if (j + 2 < m.n) k2 = fetch_keys(p, m, j + 2);
-      ok = load_tile<D>(p, map, r, m, k0, kv_it, pol_kv, wd);
+      ok = load_tile<D, kGeneral>(p, map, r, m, k0, kv_it, pol_kv, wd);
       k0 = k1;
       k1 = k2;
     }
@@ -501,7 +520,7 @@ __device__ __noinline__ void pv_issuer_role(const FwdParams& p, const uint8_t* s
 // was far above its scores) is queued for the exact pass.
 // Exact pass (kExact = true): the running row maximum, agreed between the
 // two threads of a row, with a lazy rescale of O.
-template <int D, bool kExact>
+template <int D, bool kExact, bool kGeneral>
 __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, const Smem<D>& sm,
                                              uint32_t tmem, const Watchdog& wd) {
   using C = Cfg<D>;
@@ -520,6 +539,12 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   float* xbuf = reinterpret_cast<float*>(smem + C::kOffX);
   uint32_t sg = 0, rows = 0, xc = 0, q_it = 0;
   uint32_t bits = 0xffffffffu;  // this row's sub-mask bits for the current slot
+  // Element mask (causal / key lengths): key position of the first key of each
+  // of this thread's two 32-key chunks of the current slot (-1: padding), the
+  // last key position this row keeps, and the smallest of that over the warp.
+  int cbase[2] = {0, 0};
+  int lim_row = 0x7fffffff, lim_warp = 0x7fffffff;
+  bool live = false;  // some key of this thread's columns kept in the current slot
 
   // One float per row with the thread of the other key half that owns the
   // same row (warp quad + 4 <-> quad + 8); double-buffered by round parity.
@@ -556,6 +581,25 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         if (!((bits >> ((2 * h + c) >> ku_shift)) & 1u)) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[c * 32 + e] = __float_as_uint(-INFINITY);
+        }
+      }
+    }
+    live = !submask || bits != 0u;  // the row keeps a key of this slot (block level)
+    if constexpr (kGeneral) {
+      if (p.elem_mask) {
+        live = false;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (submask && !((bits >> ((2 * h + c) >> ku_shift)) & 1u)) continue;
+          // Keys base .. base+31 (ascending): all kept for every row of the
+          // warp when the last one is within the warp's smallest limit
+          // (warp-uniform); otherwise per element.
+          const int base = cbase[c];
+          live |= (base >= 0 && base <= lim_row);
+          if (base >= 0 && base + 31 <= lim_warp) continue;
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (base < 0 || base + e > lim_row) v[c * 32 + e] = __float_as_uint(-INFINITY);
         }
       }
     }
@@ -635,13 +679,27 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     __syncwarp();
     if (lane == 0) mbar_arrive(sm.bar(C::kBarQEmpty + qb));
     ++q_it;
+    if (kGeneral && p.elem_mask) {
+      const int qpos = m.qt * 128 + rloc, qmin = m.qt * 128 + quad * 32;
+      const int kvl = p.kv_lens ? __ldg(p.kv_lens + m.bh / p.H) : 0x7fffffff;
+      lim_row = min(p.causal ? qpos + p.causal_off : 0x7fffffff, kvl - 1);
+      lim_warp = min(p.causal ? qmin + p.causal_off : 0x7fffffff, kvl - 1);
+    }
     float l_run = 0.f, lw_run = 0.f;  // exact and bf16-weight row sums
-    bool has_keys = !submask;         // (bounded pass) some key of the row is selected
+    bool has_keys = false;            // (bounded pass) some key of this thread's columns is kept
     bool ok = true;
     for (int j = 0; j < m.n; ++j) {
       const int b = (int)(sg & 1u);
       const uint32_t u = sg >> 1;
       if (submask) bits = (__ldg(p.slot_mask + m.s0 + j) >> (qi * p.rk)) & my_bits_mask;
+      if (kGeneral && p.elem_mask) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int col0 = 64 * h + 32 * c;
+          const int y = __ldg(p.slot_ku + (size_t)(m.s0 + j) * p.rk + col0 / p.ku);
+          cbase[c] = (y < 0) ? -1 : y * p.ku + col0 % p.ku;
+        }
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarSFull + b), u & 1u, wd, kSiteSFull))) {
         ok = false;
         break;
@@ -657,7 +715,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       float sum, sum_w, factor = 1.f;
       const uint32_t pcol = tmem + tl + kColP + 64u * (uint32_t)b + 32u * (uint32_t)h;
       if constexpr (!kExact) {
-        if (submask) has_keys |= (bits != 0u);
+        has_keys |= live;  // (set by load_s)
         sum = exp_pack(v, pk, m_ref, std::false_type{}, nullptr, &sum_w);
         // P buffer b was last read by the P V of slot g - 2.
         if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
@@ -772,8 +830,13 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     const float L = l_run + l_other, Lw = lw_run + lw_other;
     const float inv = (Lw > 0.f) ? 1.f / Lw : 0.f;
     if constexpr (!kExact) {
-      // Both threads of a row compute the same L and has_keys.
-      const bool need = has_keys && !(Lw >= kFallbackPerKey * (float)(m.n * 128));
+      // Whether the row keeps any key: without an element mask both threads
+      // see the same sub-mask bits; with one, they combine their columns.
+      float hk_other = has_keys ? 1.f : 0.f;
+      if (kGeneral && p.elem_mask && !exchange(has_keys ? 1.f : 0.f, hk_other)) break;
+      const bool row_keys = has_keys || hk_other > 0.f;
+      // Both threads of a row compute the same Lw and row_keys.
+      const bool need = row_keys && !(Lw >= kFallbackPerKey * (float)(m.n * 128));
       if (__any_sync(0xffffffffu, need) && lane == 0) {
         if (atomicExch(p.fb_flag + m.row, 1) == 0)
           p.fb_list[atomicAdd(p.control + kCtlFallbackCount, 1)] = m.row;
@@ -802,7 +865,9 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   }
 }
 
-template <int D, bool kExact>
+// kGeneral: paged K/V and/or element masks (runtime-selected inside); the
+// plain instantiation carries none of that code.
+template <int D, bool kExact, bool kGeneral>
 __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -854,14 +919,14 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
 
   if (warp >= 4) {
     regs_inc<kRegsSoftmax>();
-    softmax_role<D, kExact>(p, smem, sm, tmem, wd);
+    softmax_role<D, kExact, kGeneral>(p, smem, sm, tmem, wd);
   } else {
     regs_dec<kRegsControl>();
     if (lane == 0 && !*abort_flag) {
-      if (warp == 0) producer_role<D>(p, smem, sm, wd, true);
+      if (warp == 0) producer_role<D, kGeneral>(p, smem, sm, wd, true);
       else if (warp == 1) s_issuer_role<D>(p, smem, sm, tmem, wd);
       else if (warp == 2) pv_issuer_role<D>(p, smem, sm, tmem, wd);
-      else if (warp == 3) producer_role<D>(p, smem, sm, wd, false);
+      else if (warp == 3) producer_role<D, kGeneral>(p, smem, sm, wd, false);
     }
   }
 
@@ -887,51 +952,63 @@ __global__ void watchdog_selftest_kernel(int32_t* status, long long limit_ns) {
   if (mbar_wait(bar, 0, wd, kSiteSelftest)) status[3] = 1;
 }
 
-template <int D, bool kExact>
+template <int D, bool kExact, bool kGeneral>
 cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t stream) {
   const int smem = Cfg<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(bsa_fwd_kernel<D, kExact>,
+  cudaError_t e = cudaFuncSetAttribute(bsa_fwd_kernel<D, kExact, kGeneral>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  bsa_fwd_kernel<D, kExact><<<grid, kThreads, smem, stream>>>(p);
+  bsa_fwd_kernel<D, kExact, kGeneral><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 // Largest key norm of every K unit (ku rows) of every K/V head, i.e. a bound
 // on |k| for the Cauchy-Schwarz reference of the bounded pass; also clears
 // the fallback flags.  One warp per unit, one row per lane at a time with the
-// row's d/8 16-byte loads all in flight; one reduction at the end.
+// row's d/8 16-byte loads all in flight; one reduction at the end.  Units
+// wholly past the sequence's key length (or, paged, without a valid page)
+// get 0 and are not read: their keys are masked.
 template <int D>
-__global__ void __launch_bounds__(256) kmax_kernel(const uint16_t* __restrict__ K,
-                                                   float* __restrict__ kmax, int units, int ku,
-                                                   int32_t* __restrict__ fb_flag, int rows) {
+__global__ void __launch_bounds__(256) kmax_kernel(const FwdParams p) {
   const int tid = blockIdx.x * blockDim.x + threadIdx.x;
-  for (int i = tid; i < rows; i += gridDim.x * blockDim.x) fb_flag[i] = 0;
+  for (int i = tid; i < p.rows; i += gridDim.x * blockDim.x) p.fb_flag[i] = 0;
   const int unit = tid >> 5, lane = threadIdx.x & 31;
-  if (unit >= units) return;
-  // K units are contiguous in the [B*Hkv*Nk, d] view: unit i covers rows [i*ku, (i+1)*ku).
+  if (unit >= p.B * p.Hkv * p.NKU) return;
+  const int head = unit / p.NKU, y = unit % p.NKU;  // head = b * Hkv + hkv
+  const int b = head / p.Hkv, hkv = head % p.Hkv;
+  const int key = y * p.ku;
+  long long row0 = (long long)unit * p.ku;  // contiguous: units in row order
+  bool skip = p.kv_lens != nullptr && key >= __ldg(p.kv_lens + b);
+  if (p.block_table != nullptr && !skip) {
+    const int lp = key / p.page_size;
+    const int phys = (lp < p.max_pages) ? __ldg(p.block_table + (size_t)b * p.max_pages + lp) : -1;
+    if (phys < 0 || phys >= p.num_pages) skip = true;
+    else row0 = ((long long)phys * p.Hkv + hkv) * p.page_size + key % p.page_size;
+  }
   float best = 0.f;
-  for (int r = lane; r < ku; r += 32) {
-    const uint4* src = reinterpret_cast<const uint4*>(K + ((size_t)unit * ku + r) * D);
-    uint4 x[D / 8];
+  if (!skip) {
+    for (int r = lane; r < p.ku; r += 32) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.K + (size_t)(row0 + r) * D);
+      uint4 x[D / 8];
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) x[c] = __ldg(src + c);
-    float s2a = 0.f, s2b = 0.f;
+      for (int c = 0; c < D / 8; ++c) x[c] = __ldg(src + c);
+      float s2a = 0.f, s2b = 0.f;
 #pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      const uint32_t w4[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
+      for (int c = 0; c < D / 8; ++c) {
+        const uint32_t w4[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
-        s2a = fmaf(lo, lo, s2a);
-        s2b = fmaf(hi, hi, s2b);
+        for (int e = 0; e < 4; ++e) {
+          const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
+          s2a = fmaf(lo, lo, s2a);
+          s2b = fmaf(hi, hi, s2b);
+        }
       }
+      best = fmaxf(best, s2a + s2b);
     }
-    best = fmaxf(best, s2a + s2b);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
-  if (lane == 0) kmax[unit] = sqrtf(best);
+  if (lane == 0) p.kmax[unit] = sqrtf(best);
 }
 
 // Largest key norm over the K units of each plan row's slots (one warp per
@@ -958,8 +1035,7 @@ template <int D>
 cudaError_t launch_passes(const FwdParams& p, int grid, cudaStream_t stream) {
   const long long units = (long long)p.B * p.Hkv * p.NKU;
   const long long blocks = (units + 7) / 8;
-  kmax_kernel<D><<<(unsigned)(blocks > 0 ? blocks : 1), 256, 0, stream>>>(p.K, p.kmax, (int)units,
-                                                                        p.ku, p.fb_flag, p.rows);
+  kmax_kernel<D><<<(unsigned)(blocks > 0 ? blocks : 1), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   rowbound_kernel<<<(unsigned)((p.rows + 7) / 8), 256, 0, stream>>>(p);
@@ -968,14 +1044,15 @@ cudaError_t launch_passes(const FwdParams& p, int grid, cudaStream_t stream) {
   FwdParams a = p;
   a.work_counter = p.control + kCtlWorkCounter;
   a.work_count = nullptr;
-  e = launch_d<D, false>(a, grid, stream);
+  const bool general = p.block_table != nullptr || p.elem_mask;
+  e = general ? launch_d<D, false, true>(a, grid, stream) : launch_d<D, false, false>(a, grid, stream);
   if (e != cudaSuccess) return e;
   // Exact pass over the queued rows (exits at once when none was queued).
   FwdParams x = p;
   x.order = p.fb_list;
   x.work_counter = p.control + kCtlFallbackWork;
   x.work_count = p.control + kCtlFallbackCount;
-  return launch_d<D, true>(x, grid, stream);
+  return general ? launch_d<D, true, true>(x, grid, stream) : launch_d<D, true, false>(x, grid, stream);
 }
 
 }  // namespace

@@ -85,6 +85,14 @@ struct FwdParams {
   float* rowk;           // largest key norm over each plan row's K units
   int32_t* fb_flag;      // per plan row: queued for the exact pass
   int32_t* fb_list;      // plan rows queued for the exact pass
+  // Paged K/V (block_table == nullptr: contiguous [B*Hkv*Nk, d]).
+  const int32_t* block_table;    // [B][max_pages] physical page per logical page
+  int max_pages, page_size, num_pages;
+  // Element mask inside selected blocks.
+  const int32_t* kv_lens;        // [B] or nullptr
+  int causal;                    // key j visible to query i iff j <= i + causal_off
+  int causal_off;                // Nk - Nq
+  int elem_mask;                 // causal || kv_lens
   int32_t* work_counter;         // set by launch_forward: the pass's work counter
   const int32_t* work_count;     // number of work items (nullptr: rows)
   long long slot_capacity;

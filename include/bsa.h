@@ -142,12 +142,58 @@ void bsa_plan_destroy(bsa_plan* plan);
  * (written; natural log, -inf for rows with no selected key).  All 16-byte
  * aligned; Q/K/V/O must not alias.  d in {64, 128}.  scale <= 0 selects
  * 1/sqrt(d).  Nq, Nk, Hkv and the block sizes come from the plan.
- * Enqueues one memset of the plan's control words and one persistent kernel
- * on `stream`.  Errors: BSA_ERR_INVALID_ARG, BSA_ERR_UNSUPPORTED,
- * BSA_ERR_PLAN_MISMATCH (NULL/foreign plan), BSA_ERR_ARCH, BSA_ERR_CUDA.
+ * Enqueues one memset of the plan's control words and four kernels on
+ * `stream`: the key-norm and row-bound passes, the forward pass over every
+ * plan row, and an exact second pass over the rows the first one queued (it
+ * exits at once when none was).  Errors: BSA_ERR_INVALID_ARG,
+ * BSA_ERR_UNSUPPORTED, BSA_ERR_PLAN_MISMATCH (NULL/foreign plan),
+ * BSA_ERR_ARCH, BSA_ERR_CUDA.  Same as bsa_forward_ex with no pages, no key
+ * lengths and no flags.
  */
 bsa_status bsa_forward(const bsa_plan* plan, const void* Q, const void* K, const void* V,
                        void* O, float* LSE, int d, float scale, void* stream);
+
+/*
+ * Paged K/V for bsa_forward_ex ("CompactAttention: Accelerating Chunked
+ * Prefill with Block-Union KV Selection", summary: zero-copy paged attention
+ * execution; the PagedAttention entry of the related-papers list on the
+ * "TiledAttention" page: on-demand page allocation of the KV cache).
+ * The K and V pools are device bf16 [num_pages][Hkv][page_size][d]; key
+ * position j of sequence b lives in physical page
+ * block_table[b * max_pages + j / page_size], row j % page_size.
+ * page_size must be a positive multiple of the plan's K unit min(bk, 128)
+ * (so a unit never straddles two pages); max_pages * page_size >= Nk.
+ */
+typedef struct bsa_kv_pages {
+  const int32_t* block_table;  /* device int32 [B][max_pages], caller-owned */
+  int max_pages;               /* logical pages per sequence */
+  int page_size;               /* keys per page */
+  int num_pages;               /* pages in each pool */
+} bsa_kv_pages;
+
+/* Intra-block causal masking: key position j is visible to query position i
+ * only when j <= i + (Nk - Nq) (queries are the last Nq positions). */
+#define BSA_FWD_CAUSAL 0x1
+
+/*
+ * bsa_forward_ex -- bsa_forward with paged K/V, per-sequence key lengths and
+ * intra-block causal masking.  Within every block the mask selects, element
+ * (i, j) is dropped when BSA_FWD_CAUSAL is set and j > i + Nk - Nq, or when
+ * kv_lens is given and j >= kv_lens[b]; a row left with no key gets O = 0
+ * and LSE = -inf, as a row with no selected block does.
+ * pages: NULL for contiguous K, V [B][Hkv][Nk][d]; else K and V are the
+ *   pools described above.
+ * kv_lens: NULL, or device int32 [B] (each in [0, Nk]), caller-owned.
+ * flags: 0 or BSA_FWD_CAUSAL.
+ * Other arguments and errors as bsa_forward; additionally
+ * BSA_ERR_UNSUPPORTED for a page size that is not a multiple of the K unit
+ * and BSA_ERR_INVALID_ARG for a NULL block table, non-positive sizes or
+ * unknown flags.  A block-table entry outside [0, num_pages) is skipped and
+ * reported by bsa_sync_status as BSA_ERR_PLAN_MISMATCH.
+ */
+bsa_status bsa_forward_ex(const bsa_plan* plan, const void* Q, const void* K, const void* V,
+                          const bsa_kv_pages* pages, const int32_t* kv_lens, int flags,
+                          void* O, float* LSE, int d, float scale, void* stream);
 
 /*
  * bsa_sync_status -- synchronise `stream`, then report the status word the
