@@ -254,6 +254,24 @@ def run_gb300(args):
 
     mask_d = w.mask.to(dev)
     q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
+    fwd_extra = {"causal": bool(args.causal)}
+    if args.page_size:
+        # paged K/V: the sequence's pages scattered over the pools in a seeded
+        # random order, read through the block table (bsa_forward_ex)
+        ps = args.page_size
+        B_, Hkv_, Nk_, d_ = k.shape
+        if Nk_ % ps:
+            raise SystemExit(f"--page-size {ps} does not divide Nk = {Nk_}")
+        npg = Nk_ // ps
+        perm = torch.randperm(B_ * npg, generator=torch.Generator().manual_seed(5)).to(dev)
+
+        def to_pool(t):
+            pages = t.view(B_, Hkv_, npg, ps, d_).permute(0, 2, 1, 3, 4).reshape(B_ * npg, Hkv_, ps, d_)
+            pool = torch.empty(pages.shape, dtype=pages.dtype, device=dev)
+            pool[perm] = pages
+            return pool
+        k, v = to_pool(k), to_pool(v)
+        fwd_extra["block_table"] = perm.view(B_, npg).to(torch.int32).contiguous()
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
     L = bsa.plan_layout(*w.mask.shape, w.bq, w.bk, w.gqa_group)
@@ -266,7 +284,7 @@ def run_gb300(args):
         p = bsa.plan(mask_d, w.bq, w.bk, w.gqa_group, workspace=wsbuf)
         if ev is not None:
             ev[0].record(stream)
-        bsa.forward(p, q, k, v, out=o, lse=lse)
+        bsa.forward(p, q, k, v, out=o, lse=lse, **fwd_extra)
         if ev is not None:
             ev[1].record(stream)
         return p
@@ -338,14 +356,22 @@ def run_gb300(args):
 
     value = flop * ws / (ms * 1e-3) / 1e12
     achieved = flop / (fwd_ms * 1e-3) / 1e12
+    cfg = _config(w)
+    if args.page_size:
+        cfg["kv_pages"] = (f"page_size {args.page_size}, pages shuffled across the pool, read "
+                           "through a block table (e2e stays on contiguous host buffers)")
+    if args.causal:
+        cfg["causal"] = ("intra-block causal element mask; FLOP counted over whole selected "
+                         "blocks, as the tensor cores execute them")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(w),
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
         "pct_of_peak": 100.0 * value / ws / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
-                     "traffic": args.traffic if args.traffic is not None else _traffic(w.name),
+                     "traffic": (args.traffic if args.traffic is not None else
+                                 None if (args.page_size or args.causal) else _traffic(w.name)),
                      # forward_ms spans the whole bsa_forward call: key-norm and
                      # row-bound passes, the bounded pass (the dominant kernel)
                      # and the exact pass over queued rows.
@@ -378,6 +404,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--page-size", type=int, default=0,
+                    help="read K/V through a block table of pages of this many keys (0: contiguous)")
+    ap.add_argument("--causal", action="store_true",
+                    help="intra-block causal masking (queries are the last Nq positions)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per forward launch from an ncu capture of this kernel")
     args = ap.parse_args()

@@ -543,8 +543,12 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   // of this thread's two 32-key chunks of the current slot (-1: padding), the
   // last key position this row keeps, and the smallest of that over the warp.
   int cbase[2] = {0, 0};
-  int lim_row = 0x7fffffff, lim_warp = 0x7fffffff;
+  int lim_row = 0x7fffffff, lim_warp = 0x7fffffff, lim_warp_hi = 0x7fffffff;
   bool live = false;  // some key of this thread's columns kept in the current slot
+  // Bit c: 32-key chunk c of this thread's columns may hold a kept key for
+  // some row of the warp (warp-uniform).  The exponentials of a chunk without
+  // one are skipped: its weights are +0 either way.
+  uint32_t chunks = 3u;
 
   // One float per row with the thread of the other key half that owns the
   // same row (warp quad + 4 <-> quad + 8); double-buffered by round parity.
@@ -573,14 +577,20 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     tmem_ld32_at<0>(sbuf + 64u * (uint32_t)h, v);
     tmem_ld32_at<32>(sbuf + 64u * (uint32_t)h + 32u, v);
     tmem_wait_ld();
+    chunks = 3u;
     if (submask) {
       // 32-key chunk 2h + c lies in k-unit (2h + c) >> ku_shift; a warp's rows
-      // share one q-unit, so the branch is warp-uniform.
+      // share one q-unit, so the branch is warp-uniform.  The bounded pass
+      // never reads a dropped chunk's scores; the exact pass takes maxima
+      // over all 64, so there they become -inf.
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         if (!((bits >> ((2 * h + c) >> ku_shift)) & 1u)) {
+          chunks &= ~(1u << c);
+          if constexpr (kExact) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[c * 32 + e] = __float_as_uint(-INFINITY);
+            for (int e = 0; e < 32; ++e) v[c * 32 + e] = __float_as_uint(-INFINITY);
+          }
         }
       }
     }
@@ -597,6 +607,10 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
           const int base = cbase[c];
           live |= (base >= 0 && base <= lim_row);
           if (base >= 0 && base + 31 <= lim_warp) continue;
+          if (base < 0 || base > lim_warp_hi) {  // no row of the warp keeps a key of it
+            chunks &= ~(1u << c);
+            if constexpr (!kExact) continue;
+          }
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             if (base < 0 || base + e > lim_row) v[c * 32 + e] = __float_as_uint(-INFINITY);
@@ -608,28 +622,31 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   // Returns the sum of the 64 values of p; *sum_w gets the sum of the same
   // values as rounded to bf16, i.e. of the weights the P V product applies
   // (O is divided by that sum, so exactly those weights are normalised; the
-  // log-sum-exp uses the exact one).  With kMax, also the maximum of the raw
-  // scores in *mx.
-  auto exp_pack = [&](const uint32_t (&v)[64], uint32_t (&pk)[32], float m, auto with_max,
-                      float* mx, float* sum_w) -> float {
-    constexpr bool kMax = decltype(with_max)::value;
+  // log-sum-exp uses the exact one).  Chunks dropped from `chunks` get +0
+  // weights without exponentials (adding +0 leaves the sums as they are).
+  auto exp_pack = [&](const uint32_t (&v)[64], uint32_t (&pk)[32], float m, float* sum_w) -> float {
     const float mb = (m == -INFINITY) ? 0.f : m;
     const uint64_t nmbx2 = f2_make(-mb, -mb);
     uint64_t acc2[2] = {0ull, 0ull};
     float accw[4] = {0.f, 0.f, 0.f, 0.f};
-    float mx2[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const float a0 = __uint_as_float(v[2 * e]), a1 = __uint_as_float(v[2 * e + 1]);
-      if (kMax) mx2[e & 1] = fmax3(mx2[e & 1], a0, a1);
-      float x0, x1;
-      f2_split(ffma2(f2_make(a0, a1), sl2x2, nmbx2), x0, x1);
-      const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-      pk[e] = pack_bf16x2(p0, p1);
-      acc2[e & 1] = fadd2(acc2[e & 1], f2_make(p0, p1));
-      add_bf16x2_f32(accw[2 * (e & 1)], accw[2 * (e & 1) + 1], pk[e]);
+    for (int c = 0; c < 2; ++c) {
+      if (chunks & (1u << c)) {
+#pragma unroll
+        for (int e = 16 * c; e < 16 * c + 16; ++e) {
+          float x0, x1;
+          f2_split(ffma2(f2_make(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sl2x2, nmbx2),
+                   x0, x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          pk[e] = pack_bf16x2(p0, p1);
+          acc2[e & 1] = fadd2(acc2[e & 1], f2_make(p0, p1));
+          add_bf16x2_f32(accw[2 * (e & 1)], accw[2 * (e & 1) + 1], pk[e]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 16 * c; e < 16 * c + 16; ++e) pk[e] = 0u;
+      }
     }
-    if (kMax) *mx = fmaxf(mx2[0], mx2[1]);
     *sum_w = (accw[0] + accw[1]) + (accw[2] + accw[3]);
     float s0, s1, s2, s3;
     f2_split(acc2[0], s0, s1);
@@ -684,6 +701,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       const int kvl = p.kv_lens ? __ldg(p.kv_lens + m.bh / p.H) : 0x7fffffff;
       lim_row = min(p.causal ? qpos + p.causal_off : 0x7fffffff, kvl - 1);
       lim_warp = min(p.causal ? qmin + p.causal_off : 0x7fffffff, kvl - 1);
+      lim_warp_hi = min(p.causal ? qmin + 31 + p.causal_off : 0x7fffffff, kvl - 1);
     }
     float l_run = 0.f, lw_run = 0.f;  // exact and bf16-weight row sums
     bool has_keys = false;            // (bounded pass) some key of this thread's columns is kept
@@ -695,9 +713,9 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       if (kGeneral && p.elem_mask) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const int col0 = 64 * h + 32 * c;
-          const int y = __ldg(p.slot_ku + (size_t)(m.s0 + j) * p.rk + col0 / p.ku);
-          cbase[c] = (y < 0) ? -1 : y * p.ku + col0 % p.ku;
+          const int col0 = 64 * h + 32 * c;  // ku = 32 << ku_shift
+          const int y = __ldg(p.slot_ku + (size_t)(m.s0 + j) * p.rk + (col0 >> (5 + ku_shift)));
+          cbase[c] = (y < 0) ? -1 : (y << (5 + ku_shift)) + (col0 & (p.ku - 1));
         }
       }
       if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarSFull + b), u & 1u, wd, kSiteSFull))) {
@@ -716,7 +734,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       const uint32_t pcol = tmem + tl + kColP + 64u * (uint32_t)b + 32u * (uint32_t)h;
       if constexpr (!kExact) {
         has_keys |= live;  // (set by load_s)
-        sum = exp_pack(v, pk, m_ref, std::false_type{}, nullptr, &sum_w);
+        sum = exp_pack(v, pk, m_ref, &sum_w);
         // P buffer b was last read by the P V of slot g - 2.
         if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
           ok = false;
@@ -742,7 +760,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
           break;
         }
         m_ref = fmaxf(mx, mo) * sl2;  // stays -inf while every key so far is masked
-        sum = exp_pack(v, pk, m_ref, std::false_type{}, nullptr, &sum_w);
+        sum = exp_pack(v, pk, m_ref, &sum_w);
         if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
           ok = false;
           break;
@@ -751,7 +769,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       } else {
         // Exponentials against the current reference right away; whether a
         // rescale is due is settled while P is being written.
-        sum = exp_pack(v, pk, m_ref, std::false_type{}, nullptr, &sum_w);
+        sum = exp_pack(v, pk, m_ref, &sum_w);
         post(sum_w);
         if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
           ok = false;
@@ -787,7 +805,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
               factor = ex2_approx(m_ref - m_new);
               m_ref = m_new;
             }
-            sum = exp_pack(v, pk, m_ref, std::false_type{}, nullptr, &sum_w);
+            sum = exp_pack(v, pk, m_ref, &sum_w);
             // O changes scale: the P V of slot g - 1 must have finished with
             // it (the one of slot g starts only after this slot's P is
             // published).

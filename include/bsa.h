@@ -188,8 +188,12 @@ typedef struct bsa_kv_pages {
  * Other arguments and errors as bsa_forward; additionally
  * BSA_ERR_UNSUPPORTED for a page size that is not a multiple of the K unit
  * and BSA_ERR_INVALID_ARG for a NULL block table, non-positive sizes or
- * unknown flags.  A block-table entry outside [0, num_pages) is skipped and
- * reported by bsa_sync_status as BSA_ERR_PLAN_MISMATCH.
+ * unknown flags.  Keys at or past kv_lens[b] are masked out, so the entry
+ * of a page holding none below it may be anything (-1 for an unallocated
+ * page; the kernel then reads page 0 in its place and discards it); an entry
+ * outside [0, num_pages) for a page that holds a key below kv_lens[b] (every
+ * key when kv_lens is NULL) is skipped and reported by bsa_sync_status as
+ * BSA_ERR_PLAN_MISMATCH.
  */
 bsa_status bsa_forward_ex(const bsa_plan* plan, const void* Q, const void* K, const void* V,
                           const bsa_kv_pages* pages, const int32_t* kv_lens, int flags,
