@@ -301,6 +301,7 @@ bsa_status bsa_forward_ex(const bsa_plan* plan, const void* Q, const void* K, co
     fp.max_pages = pages->max_pages;
     fp.page_size = pages->page_size;
     fp.num_pages = pages->num_pages;
+    fp.prow = reinterpret_cast<int32_t*>(p->ws + fs.off_prow);
   }
   fp.kv_lens = kv_lens;
   fp.causal = (flags & BSA_FWD_CAUSAL) ? 1 : 0;

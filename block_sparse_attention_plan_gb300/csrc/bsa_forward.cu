@@ -223,34 +223,19 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 }
 
 // ------------------------------------------------------------------ producers
-// Row of K unit y of the item's K/V head in the TMA view of the paged pools
-// [num_pages*Hkv*page_size, d] (contiguous K/V use kvrow0 + y*ku).  A page
-// outside the table is an error only when the unit holds keys within the
-// sequence's key length (beyond it the keys are masked, so any valid page
-// serves).
-__device__ __forceinline__ int unit_row(const FwdParams& p, const Item& m, int y) {
-  if (p.block_table == nullptr) return m.kvrow0 + y * p.ku;
-  const int b = m.bh / p.H, hkv = (m.bh % p.H) / p.g;
-  const int key = y * p.ku;
-  const int lp = key / p.page_size, off = key % p.page_size;
-  int phys = (lp < p.max_pages) ? __ldg(p.block_table + (size_t)b * p.max_pages + lp) : -1;
-  if (phys < 0 || phys >= p.num_pages) {
-    const bool live = p.kv_lens == nullptr || key < __ldg(p.kv_lens + b);
-    if (live) record_status(p.control, -7, kSitePlanRange + 4);
-    phys = 0;
-  }
-  return (phys * p.Hkv + hkv) * p.page_size + off;
-}
-
-// K/V units of one slot as the plan lists them (rk <= 4 entries, -1 = padding).
-// A producer reads them two slots ahead, so the global-load latency overlaps
-// its stage waits instead of sitting between a stage freeing and its copy.
+// K/V units of one slot as the plan lists them (rk <= 4 entries, -1 = padding)
+// or, for paged K/V, their pool rows as the row-bound pass resolved them.  A
+// producer reads them two slots ahead, so the global-load latency overlaps
+// its stage waits instead of sitting between a stage freeing and its copy
+// (a block-table lookup there, dependent on the plan entry, cost the paged
+// path about 40 %).
 struct SlotKeys {
   int y[4];
 };
+template <bool kGeneral>
 __device__ __forceinline__ SlotKeys fetch_keys(const FwdParams& p, const Item& m, int j) {
   SlotKeys k;
-  const int32_t* ent = p.slot_ku + (size_t)(m.s0 + j) * p.rk;
+  const int32_t* ent = ((kGeneral && p.prow) ? p.prow : p.slot_ku) + (size_t)(m.s0 + j) * p.rk;
 #pragma unroll
   for (int u = 0; u < 4; ++u) k.y[u] = (u < p.rk) ? __ldg(ent + u) : -1;
   return k;
@@ -275,8 +260,9 @@ __device__ __forceinline__ bool load_tile(const FwdParams& p, const CUtensorMap*
   if (!mbar_wait(r.empty + 8u * stage, ph ^ 1u, wd, kSiteKvEmpty)) return false;
   const uint32_t full = r.full + 8u * stage;
   mbar_arrive_expect_tx(full, C::kTileBytes);
+  const bool paged = kGeneral && p.prow != nullptr;  // keys are pool rows
   int first = keys.y[0];
-  if (first < 0 || first >= p.NKU) {
+  if (first < 0 || (!paged && first >= p.NKU)) {
     record_status(p.control, -7, kSitePlanRange + 2);
     first = 0;
   }
@@ -287,11 +273,11 @@ __device__ __forceinline__ bool load_tile(const FwdParams& p, const CUtensorMap*
     int y = keys.y[u];
     if (y < 0) {
       y = first;  // padding position: load real rows, the sub-mask hides them
-    } else if (y >= p.NKU) {
+    } else if (!paged && y >= p.NKU) {
       record_status(p.control, -7, kSitePlanRange + 3);
       y = first;
     }
-    const int row = kGeneral ? unit_row(p, m, y) : m.kvrow0 + y * p.ku;
+    const int row = paged ? y : m.kvrow0 + y * p.ku;
 #pragma unroll
     for (int c = 0; c < C::kChunks; ++c)
       tma_load_2d(dst0 + c * C::kChunkBytes + u * p.ku * 128, map, c * 64, row, full, pol);
@@ -352,11 +338,11 @@ __device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, co
                     sm.bar(C::kBarQFull + qb), pol_q);
       ++q_it;
     }
-    SlotKeys k0 = fetch_keys(p, m, 0), k1 = k0;
-    if (m.n > 1) k1 = fetch_keys(p, m, 1);
+    SlotKeys k0 = fetch_keys<kGeneral>(p, m, 0), k1 = k0;
+    if (m.n > 1) k1 = fetch_keys<kGeneral>(p, m, 1);
     for (int j = 0; j < m.n && ok; ++j) {
       SlotKeys k2 = k1;
-      if (j + 2 < m.n) k2 = fetch_keys(p, m, j + 2);
+      if (j + 2 < m.n) k2 = fetch_keys<kGeneral>(p, m, j + 2);
       ok = load_tile<D, kGeneral>(p, map, r, m, k0, kv_it, pol_kv, wd);
       k0 = k1;
       k1 = k2;
@@ -1030,18 +1016,41 @@ __global__ void __launch_bounds__(256) kmax_kernel(const FwdParams p) {
 }
 
 // Largest key norm over the K units of each plan row's slots (one warp per
-// row), the |k| factor of the row's Cauchy-Schwarz reference.
+// row), the |k| factor of the row's Cauchy-Schwarz reference.  Paged K/V: also
+// the pool row of each slot position's unit, (page*Hkv + hkv)*page_size +
+// key % page_size with the page from the block table, so the producers read
+// rows as they would plan entries.  A page outside the table is an error only
+// when the unit holds keys within the sequence's key length (beyond it the
+// keys are masked, so page 0 serves).
 __global__ void __launch_bounds__(256) rowbound_kernel(const FwdParams p) {
   const int row = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
   if (row >= p.rows) return;
   const int s0 = __ldg(p.row_ptr + row), s1 = __ldg(p.row_ptr + row + 1);
   float km = 0.f;
   if (s0 >= 0 && s1 >= s0 && (long long)s1 <= p.slot_capacity) {  // else the forward reports it
-    const int bh = row / p.NQT, b = bh / p.H, h = bh % p.H;
-    const float* kh = p.kmax + (size_t)(b * p.Hkv + h / p.g) * p.NKU;
+    const int bh = row / p.NQT, b = bh / p.H, h = bh % p.H, hkv = h / p.g;
+    const float* kh = p.kmax + (size_t)(b * p.Hkv + hkv) * p.NKU;
+    const int kvl = (p.prow && p.kv_lens) ? __ldg(p.kv_lens + b) : 0x7fffffff;
     for (long long i = (long long)s0 * p.rk + lane; i < (long long)s1 * p.rk; i += 32) {
       const int y = __ldg(p.slot_ku + i);
-      if (y >= 0 && y < p.NKU) km = fmaxf(km, __ldg(kh + y));
+      const bool valid = y >= 0 && y < p.NKU;
+      if (valid) km = fmaxf(km, __ldg(kh + y));
+      if (p.prow) {
+        int prow = -1;  // padding, or an entry out of range (reported here)
+        if (valid) {
+          const int key = y * p.ku;
+          const int lp = key / p.page_size;
+          int phys = (lp < p.max_pages) ? __ldg(p.block_table + (size_t)b * p.max_pages + lp) : -1;
+          if (phys < 0 || phys >= p.num_pages) {
+            if (key < kvl) record_status(p.control, -7, kSitePlanRange + 4);
+            phys = 0;
+          }
+          prow = (phys * p.Hkv + hkv) * p.page_size + (key - lp * p.page_size);
+        } else if (y != -1) {
+          record_status(p.control, -7, kSitePlanRange + 3);
+        }
+        p.prow[i] = prow;
+      }
     }
   }
 #pragma unroll

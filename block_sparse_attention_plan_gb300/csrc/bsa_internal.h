@@ -49,9 +49,10 @@ inline uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255); }
 // Forward-pass scratch inside a plan workspace, after the plan-construction
 // scratch: the largest key norm of every K unit (float[B*Hkv*NKU]), that of
 // every plan row's selected units (float[rows]), a fallback flag per plan row
-// and the list of rows queued for the exact pass (int32[rows] each).
+// and the list of rows queued for the exact pass (int32[rows] each), and for
+// paged K/V the pool row of every slot position (int32[slot_capacity*rk]).
 struct FwdScratch {
-  uint64_t off_kmax, off_rowk, off_fb_flag, off_fb_list, end;
+  uint64_t off_kmax, off_rowk, off_fb_flag, off_fb_list, off_prow, end;
 };
 inline FwdScratch fwd_scratch(const bsa_plan_layout& L) {
   uint64_t off = L.off_scratch;
@@ -64,6 +65,7 @@ inline FwdScratch fwd_scratch(const bsa_plan_layout& L) {
   f.off_rowk = off;    off = align256(off + 4ull * (uint64_t)L.rows);
   f.off_fb_flag = off; off = align256(off + 4ull * (uint64_t)L.rows);
   f.off_fb_list = off; off = align256(off + 4ull * (uint64_t)L.rows);
+  f.off_prow = off;    off = align256(off + 4ull * (uint64_t)L.slot_capacity * L.rk);
   f.end = off;
   return f;
 }
@@ -88,6 +90,10 @@ struct FwdParams {
   // Paged K/V (block_table == nullptr: contiguous [B*Hkv*Nk, d]).
   const int32_t* block_table;    // [B][max_pages] physical page per logical page
   int max_pages, page_size, num_pages;
+  // Paged K/V: first pool row of the unit at each slot position (-1 = padding
+  // or an entry out of range), written by the row-bound pass; nullptr when
+  // contiguous.
+  int32_t* prow;
   // Element mask inside selected blocks.
   const int32_t* kv_lens;        // [B] or nullptr
   int causal;                    // key j visible to query i iff j <= i + causal_off
