@@ -192,19 +192,8 @@ bsa_status bsa_plan_create(const uint8_t* mask, int B, int H, int NQB, int NKB, 
   impl->device = dev;
   PlanDev& d = impl->dev;
   d.mask = mask;
-  d.row_ptr = reinterpret_cast<int32_t*>(ws + L.off_row_ptr);
-  d.slot_ku = reinterpret_cast<int32_t*>(ws + L.off_slot_ku);
-  d.slot_mask = reinterpret_cast<uint32_t*>(ws + L.off_slot_mask);
-  d.urow_ptr = reinterpret_cast<int32_t*>(ws + L.off_urow_ptr);
-  d.ukb = reinterpret_cast<int32_t*>(ws + L.off_ukb);
-  d.order = reinterpret_cast<int32_t*>(ws + L.off_order);
-  d.totals = reinterpret_cast<long long*>(ws + L.off_totals);
-  d.control = reinterpret_cast<int32_t*>(ws + L.off_control);
-  uint64_t off = L.off_scratch;
-  d.slots = reinterpret_cast<int32_t*>(ws + off); off = align256(off + 4ull * L.rows);
-  d.lcnt = reinterpret_cast<int32_t*>(ws + off);  off = align256(off + 4ull * L.rows);
-  d.ucnt = reinterpret_cast<int32_t*>(ws + off);  off = align256(off + 4ull * (L.urows + 1));
-  d.gstart = reinterpret_cast<int32_t*>(ws + off);
+  set_plan_views(d, ws, L);
+  d.vec = (aligned16(mask) && NKB % 16 == 0) ? 1 : 0;
   d.B = B; d.H = H; d.Hkv = L.Hkv; d.g = gqa_group; d.NQB = NQB; d.NKB = NKB;
   d.qu = L.qu; d.rq = L.rq; d.sq = L.sq; d.ku = L.ku; d.rk = L.rk; d.sk = L.sk;
   d.NQT = L.NQT; d.NKU = L.NKU; d.rows = L.rows; d.urows = L.urows;

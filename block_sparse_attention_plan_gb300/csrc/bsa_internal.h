@@ -39,12 +39,54 @@ struct PlanDev {
   int32_t* lcnt;    // scratch: selected logical blocks owned by the row
   int32_t* ucnt;    // scratch: union entries per union row
   int32_t* gstart;  // scratch: first schedule position of each K/V-head group
+  uint32_t* qbits;  // scratch: [rows][rq][W] selected k-units of each q-unit, 32 per word
+  uint32_t* ubits;  // scratch: [urows][W] union k-units of each union row
   int B, H, Hkv, g, NQB, NKB;
   int qu, rq, sq, ku, rk, sk;
   int NQT, NKU, rows, urows, nkeys, groups;
+  int W;    // bitmap words per q-unit: ceil(NKU / 32)
+  int vec;  // mask rows may be read 16 bytes at a time (16-byte aligned mask, NKB % 16 == 0)
 };
 
 inline uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255); }
+
+// Plan-construction scratch inside a plan workspace, after the plan arrays.
+struct PlanScratch {
+  uint64_t off_slots, off_lcnt, off_ucnt, off_gstart, off_qbits, off_ubits, end;
+};
+inline PlanScratch plan_scratch(const bsa_plan_layout& L) {
+  const uint64_t W = ((uint64_t)L.NKU + 31) / 32;
+  PlanScratch s;
+  uint64_t off = L.off_scratch;
+  s.off_slots = off;  off = align256(off + 4ull * (uint64_t)L.rows);
+  s.off_lcnt = off;   off = align256(off + 4ull * (uint64_t)L.rows);
+  s.off_ucnt = off;   off = align256(off + 4ull * ((uint64_t)L.urows + 1));
+  s.off_gstart = off; off = align256(off + 4ull * (uint64_t)L.groups);
+  s.off_qbits = off;  off = align256(off + 4ull * (uint64_t)L.rows * L.rq * W);
+  s.off_ubits = off;  off = align256(off + 4ull * (uint64_t)L.urows * W);
+  s.end = off;
+  return s;
+}
+
+// Points the plan views of `d` at workspace `ws` laid out by `L`.
+inline void set_plan_views(PlanDev& d, uint8_t* ws, const bsa_plan_layout& L) {
+  d.row_ptr = reinterpret_cast<int32_t*>(ws + L.off_row_ptr);
+  d.slot_ku = reinterpret_cast<int32_t*>(ws + L.off_slot_ku);
+  d.slot_mask = reinterpret_cast<uint32_t*>(ws + L.off_slot_mask);
+  d.urow_ptr = reinterpret_cast<int32_t*>(ws + L.off_urow_ptr);
+  d.ukb = reinterpret_cast<int32_t*>(ws + L.off_ukb);
+  d.order = reinterpret_cast<int32_t*>(ws + L.off_order);
+  d.totals = reinterpret_cast<long long*>(ws + L.off_totals);
+  d.control = reinterpret_cast<int32_t*>(ws + L.off_control);
+  const PlanScratch s = plan_scratch(L);
+  d.slots = reinterpret_cast<int32_t*>(ws + s.off_slots);
+  d.lcnt = reinterpret_cast<int32_t*>(ws + s.off_lcnt);
+  d.ucnt = reinterpret_cast<int32_t*>(ws + s.off_ucnt);
+  d.gstart = reinterpret_cast<int32_t*>(ws + s.off_gstart);
+  d.qbits = reinterpret_cast<uint32_t*>(ws + s.off_qbits);
+  d.ubits = reinterpret_cast<uint32_t*>(ws + s.off_ubits);
+  d.W = (L.NKU + 31) / 32;
+}
 
 // Forward-pass scratch inside a plan workspace, after the plan-construction
 // scratch: the largest key norm of every K unit (float[B*Hkv*NKU]), that of
@@ -55,11 +97,7 @@ struct FwdScratch {
   uint64_t off_kmax, off_rowk, off_fb_flag, off_fb_list, off_prow, end;
 };
 inline FwdScratch fwd_scratch(const bsa_plan_layout& L) {
-  uint64_t off = L.off_scratch;
-  off = align256(off + 4ull * (uint64_t)L.rows);          // plan scratch: slots
-  off = align256(off + 4ull * (uint64_t)L.rows);          // lcnt
-  off = align256(off + 4ull * ((uint64_t)L.urows + 1));   // ucnt
-  off = align256(off + 4ull * (uint64_t)L.groups);        // gstart
+  uint64_t off = plan_scratch(L).end;
   FwdScratch f;
   f.off_kmax = off;    off = align256(off + 4ull * (uint64_t)L.B * L.Hkv * L.NKU);
   f.off_rowk = off;    off = align256(off + 4ull * (uint64_t)L.rows);

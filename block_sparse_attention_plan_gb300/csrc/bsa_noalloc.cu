@@ -112,19 +112,8 @@ extern "C" bsa_status bsa_attention_static(const uint8_t* mask, int B, int H, in
   PlanDev pd;
   std::memset(&pd, 0, sizeof(pd));
   pd.mask = mask;
-  pd.row_ptr = reinterpret_cast<int32_t*>(ws + L.off_row_ptr);
-  pd.slot_ku = reinterpret_cast<int32_t*>(ws + L.off_slot_ku);
-  pd.slot_mask = reinterpret_cast<uint32_t*>(ws + L.off_slot_mask);
-  pd.urow_ptr = reinterpret_cast<int32_t*>(ws + L.off_urow_ptr);
-  pd.ukb = reinterpret_cast<int32_t*>(ws + L.off_ukb);
-  pd.order = reinterpret_cast<int32_t*>(ws + L.off_order);
-  pd.totals = reinterpret_cast<long long*>(ws + L.off_totals);
-  pd.control = reinterpret_cast<int32_t*>(ws + L.off_control);
-  uint64_t off = L.off_scratch;
-  pd.slots = reinterpret_cast<int32_t*>(ws + off); off = align256(off + 4ull * L.rows);
-  pd.lcnt = reinterpret_cast<int32_t*>(ws + off);  off = align256(off + 4ull * L.rows);
-  pd.ucnt = reinterpret_cast<int32_t*>(ws + off);  off = align256(off + 4ull * (L.urows + 1));
-  pd.gstart = reinterpret_cast<int32_t*>(ws + off);
+  set_plan_views(pd, ws, L);
+  pd.vec = ((reinterpret_cast<uintptr_t>(mask) & 15u) == 0 && NKB % 16 == 0) ? 1 : 0;
   pd.B = B; pd.H = H; pd.Hkv = L.Hkv; pd.g = gqa_group; pd.NQB = NQB; pd.NKB = NKB;
   pd.qu = L.qu; pd.rq = L.rq; pd.sq = L.sq; pd.ku = L.ku; pd.rk = L.rk; pd.sk = L.sk;
   pd.NQT = L.NQT; pd.NKU = L.NKU; pd.rows = L.rows; pd.urows = L.urows;

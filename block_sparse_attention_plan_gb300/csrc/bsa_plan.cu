@@ -9,16 +9,20 @@
 // intra-group union).
 //
 // Three launches, no host synchronisation:
-//   count  one warp per plan row (and per union row): per 32 k-units, each
-//          lane ORs the rq q-unit mask bytes of its k-unit; __ballot_sync +
-//          __popc give the row's unit count.
+//   count  one warp per plan row (and per union row).  Lane l owns bitmap word
+//          l of every 32-word stretch of k-units (units 32w .. 32w+31): it reads
+//          the 32 (16 when a logical block is two units) mask bytes of that
+//          word for each of the rq q-units with 16-byte loads, turns nonzero
+//          bytes into bits and stores the word in a per-q-unit bitmap; the
+//          union over q-units gives the row's unit count.  Union rows OR the
+//          g query heads' words the same way.
 //   scan   one CTA: exclusive prefix sums (row pointers, union pointers),
 //          totals, and the rank of every K/V-head group by its total slots.
-//   fill   one warp per row: ballot + prefix-popcount compaction writes the
-//          ascending k-units into slots, then the per-slot sub-masks; union
-//          rows likewise; and one CTA per K/V-head group places the group's
-//          rows in the schedule with a stable counting sort (slots
-//          descending, row id ascending).
+//   fill   one warp per row: a warp prefix sum over the words' popcounts
+//          places the ascending k-units into slots; the per-slot sub-masks
+//          are read off the per-q-unit bitmaps; union rows likewise; and one
+//          CTA per K/V-head group places the group's rows in the schedule
+//          with a stable counting sort (slots descending, row id ascending).
 #include <cstdint>
 
 #include "bsa_internal.h"
@@ -29,7 +33,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kScanThreads = 1024;
-constexpr int kBatch = 8;  // 32-unit chunks whose mask loads are issued together
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
@@ -37,60 +40,74 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-// Mask bytes of kBatch consecutive 32-unit chunks (k-units y0 + c*32 + lane)
-// for the rq q-units of q-tile qt of mask plane mbh ([NQB][NKB] of one
-// (b, h)).  Every load of the batch is issued before any is used (fully
-// unrolled, predicated on rq <= 4), so a warp waits for one round trip per
-// batch instead of one per byte.
-struct UnitBatch {
-  int u[kBatch];    // k-unit selected by some q-unit of the tile
-  int own[kBatch];  // logical blocks first-owned here (see count kernel)
+// Nonzero bytes of a 32-bit word -> 4 bits (byte k -> bit k).
+__device__ __forceinline__ uint32_t nz4(uint32_t v) {
+  const uint32_t m = __vcmpne4(v, 0u);  // 0xff for each nonzero byte
+  return ((m >> 7) & 1u) | ((m >> 14) & 2u) | ((m >> 21) & 4u) | ((m >> 28) & 8u);
+}
+
+// Mask bytes behind one bitmap word: 32 bytes (sk = 1) or 16 (sk = 2).
+struct Raw {
+  uint4 a, b;
 };
 
-__device__ __forceinline__ UnitBatch unit_batch(const uint8_t* __restrict__ mbh, const PlanDev& p,
-                                                int qt, int y0, int lane) {
-  const int sk_sh = p.sk >> 1, sq_sh = p.sq >> 1;  // sk, sq are 1 or 2
-  uint8_t v[kBatch][4];
-#pragma unroll
-  for (int c = 0; c < kBatch; ++c) {
-    const int y = y0 + c * 32 + lane;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int x = qt * p.rq + i;
-      v[c][i] = (i < p.rq && y < p.NKU) ? __ldg(mbh + (size_t)(x >> sq_sh) * p.NKB + (y >> sk_sh))
-                                        : (uint8_t)0;
-    }
-  }
-  UnitBatch r;
-#pragma unroll
-  for (int c = 0; c < kBatch; ++c) {
-    const int y = y0 + c * 32 + lane;
-    const bool first_k = (y & sk_sh) == 0;
-    int u = 0, o = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int x = qt * p.rq + i;
-      const int sel = v[c][i] != 0;
-      u |= sel;
-      o += (sel && first_k && (x & sq_sh) == 0);
-    }
-    r.u[c] = u;
-    r.own[c] = o;
+// Mask row of q-unit x in the (b, h) plane mbh ([NQB][NKB] bytes).
+__device__ __forceinline__ const uint8_t* qunit_row(const uint8_t* mbh, const PlanDev& p, int x) {
+  return mbh + (size_t)(x >> (p.sq >> 1)) * p.NKB;
+}
+
+// 16-byte loads of word w of a mask row (the word lies wholly inside the row,
+// the row is 16-byte aligned).
+__device__ __forceinline__ Raw raw_load(const uint8_t* row, int w, int sk_sh) {
+  Raw r;
+  if (sk_sh == 0) {
+    const uint4* s = reinterpret_cast<const uint4*>(row + 32 * (size_t)w);
+    r.a = __ldg(s);
+    r.b = __ldg(s + 1);
+  } else {
+    r.a = __ldg(reinterpret_cast<const uint4*>(row + 16 * (size_t)w));
+    r.b = make_uint4(0u, 0u, 0u, 0u);
   }
   return r;
 }
 
-// GQA union over the g query heads of K/V head hk: for each head the same
-// hoisted batch of loads, OR-ed together.
-__device__ __forceinline__ void union_batch(const PlanDev& p, int b, int hk, int qt, int y0,
-                                            int lane, int (&u)[kBatch]) {
+__device__ __forceinline__ uint32_t raw_bits(const Raw& r, int sk_sh) {
+  const uint32_t lo = nz4(r.a.x) | (nz4(r.a.y) << 4) | (nz4(r.a.z) << 8) | (nz4(r.a.w) << 12);
+  if (sk_sh == 0)
+    return lo | (nz4(r.b.x) << 16) | (nz4(r.b.y) << 20) | (nz4(r.b.z) << 24) | (nz4(r.b.w) << 28);
+  // 16 logical blocks, each two k-units: bit b -> bits 2b and 2b + 1.
+  uint32_t t = lo;
+  t = (t | (t << 8)) & 0x00ff00ffu;
+  t = (t | (t << 4)) & 0x0f0f0f0fu;
+  t = (t | (t << 2)) & 0x33333333u;
+  t = (t | (t << 1)) & 0x55555555u;
+  return t | (t << 1);
+}
+
+// Word w of a mask row one byte at a time (unaligned masks, the last word).
+__device__ uint32_t slow_bits(const uint8_t* row, const PlanDev& p, int w, int sk_sh) {
+  uint32_t bits = 0;
+  for (int t = 0; t < 32; ++t) {
+    const int y = 32 * w + t;
+    if (y < p.NKU && __ldg(row + (y >> sk_sh)) != 0) bits |= 1u << t;
+  }
+  return bits;
+}
+
+// Selected-unit words (k-units 32w .. 32w+31) of up to four mask rows, all
+// loads issued before any is used.  Rows with index >= n give 0.
+__device__ __forceinline__ void row_words(const uint8_t* const (&rows)[4], int n, const PlanDev& p,
+                                          int w, uint32_t (&out)[4]) {
+  const int sk_sh = p.sk >> 1;
+  const bool fast = p.vec && 32 * (w + 1) <= p.NKU;
+  Raw raw[4];
 #pragma unroll
-  for (int c = 0; c < kBatch; ++c) u[c] = 0;
-  for (int hh = 0; hh < p.g; ++hh) {
-    const uint8_t* mbh = p.mask + ((size_t)(b * p.H + hk * p.g + hh)) * p.NQB * p.NKB;
-    const UnitBatch r = unit_batch(mbh, p, qt, y0, lane);
+  for (int i = 0; i < 4; ++i)
+    if (i < n && fast) raw[i] = raw_load(rows[i], w, sk_sh);
 #pragma unroll
-    for (int c = 0; c < kBatch; ++c) u[c] |= r.u[c];
+  for (int i = 0; i < 4; ++i) {
+    out[i] = 0u;
+    if (i < n && w < p.W) out[i] = fast ? raw_bits(raw[i], sk_sh) : slow_bits(rows[i], p, w, sk_sh);
   }
 }
 
@@ -102,16 +119,31 @@ __global__ void __launch_bounds__(kThreads) plan_count_kernel(const PlanDev p) {
     if (r >= p.rows) return;
     const int bh = r / p.NQT, qt = r % p.NQT;
     const uint8_t* mbh = p.mask + (size_t)bh * p.NQB * p.NKB;
-    int cnt = 0, own = 0;
-    for (int y0 = 0; y0 < p.NKU; y0 += 32 * kBatch) {
-      const UnitBatch r = unit_batch(mbh, p, qt, y0, lane);
+    const uint8_t* rows[4];
 #pragma unroll
-      for (int c = 0; c < kBatch; ++c) {
-        cnt += __popc(__ballot_sync(0xffffffffu, r.u[c]));
-        own += r.own[c];
+    for (int i = 0; i < 4; ++i) rows[i] = qunit_row(mbh, p, qt * p.rq + (i < p.rq ? i : 0));
+    // A logical block is counted once: at its first q-unit (x even when
+    // sq = 2) and its first k-unit (even units when sk = 2).
+    const uint32_t kfirst = p.sk == 2 ? 0x55555555u : 0xffffffffu;
+    int cnt = 0, own = 0;
+    for (int w0 = 0; w0 < p.W; w0 += 32) {
+      const int w = w0 + lane;
+      uint32_t words[4];
+      row_words(rows, p.rq, p, w, words);
+      uint32_t u = 0u;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (i >= p.rq) break;
+        if (w < p.W) p.qbits[((size_t)r * p.rq + i) * p.W + w] = words[i];
+        u |= words[i];
+        if (((qt * p.rq + i) & (p.sq >> 1)) == 0) own += __popc(words[i] & kfirst);
       }
+      cnt += __popc(u);
     }
-    for (int s = 16; s > 0; s >>= 1) own += __shfl_xor_sync(0xffffffffu, own, s);
+    for (int s = 16; s > 0; s >>= 1) {
+      cnt += __shfl_xor_sync(0xffffffffu, cnt, s);
+      own += __shfl_xor_sync(0xffffffffu, own, s);
+    }
     if (lane == 0) {
       p.slots[r] = (cnt + p.rk - 1) / p.rk;
       p.lcnt[r] = own;
@@ -121,13 +153,28 @@ __global__ void __launch_bounds__(kThreads) plan_count_kernel(const PlanDev p) {
     if (ur >= p.urows) return;
     const int bhk = ur / p.NQT, qt = ur % p.NQT;
     const int b = bhk / p.Hkv, hk = bhk % p.Hkv;
+    const int nsrc = p.g * p.rq;  // (head, q-unit) mask rows OR-ed into the union
     int cnt = 0;
-    for (int y0 = 0; y0 < p.NKU; y0 += 32 * kBatch) {
-      int u[kBatch];
-      union_batch(p, b, hk, qt, y0, lane, u);
+    for (int w0 = 0; w0 < p.W; w0 += 32) {
+      const int w = w0 + lane;
+      uint32_t u = 0u;
+      for (int k0 = 0; k0 < nsrc; k0 += 4) {
+        const uint8_t* rows[4];
 #pragma unroll
-      for (int c = 0; c < kBatch; ++c) cnt += __popc(__ballot_sync(0xffffffffu, u[c]));
+        for (int i = 0; i < 4; ++i) {
+          const int k = k0 + i < nsrc ? k0 + i : k0;
+          const int hh = k / p.rq, ii = k % p.rq;
+          const uint8_t* mbh = p.mask + ((size_t)(b * p.H + hk * p.g + hh)) * p.NQB * p.NKB;
+          rows[i] = qunit_row(mbh, p, qt * p.rq + ii);
+        }
+        uint32_t words[4];
+        row_words(rows, nsrc - k0 < 4 ? nsrc - k0 : 4, p, w, words);
+        u |= words[0] | words[1] | words[2] | words[3];
+      }
+      if (w < p.W) p.ubits[(size_t)ur * p.W + w] = u;
+      cnt += __popc(u);
     }
+    for (int s = 16; s > 0; s >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, s);
     if (lane == 0) p.ucnt[ur] = cnt;
   }
 }
@@ -226,62 +273,66 @@ __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(const PlanDev p
   }
 }
 
+// Writes the set bits of `u` (bitmap word w of the warp's lane) as ascending
+// k-units at out[pos + ...] (entries at or beyond cap are dropped); returns
+// the number of set bits over the warp.
+__device__ __forceinline__ int compact_word(uint32_t u, int w, int lane, int32_t* out, int pos,
+                                            int cap) {
+  const int c = __popc(u);
+  int incl = c;
+  for (int s = 1; s < 32; s <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, s);
+    if (lane >= s) incl += y;
+  }
+  int idx = pos + incl - c;
+  while (u) {
+    const int bit = __ffs(u) - 1;
+    u &= u - 1u;
+    if (idx < cap) out[idx] = 32 * w + bit;
+    ++idx;
+  }
+  return __shfl_sync(0xffffffffu, incl, 31);
+}
+
 __device__ void fill_row(const PlanDev& p, int r, int lane) {
-  const int bh = r / p.NQT, qt = r % p.NQT;
-  const uint8_t* mbh = p.mask + (size_t)bh * p.NQB * p.NKB;
   const int s0 = p.row_ptr[r];
   const int n = p.row_ptr[r + 1] - s0;
   const int cap = n * p.rk;
   int32_t* out = p.slot_ku + (size_t)s0 * p.rk;
+  const uint32_t* qb = p.qbits + (size_t)r * p.rq * p.W;
   int pos = 0;
-  for (int y0 = 0; y0 < p.NKU; y0 += 32 * kBatch) {
-    const UnitBatch r = unit_batch(mbh, p, qt, y0, lane);
-#pragma unroll
-    for (int c = 0; c < kBatch; ++c) {  // ascending k-units: chunk by chunk
-      const uint32_t bal = __ballot_sync(0xffffffffu, r.u[c]);
-      if (r.u[c]) {
-        const int idx = pos + __popc(bal & lanemask_lt());
-        if (idx < cap) out[idx] = y0 + c * 32 + lane;
-      }
-      pos += __popc(bal);
+  for (int w0 = 0; w0 < p.W; w0 += 32) {
+    const int w = w0 + lane;
+    uint32_t u = 0u;
+    if (w < p.W) {
+      for (int i = 0; i < p.rq; ++i) u |= qb[(size_t)i * p.W + w];
     }
+    pos += compact_word(u, w, lane, out, pos, cap);
   }
   for (int idx = pos + lane; idx < cap; idx += 32) out[idx] = -1;
-  __threadfence_block();
   __syncwarp();
+  // Sub-mask of each slot: bit i*rk + j when q-unit i selects the unit at
+  // position j (read off the q-unit bitmaps).
   for (int s = lane; s < n; s += 32) {
     uint32_t bits = 0;
     for (int j = 0; j < p.rk; ++j) {
       const int y = out[s * p.rk + j];
       if (y < 0) continue;
-      const int kb = y >> (p.sk >> 1);
-      for (int ii = 0; ii < p.rq; ++ii) {
-        const int x = qt * p.rq + ii;
-        if (__ldg(mbh + (size_t)(x >> (p.sq >> 1)) * p.NKB + kb) != 0) bits |= 1u << (ii * p.rk + j);
-      }
+      for (int i = 0; i < p.rq; ++i)
+        if ((qb[(size_t)i * p.W + (y >> 5)] >> (y & 31)) & 1u) bits |= 1u << (i * p.rk + j);
     }
     p.slot_mask[s0 + s] = bits;
   }
 }
 
 __device__ void fill_union_row(const PlanDev& p, int ur, int lane) {
-  const int bhk = ur / p.NQT, qt = ur % p.NQT;
-  const int b = bhk / p.Hkv, hk = bhk % p.Hkv;
   const int s0 = p.urow_ptr[ur];
   const int cap = p.urow_ptr[ur + 1] - s0;
+  const uint32_t* ub = p.ubits + (size_t)ur * p.W;
   int pos = 0;
-  for (int y0 = 0; y0 < p.NKU; y0 += 32 * kBatch) {
-    int u[kBatch];
-    union_batch(p, b, hk, qt, y0, lane, u);
-#pragma unroll
-    for (int c = 0; c < kBatch; ++c) {
-      const uint32_t bal = __ballot_sync(0xffffffffu, u[c]);
-      if (u[c]) {
-        const int idx = pos + __popc(bal & lanemask_lt());
-        if (idx < cap) p.ukb[s0 + idx] = y0 + c * 32 + lane;
-      }
-      pos += __popc(bal);
-    }
+  for (int w0 = 0; w0 < p.W; w0 += 32) {
+    const int w = w0 + lane;
+    pos += compact_word(w < p.W ? ub[w] : 0u, w, lane, p.ukb + s0, pos, cap);
   }
 }
 

@@ -69,3 +69,28 @@ def test_plan_many_rows_sort_segments(bsa):
     w = W.random_problem(7, 1, 8, 8, 8192, 4096, 16, 128, 128, 0.05)
     _, a = gpu_plan_arrays(bsa, w.mask, 128, 128, 1)
     assert_plan_equal(a, OP.build_plan(w.mask.numpy(), 128, 128, 1))
+
+
+@pytest.mark.parametrize("bq,bk", [(128, 64), (64, 256), (32, 32)])
+def test_plan_long_rows_and_unaligned_mask(bsa, bq, bk):
+    # More than 1024 k-units per row (several 32-word stretches, a partial
+    # last word), non-binary bytes; then the same mask at an odd address,
+    # which the plan must read byte by byte.
+    g = 2
+    NKB = 1040 if bk <= 64 else 528
+    gen = torch.Generator().manual_seed(bq * 7 + bk)
+    vals = torch.randint(0, 256, (1, 4, 256 // bq * 2, NKB), generator=gen, dtype=torch.int32)
+    keep = torch.rand(vals.shape, generator=gen) < 0.15
+    m = torch.where(keep, vals.clamp(min=1), torch.zeros_like(vals)).to(torch.uint8).contiguous()
+    ref = OP.build_plan(m.numpy(), bq, bk, g)
+    _, a = gpu_plan_arrays(bsa, m, bq, bk, g)
+    assert_plan_equal(a, ref)
+    buf = torch.zeros(m.numel() + 16, dtype=torch.uint8, device="cuda")
+    off = buf[1:1 + m.numel()].view(m.shape)
+    off.copy_(m.cuda())
+    assert off.data_ptr() % 16 == 1
+    p = bsa.plan(off, bq, bk, g)
+    a2 = {k: (v.cpu().numpy() if torch.is_tensor(v) else v) for k, v in p.arrays().items()}
+    a2["slot_mask"] = a2["slot_mask"].astype(np.int64) & 0xFFFFFFFF
+    assert bsa.plan_check(p) == 0
+    assert_plan_equal(a2, ref)
