@@ -305,6 +305,7 @@ bsa_status bsa_forward_ex(const bsa_plan* plan, const void* Q, const void* K, co
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return BSA_ERR_CUDA;
+  fp.sms = sms;
   long long grid = env_ll("BSA_GRID", sms);
   if (grid > L.rows) grid = L.rows;
   if (grid < 1) grid = 1;

@@ -881,6 +881,9 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   const Watchdog wd{abort_flag, p.control + kCtlStatus, p.control + kCtlDetail, p.watchdog_ns};
+  // A pass over a queue (the exact pass) with nothing queued: leave before
+  // any setup.  The count was written by the previous kernel in the stream.
+  if (p.work_count != nullptr && *reinterpret_cast<const volatile int32_t*>(p.work_count) <= 0) return;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -968,38 +971,108 @@ cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t stream) {
 
 // Largest key norm of every K unit (ku rows) of every K/V head, i.e. a bound
 // on |k| for the Cauchy-Schwarz reference of the bounded pass; also clears
-// the fallback flags.  One warp per unit, one row per lane at a time with the
-// row's d/8 16-byte loads all in flight; one reduction at the end.  Units
-// wholly past the sequence's key length (or, paged, without a valid page)
-// get 0 and are not read: their keys are masked.
+// the fallback flags.  Each CTA streams groups of kKmaxGroupBytes / (ku*d*2)
+// consecutive units through a ring of shared-memory stages with bulk copies
+// (one thread issues them, completion on the stage's mbarrier), so many
+// bytes are in flight per SM with few registers; each thread then reduces
+// the rows it owns (16-byte reads rotated across the row so the threads of a
+// warp hit different banks).  Units wholly past the sequence's key length
+// (or, paged, without a valid page) get 0 and are not read: their keys are
+// masked.
+constexpr int kKmaxThreads = 128;
+constexpr int kKmaxStages = 3;
+constexpr uint32_t kKmaxGroupBytes = 32768;
+constexpr int kKmaxSmem = kKmaxStages * (int)kKmaxGroupBytes + 1024;
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 template <int D>
-__global__ void __launch_bounds__(256) kmax_kernel(const FwdParams p) {
-  const int tid = blockIdx.x * blockDim.x + threadIdx.x;
-  for (int i = tid; i < p.rows; i += gridDim.x * blockDim.x) p.fb_flag[i] = 0;
-  const int unit = tid >> 5, lane = threadIdx.x & 31;
-  if (unit >= p.B * p.Hkv * p.NKU) return;
-  const int head = unit / p.NKU, y = unit % p.NKU;  // head = b * Hkv + hkv
-  const int b = head / p.Hkv, hkv = head % p.Hkv;
-  const int key = y * p.ku;
-  long long row0 = (long long)unit * p.ku;  // contiguous: units in row order
-  bool skip = p.kv_lens != nullptr && key >= __ldg(p.kv_lens + b);
-  if (p.block_table != nullptr && !skip) {
-    const int lp = key / p.page_size;
-    const int phys = (lp < p.max_pages) ? __ldg(p.block_table + (size_t)b * p.max_pages + lp) : -1;
-    if (phys < 0 || phys >= p.num_pages) skip = true;
-    else row0 = ((long long)phys * p.Hkv + hkv) * p.page_size + key % p.page_size;
+__global__ void __launch_bounds__(kKmaxThreads) kmax_kernel(const FwdParams p) {
+  extern __shared__ __align__(1024) uint8_t kmax_smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = blockIdx.x * kKmaxThreads + tid; i < p.rows; i += gridDim.x * kKmaxThreads)
+    p.fb_flag[i] = 0;
+  const uint32_t base = smem_u32(kmax_smem);
+  const uint32_t bars = base + kKmaxStages * kKmaxGroupBytes;  // kKmaxStages mbarriers
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(kmax_smem + kKmaxStages * kKmaxGroupBytes + 64);
+  int* skip_s = reinterpret_cast<int*>(kmax_smem + kKmaxStages * kKmaxGroupBytes + 128);  // [stages][32]
+  float* rmax_s = reinterpret_cast<float*>(kmax_smem + kKmaxStages * kKmaxGroupBytes + 640);  // [8]
+  const Watchdog wd{abort_flag, p.control + kCtlStatus, p.control + kCtlDetail, p.watchdog_ns};
+  const uint32_t ubytes = (uint32_t)p.ku * D * 2;
+  const int G = (int)(kKmaxGroupBytes / ubytes);  // units per stage (1 .. 8)
+  const long long units = (long long)p.B * p.Hkv * p.NKU;
+  const long long groups = (units + G - 1) / G;
+  if (tid == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < kKmaxStages; ++s) mbar_init(bars + 8u * s, 1);
+    fence_barrier_init();
   }
-  float best = 0.f;
-  if (!skip) {
-    for (int r = lane; r < p.ku; r += 32) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.K + (size_t)(row0 + r) * D);
-      uint4 x[D / 8];
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) x[c] = __ldg(src + c);
+  __syncthreads();
+
+  // Thread 0: start the copies of unit group gi into stage s.
+  auto issue = [&](long long gi, int s) {
+    uint32_t bytes = 0;
+    for (int k = 0; k < G; ++k) {
+      const long long unit = gi * G + k;
+      int skip = 1;
+      long long row0 = 0;
+      if (unit < units) {
+        const int head = (int)(unit / p.NKU), y = (int)(unit % p.NKU);  // head = b * Hkv + hkv
+        const int b = head / p.Hkv, hkv = head % p.Hkv;
+        const int key = y * p.ku;
+        skip = (p.kv_lens != nullptr && key >= __ldg(p.kv_lens + b)) ? 1 : 0;
+        row0 = unit * p.ku;  // contiguous: units in row order
+        if (p.block_table != nullptr && !skip) {
+          const int lp = key / p.page_size;
+          const int phys = (lp < p.max_pages) ? __ldg(p.block_table + (size_t)b * p.max_pages + lp) : -1;
+          if (phys < 0 || phys >= p.num_pages) skip = 1;
+          else row0 = ((long long)phys * p.Hkv + hkv) * p.page_size + (key - lp * p.page_size);
+        }
+      }
+      skip_s[s * 32 + k] = skip;
+      if (!skip) bytes += ubytes;
+    }
+    mbar_arrive_expect_tx(bars + 8u * s, bytes);
+    for (int k = 0; k < G; ++k) {
+      if (skip_s[s * 32 + k]) continue;
+      const long long unit = gi * G + k;
+      const int head = (int)(unit / p.NKU), y = (int)(unit % p.NKU);
+      long long row0 = unit * p.ku;
+      if (p.block_table != nullptr) {
+        const int b = head / p.Hkv, hkv = head % p.Hkv, key = y * p.ku, lp = key / p.page_size;
+        const int phys = __ldg(p.block_table + (size_t)b * p.max_pages + lp);
+        row0 = ((long long)phys * p.Hkv + hkv) * p.page_size + (key - lp * p.page_size);
+      }
+      bulk_load(base + s * kKmaxGroupBytes + k * ubytes, p.K + (size_t)row0 * D, ubytes, bars + 8u * s);
+    }
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < kKmaxStages; ++s) {
+      const long long gi = blockIdx.x + (long long)s * gridDim.x;
+      if (gi < groups) issue(gi, s);
+    }
+  }
+  constexpr int kChunks = D / 8;  // 16-byte chunks per row
+  const int rows = G * p.ku;      // rows per stage: 32768 / (2 D)
+  uint32_t it = 0;
+  for (long long gi = blockIdx.x; gi < groups; gi += gridDim.x, ++it) {
+    const int s = (int)(it % kKmaxStages);
+    const bool waited = mbar_wait(bars + 8u * s, (it / kKmaxStages) & 1u, wd, kSiteKvFull);
+    if (!__syncthreads_and(waited)) break;  // uniform: no thread left behind at a barrier
+    // Rows tid, tid + 128, ... of the stage; row r at byte r * 2D.
+    for (int rb = 0; rb * kKmaxThreads < rows; ++rb) {
+      const int r = rb * kKmaxThreads + tid;
+      const uint32_t rowp = base + s * kKmaxGroupBytes + (uint32_t)r * (D * 2);
       float s2a = 0.f, s2b = 0.f;
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint32_t w4[4] = {x[c].x, x[c].y, x[c].z, x[c].w};
+      for (int c = 0; c < kChunks; ++c) {
+        const uint4 x = ld_shared_v4(rowp + (uint32_t)(((c + tid) % kChunks) * 16));
+        const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
@@ -1007,12 +1080,36 @@ __global__ void __launch_bounds__(256) kmax_kernel(const FwdParams p) {
           s2b = fmaf(hi, hi, s2b);
         }
       }
-      best = fmaxf(best, s2a + s2b);
+      float m = s2a + s2b;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) rmax_s[rb * (kKmaxThreads / 32) + warp] = m;  // rows 32*(rb*4+warp) ..
+    }
+    __syncthreads();
+    if (tid < G) {
+      const long long unit = gi * G + tid;
+      if (unit < units) {
+        float m = 0.f;
+        if (!skip_s[s * 32 + tid]) {
+          const int b0 = tid * p.ku / 32, b1 = (tid + 1) * p.ku / 32;  // 32-row blocks of the unit
+          for (int q = b0; q < b1; ++q) m = fmaxf(m, rmax_s[q]);
+        }
+        p.kmax[unit] = sqrtf(m);
+      }
+    }
+    __syncthreads();  // stage s and rmax_s free again
+    if (tid == 0) {
+      const long long gn = gi + (long long)kKmaxStages * gridDim.x;
+      if (gn < groups) issue(gn, s);
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
-  if (lane == 0) p.kmax[unit] = sqrtf(best);
+  if (*abort_flag && tid == 0) {
+    // Let copies already issued land before the CTA's shared memory goes away.
+    for (int s = 0; s < kKmaxStages; ++s) {
+      const long long gi = blockIdx.x + (long long)(it + s) * gridDim.x;
+      if (gi < groups) drain_wait(bars + 8u * ((it + s) % kKmaxStages), ((it + s) / kKmaxStages) & 1u, wd);
+    }
+  }
 }
 
 // Largest key norm over the K units of each plan row's slots (one warp per
@@ -1061,9 +1158,14 @@ __global__ void __launch_bounds__(256) rowbound_kernel(const FwdParams p) {
 template <int D>
 cudaError_t launch_passes(const FwdParams& p, int grid, cudaStream_t stream) {
   const long long units = (long long)p.B * p.Hkv * p.NKU;
-  const long long blocks = (units + 7) / 8;
-  kmax_kernel<D><<<(unsigned)(blocks > 0 ? blocks : 1), 256, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  const long long kgroups = (units + (kKmaxGroupBytes / (p.ku * D * 2)) - 1) / (kKmaxGroupBytes / (p.ku * D * 2));
+  long long kgrid = 2ll * (p.sms > 0 ? p.sms : 1);
+  if (kgrid > kgroups) kgrid = kgroups;
+  if (kgrid < 1) kgrid = 1;
+  cudaError_t e = cudaFuncSetAttribute(kmax_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kKmaxSmem);
+  if (e != cudaSuccess) return e;
+  kmax_kernel<D><<<(unsigned)kgrid, kKmaxThreads, kKmaxSmem, stream>>>(p);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   rowbound_kernel<<<(unsigned)((p.rows + 7) / 8), 256, 0, stream>>>(p);
   e = cudaGetLastError();

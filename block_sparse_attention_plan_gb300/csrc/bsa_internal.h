@@ -142,6 +142,7 @@ struct FwdParams {
   long long slot_capacity;
   long long watchdog_ns;
   int B, H, Hkv, g, NQT, NKU, Nq, Nk, rq, rk, qu, ku, rows;
+  int sms;           // multiprocessors of the device (grid of the key-norm pass)
   float scale_log2;  // scale * log2(e)
 };
 

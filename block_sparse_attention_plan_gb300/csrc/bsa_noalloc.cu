@@ -146,6 +146,7 @@ extern "C" bsa_status bsa_attention_static(const uint8_t* mask, int B, int H, in
   fp.rows = L.rows;
   const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)d);
   fp.scale_log2 = (float)(sc * 1.4426950408889634);
+  fp.sms = sms;
   const int grid = sms < L.rows ? sms : L.rows;
 
   // The control words (work counter, status) must start at zero on every call.
