@@ -89,6 +89,12 @@ def library() -> ctypes.CDLL:
     lib.bsa_watchdog_selftest.argtypes = [VP, I, VP]
     lib.bsa_attention_static.restype = I
     lib.bsa_attention_static.argtypes = [U8P, I, I, I, I, I, I, I, VP, VP, VP, VP, VP, I, F, VP]
+    lib.bsa_attention_host_buffer_bytes.restype = I
+    lib.bsa_attention_host_buffer_bytes.argtypes = [I, I, I, I, I, I, I, I, I,
+                                                    ctypes.POINTER(ctypes.c_size_t)]
+    lib.bsa_attention_host.restype = I
+    lib.bsa_attention_host.argtypes = [U8P, I, I, I, I, I, I, I, VP, VP, VP, VP, VP, I, F, I, VP,
+                                       ctypes.c_size_t, VP]
     _lib = lib
     return lib
 
@@ -256,29 +262,54 @@ def watchdog_selftest(limit_us: int = 20000, device: Optional[torch.device] = No
                                            _stream_ptr(None))
 
 
+_host_buffers = {}
+
+
+def host_buffer_bytes(B: int, H: int, NQB: int, NKB: int, bq: int, bk: int, gqa_group: int, d: int,
+                      chunks: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(library().bsa_attention_host_buffer_bytes(B, H, NQB, NKB, bq, bk, gqa_group, d, chunks,
+                                                     ctypes.byref(n)), "bsa_attention_host_buffer_bytes")
+    return int(n.value)
+
+
 def attention(mask: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, bq: int,
               bk: int, scale: Optional[float] = None, device: str = "cuda",
-              stream: Optional[torch.cuda.Stream] = None):
-    """One call from host or device tensors: copies inputs to the device (from
-    pinned memory, asynchronously), plans, runs, and copies O/LSE back when the
-    inputs were on the host.  Returns (O, LSE) on the inputs' device."""
+              stream: Optional[torch.cuda.Stream] = None, chunks: int = 8,
+              out: Optional[torch.Tensor] = None, lse_out: Optional[torch.Tensor] = None):
+    """One call from host or device tensors.  Host tensors go through
+    bsa_attention_host (chunks copied in, computed and copied out on
+    overlapping streams; pinned memory keeps the copies asynchronous), with a
+    device scratch buffer cached per shape; O and LSE come back in pinned host
+    tensors (or ``out`` / ``lse_out``).  Device tensors: plan + forward.
+    Returns (O, LSE) on the inputs' device."""
     host = not q.is_cuda
     g = q.shape[1] // k.shape[1]
-    if host:
-        mask_d = mask.to(device, non_blocking=True)
-        q_d, k_d, v_d = (t.to(device, non_blocking=True) for t in (q, k, v))
-    else:
-        mask_d, q_d, k_d, v_d = mask, q, k, v
-    pl = plan(mask_d, bq, bk, g, stream=stream)
-    o, lse = forward(pl, q_d, k_d, v_d, scale=scale, stream=stream)
-    if host:
-        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-        l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-        o_h.copy_(o, non_blocking=True)
-        l_h.copy_(lse, non_blocking=True)
-        (stream or torch.cuda.current_stream()).synchronize()
-        return o_h, l_h
-    return o, lse
+    if not host:
+        pl = plan(mask, bq, bk, g, stream=stream)
+        return forward(pl, q, k, v, scale=scale, stream=stream)
+    B, H, NQB, NKB = mask.shape
+    d = q.shape[3]
+    for name, t in (("mask", mask), ("q", q), ("k", k), ("v", v)):
+        if not t.is_contiguous() or t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    key = (torch.device(device).index, B, H, NQB, NKB, bq, bk, g, d, chunks)
+    buf = _host_buffers.get(key)
+    if buf is None:
+        nbytes = host_buffer_bytes(B, H, NQB, NKB, bq, bk, g, d, chunks)
+        _host_buffers.clear()  # one cached buffer at a time
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _host_buffers[key] = buf
+    o_h = out if out is not None else torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    l_h = lse_out if lse_out is not None else torch.empty(q.shape[:3], dtype=torch.float32,
+                                                          pin_memory=True)
+    _check(library().bsa_attention_host(
+        ctypes.c_void_p(mask.data_ptr()), B, H, NQB, NKB, bq, bk, g,
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+        ctypes.c_void_p(o_h.data_ptr()), ctypes.c_void_p(l_h.data_ptr()), d,
+        0.0 if scale is None else float(scale), chunks, ctypes.c_void_p(buf.data_ptr()), buf.numel(),
+        _stream_ptr(stream)), "bsa_attention_host")
+    return o_h, l_h
 
 
 def attention_static(mask: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -261,6 +261,36 @@ bsa_status bsa_attention_static(const uint8_t* mask, int B, int H, int NQB, int 
                                 int bk, int gqa_group, const void* Q, const void* K, const void* V,
                                 void* O, float* LSE, int d, float scale, void* stream);
 
+/*
+ * bsa_attention_host -- plan + forward from HOST buffers, with the transfers
+ * overlapped with the computation.  The pages describe the attention and its
+ * GPU execution, not host transfers; this is plumbing around the same plan
+ * and forward (each row's result is bit-identical to bsa_plan_create +
+ * bsa_forward on device copies of the same inputs).
+ * The B*Hkv (batch, K/V head) units are cut into `chunks` contiguous chunks
+ * (clamped to [1, B*Hkv]); chunk i is copied in on one stream, planned and
+ * run on `stream`, and copied out on another, so that the copy-in of chunk
+ * i+1 and the copy-out of chunk i-1 overlap the computation of chunk i.
+ * mask, Q, K, V: host, layouts as for bsa_plan_create / bsa_forward (pinned
+ * memory lets the copies run asynchronously; pageable memory works but
+ * serialises them).  O, LSE: host outputs, same layouts.
+ * buffer: device scratch of at least bsa_attention_host_buffer_bytes(...)
+ * bytes, 256-byte aligned, owned by the caller (two chunk slots: inputs,
+ * outputs, plan workspace; and one status word per chunk).
+ * The GQA union table is not built (the forward does not read it).
+ * Synchronous: returns once O and LSE are in host memory (it synchronises
+ * `stream`).  Errors: BSA_ERR_INVALID_ARG, BSA_ERR_UNSUPPORTED,
+ * BSA_ERR_WORKSPACE (buffer too small), BSA_ERR_ARCH, BSA_ERR_CUDA, and the
+ * first device status a chunk's forward recorded (BSA_ERR_TIMEOUT,
+ * BSA_ERR_PLAN_MISMATCH).
+ */
+bsa_status bsa_attention_host_buffer_bytes(int B, int H, int NQB, int NKB, int bq, int bk,
+                                           int gqa_group, int d, int chunks, size_t* bytes);
+bsa_status bsa_attention_host(const uint8_t* mask, int B, int H, int NQB, int NKB, int bq, int bk,
+                              int gqa_group, const void* Q, const void* K, const void* V, void* O,
+                              float* LSE, int d, float scale, int chunks, void* buffer,
+                              size_t buffer_bytes, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* bsa_status_string(int status);
 
