@@ -162,3 +162,36 @@ def build_plan(mask, bq: int, bk: int, gqa_group: int = 1) -> dict:
         "order": order.astype(np.int32),
         "totals": totals,
     }
+
+
+def affine_mask(segments, B: int, H: int, NQB: int, NKB: int, base=None) -> np.ndarray:
+    """Logical mask [B,H,NQB,NKB] (u8) of affine row descriptors.
+
+    Source: "SPLAT: A framework for optimised GPU code-generation for SParse
+    reguLar ATtention", abstract: the affine-compressed-sparse-row format
+    describes the regular geometry of sparse attention patterns so that it can
+    be analysed just in time.  The page gives no field layout; the reading
+    used here and by the CUDA path (which implements it independently) is:
+    each head h has a list of segments (a, b, stride, count) and query block
+    qb selects the key blocks
+
+        a*qb + b + stride*t,   t = 0 .. count-1,   kept when in [0, NKB),
+
+    a = 1 placing the segment relative to the query block (sliding windows,
+    strided and dilated patterns), a = 0 at fixed key blocks (global
+    columns); stride may be negative, stride 0 repeats one block.  The mask
+    is the union over the head's segments, the same for every batch entry,
+    OR-ed with ``base`` ([B,H,NQB,NKB], any non-zero byte selects) when given.
+    ``segments[h]`` is the list of (a, b, stride, count) of head h.
+    """
+    m = np.zeros((B, H, NQB, NKB), dtype=np.uint8)
+    for h in range(H):
+        for (a, b, stride, count) in segments[h]:
+            for qb in range(NQB):
+                for t in range(count):
+                    kb = a * qb + b + stride * t
+                    if 0 <= kb < NKB:
+                        m[:, h, qb, kb] = 1
+    if base is not None:
+        m |= (np.asarray(base) != 0).astype(np.uint8)
+    return m

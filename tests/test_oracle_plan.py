@@ -166,3 +166,53 @@ def test_mapping_rule():
         OP.mapping(48, 64)
     with pytest.raises(ValueError):
         OP.build_plan(np.ones((1, 1, 3, 2), np.uint8), 64, 64)  # Nq = 192
+
+
+# ---- affine row descriptors (SPLAT's ACSR reading) -------------------------
+# Each expansion is checked against the pattern's plain definition written
+# with numpy broadcasting over D = qb - kb, not against another expansion.
+
+def _D(NQB, NKB):
+    return np.subtract.outer(np.arange(NQB), np.arange(NKB))
+
+
+def test_affine_sliding_window_is_a_band():
+    NQB, NKB, W = 37, 41, 5
+    m = OP.affine_mask([[(1, -(W - 1), 1, 2 * W - 1)]], 1, 1, NQB, NKB)
+    assert np.array_equal(m[0, 0] != 0, np.abs(_D(NQB, NKB)) < W)
+
+
+def test_affine_strided_pattern():
+    NB, s = 64, 8
+    K = -(-NB // s)
+    segs = [[(1, -(s - 1), 1, 2 * s - 1), (1, -s * K, s, 2 * K + 1)]]
+    m = OP.affine_mask(segs, 2, 1, NB, NB)
+    D = _D(NB, NB)
+    want = (np.abs(D) < s) | (D % s == 0)
+    assert np.array_equal(m[0, 0] != 0, want) and np.array_equal(m[1, 0], m[0, 0])
+
+
+def test_affine_dilated_and_negative_stride():
+    NB, R = 50, 13
+    half = R // 2
+    fwd = OP.affine_mask([[(1, -2 * half, 2, 2 * half + 1)]], 1, 1, NB, NB)
+    rev = OP.affine_mask([[(1, 2 * half, -2, 2 * half + 1)]], 1, 1, NB, NB)
+    D = _D(NB, NB)
+    assert np.array_equal(fwd[0, 0] != 0, (np.abs(D) <= R) & (D % 2 == 0))
+    assert np.array_equal(fwd, rev)
+
+
+def test_affine_global_columns_zero_stride_union_with_base():
+    NQB, NKB, G = 9, 20, 3
+    base = np.zeros((1, 2, NQB, NKB), dtype=np.uint8)
+    base[0, 1, 4, 17] = 9
+    segs = [[(0, 0, 1, G)], [(0, 11, 0, 4), (1, 100, 1, 3)]]  # head 1: one column (stride 0), one segment off the grid
+    m = OP.affine_mask(segs, 1, 2, NQB, NKB, base=base)
+    want0 = np.zeros((NQB, NKB), dtype=bool)
+    want0[:, :G] = True
+    want1 = np.zeros((NQB, NKB), dtype=bool)
+    want1[:, 11] = True
+    want1[4, 17] = True
+    assert np.array_equal(m[0, 0] != 0, want0)
+    assert np.array_equal(m[0, 1] != 0, want1)
+    assert OP.affine_mask([[(1, 0, 1, 0)]], 1, 1, 4, 4).sum() == 0  # count 0 selects nothing
