@@ -278,10 +278,23 @@ def run_gb300(args):
     wsbuf = torch.empty(int(L.workspace_bytes), dtype=torch.uint8, device=dev)
     flop = w.active_flop
 
+    affine = None
+    if args.affine:
+        # sliding, strided and dilated heads as affine row segments, the
+        # BigBird-style heads as mask rows (bsa_plan_create_affine)
+        if w.name != "regular":
+            raise SystemExit("--affine describes the regular workload's patterns")
+        segs, _ = W.regular_segments(w.Hq, w.mask.shape[3])
+        affine = (bsa._lib.affine_segments(segs, dev), mask_d)  # only BigBird heads' rows are read
+
     def step(ev=None):
         if ev is not None:
             ev[2].record(stream)
-        p = bsa.plan(mask_d, w.bq, w.bk, w.gqa_group, workspace=wsbuf)
+        if affine is not None:
+            p = bsa.plan_affine(affine[0], w.B, w.mask.shape[2], w.mask.shape[3], w.bq, w.bk,
+                                w.gqa_group, mask=affine[1], workspace=wsbuf)
+        else:
+            p = bsa.plan(mask_d, w.bq, w.bk, w.gqa_group, workspace=wsbuf)
         if ev is not None:
             ev[0].record(stream)
         bsa.forward(p, q, k, v, out=o, lse=lse, **fwd_extra)
@@ -362,6 +375,9 @@ def run_gb300(args):
     if args.page_size:
         cfg["kv_pages"] = (f"page_size {args.page_size}, pages shuffled across the pool, read "
                            "through a block table (e2e stays on contiguous host buffers)")
+    if args.affine:
+        cfg["plan_input"] = ("affine row segments for the sliding, strided and dilated heads; the "
+                             "BigBird-style heads' rows read from the mask")
     if args.causal:
         cfg["causal"] = ("intra-block causal element mask; FLOP counted over whole selected "
                          "blocks, as the tensor cores execute them")
@@ -408,6 +424,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--page-size", type=int, default=0,
                     help="read K/V through a block table of pages of this many keys (0: contiguous)")
+    ap.add_argument("--affine", action="store_true",
+                    help="regular workload: plan from affine row segments (+ residual mask bytes)")
     ap.add_argument("--causal", action="store_true",
                     help="intra-block causal masking (queries are the last Nq positions)")
     ap.add_argument("--traffic", type=float, default=None,

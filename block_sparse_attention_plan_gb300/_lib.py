@@ -89,6 +89,9 @@ def library() -> ctypes.CDLL:
     lib.bsa_watchdog_selftest.argtypes = [VP, I, VP]
     lib.bsa_attention_static.restype = I
     lib.bsa_attention_static.argtypes = [U8P, I, I, I, I, I, I, I, VP, VP, VP, VP, VP, I, F, VP]
+    lib.bsa_plan_create_affine.restype = I
+    lib.bsa_plan_create_affine.argtypes = [U8P, VP, VP, I, I, I, I, I, I, I, I, VP, ctypes.c_size_t,
+                                           I, VP, ctypes.POINTER(P)]
     lib.bsa_attention_host_buffer_bytes.restype = I
     lib.bsa_attention_host_buffer_bytes.argtypes = [I, I, I, I, I, I, I, I, I,
                                                     ctypes.POINTER(ctypes.c_size_t)]
@@ -187,6 +190,47 @@ def plan(mask: torch.Tensor, bq: int, bk: int, gqa_group: int = 1, flags: int = 
         ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), flags, _stream_ptr(stream),
         ctypes.byref(h)), "bsa_plan_create")
     return Plan(h, workspace, L, mask)
+
+
+def affine_segments(segments, device="cuda"):
+    """Device arrays (segments int32 [nseg, 4], seg_ptr int32 [H + 1]) of a
+    per-head list of (a, b, stride, count) segments."""
+    flat = [tuple(int(x) for x in sg) for head in segments for sg in head]
+    ptr = [0]
+    for head in segments:
+        ptr.append(ptr[-1] + len(head))
+    seg = torch.tensor(flat if flat else [(0, 0, 0, 0)], dtype=torch.int32).reshape(-1, 4)
+    return seg.to(device).contiguous(), torch.tensor(ptr, dtype=torch.int32, device=device), len(flat)
+
+
+def plan_affine(segments, B: int, NQB: int, NKB: int, bq: int, bk: int, gqa_group: int = 1,
+                mask: Optional[torch.Tensor] = None, flags: int = 0,
+                stream: Optional[torch.cuda.Stream] = None,
+                workspace: Optional[torch.Tensor] = None, device="cuda") -> Plan:
+    """Build the plan of affine row segments (bsa_plan_create_affine):
+    ``segments[h]`` lists the (a, b, stride, count) of query head h, or
+    ``segments`` is the (seg, seg_ptr, nseg) device triple of
+    ``affine_segments`` (nothing copied per call); ``mask`` (optional device
+    u8 [B, H, NQB, NKB]) is OR-ed in."""
+    if isinstance(segments, tuple) and len(segments) == 3 and torch.is_tensor(segments[0]):
+        seg, ptr, nseg = segments
+    else:
+        seg, ptr, nseg = affine_segments(segments, device)
+    H = ptr.numel() - 1
+    if mask is not None:
+        if mask.dtype != torch.uint8 or not mask.is_cuda or tuple(mask.shape) != (B, H, NQB, NKB):
+            raise ValueError("mask must be a CUDA uint8 tensor [B, H, NQB, NKB]")
+        mask = mask.contiguous()
+    L = plan_layout(B, H, NQB, NKB, bq, bk, gqa_group, flags)
+    if workspace is None:
+        workspace = torch.empty(int(L.workspace_bytes), dtype=torch.uint8, device=device)
+    h = ctypes.c_void_p()
+    _check(library().bsa_plan_create_affine(
+        ctypes.c_void_p(mask.data_ptr() if mask is not None else None), ctypes.c_void_p(seg.data_ptr()),
+        ctypes.c_void_p(ptr.data_ptr()), nseg, B, H, NQB, NKB, bq, bk, gqa_group,
+        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), flags, _stream_ptr(stream),
+        ctypes.byref(h)), "bsa_plan_create_affine")
+    return Plan(h, workspace, L, (mask, seg, ptr))
 
 
 def forward(p: Plan, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -167,12 +167,18 @@ bsa_status bsa_plan_layout_query(int B, int H, int NQB, int NKB, int bq, int bk,
   return compute_layout(B, H, NQB, NKB, bq, bk, gqa_group, flags, out, nullptr);
 }
 
-bsa_status bsa_plan_create(const uint8_t* mask, int B, int H, int NQB, int NKB, int bq, int bk,
-                           int gqa_group, void* workspace, size_t workspace_bytes, int flags,
-                           void* stream, bsa_plan** out) {
+namespace {
+
+// Plan of a logical mask given as mask bytes, affine row segments, or both
+// (their union); see bsa_plan_create and bsa_plan_create_affine.
+bsa_status create_plan(const uint8_t* mask, const int32_t* seg, const int32_t* seg_ptr, int nseg,
+                       int B, int H, int NQB, int NKB, int bq, int bk, int gqa_group,
+                       void* workspace, size_t workspace_bytes, int flags, void* stream,
+                       bsa_plan** out) {
   if (!out) return BSA_ERR_INVALID_ARG;
   *out = nullptr;
-  if (!mask || !workspace) return BSA_ERR_INVALID_ARG;
+  if ((!mask && !seg_ptr) || !workspace) return BSA_ERR_INVALID_ARG;
+  if (seg_ptr && (nseg < 0 || (nseg > 0 && (!seg || !aligned16(seg))))) return BSA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return BSA_ERR_INVALID_ARG;
   bsa_plan_layout L;
   int nkeys = 0;
@@ -192,8 +198,11 @@ bsa_status bsa_plan_create(const uint8_t* mask, int B, int H, int NQB, int NKB, 
   impl->device = dev;
   PlanDev& d = impl->dev;
   d.mask = mask;
+  d.seg = seg_ptr ? seg : nullptr;
+  d.seg_ptr = seg_ptr;
+  d.nseg = seg_ptr ? nseg : 0;
   set_plan_views(d, ws, L);
-  d.vec = (aligned16(mask) && NKB % 16 == 0) ? 1 : 0;
+  d.vec = (mask && aligned16(mask) && NKB % 16 == 0) ? 1 : 0;
   d.B = B; d.H = H; d.Hkv = L.Hkv; d.g = gqa_group; d.NQB = NQB; d.NKB = NKB;
   d.qu = L.qu; d.rq = L.rq; d.sq = L.sq; d.ku = L.ku; d.rk = L.rk; d.sk = L.sk;
   d.NQT = L.NQT; d.NKU = L.NKU; d.rows = L.rows; d.urows = L.urows;
@@ -206,6 +215,32 @@ bsa_status bsa_plan_create(const uint8_t* mask, int B, int H, int NQB, int NKB, 
   }
   *out = reinterpret_cast<bsa_plan*>(impl);
   return BSA_OK;
+}
+
+}  // namespace
+
+bsa_status bsa_plan_create(const uint8_t* mask, int B, int H, int NQB, int NKB, int bq, int bk,
+                           int gqa_group, void* workspace, size_t workspace_bytes, int flags,
+                           void* stream, bsa_plan** out) {
+  if (!mask) {
+    if (out) *out = nullptr;
+    return BSA_ERR_INVALID_ARG;
+  }
+  return create_plan(mask, nullptr, nullptr, 0, B, H, NQB, NKB, bq, bk, gqa_group, workspace,
+                     workspace_bytes, flags, stream, out);
+}
+
+bsa_status bsa_plan_create_affine(const uint8_t* mask, const int32_t* segments,
+                                  const int32_t* seg_ptr, int nseg, int B, int H, int NQB,
+                                  int NKB, int bq, int bk, int gqa_group, void* workspace,
+                                  size_t workspace_bytes, int flags, void* stream,
+                                  bsa_plan** out) {
+  if (!seg_ptr) {
+    if (out) *out = nullptr;
+    return BSA_ERR_INVALID_ARG;
+  }
+  return create_plan(mask, segments, seg_ptr, nseg, B, H, NQB, NKB, bq, bk, gqa_group, workspace,
+                     workspace_bytes, flags, stream, out);
 }
 
 bsa_status bsa_plan_get_layout(const bsa_plan* plan, bsa_plan_layout* out) {

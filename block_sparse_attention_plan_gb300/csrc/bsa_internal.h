@@ -44,6 +44,9 @@ struct PlanDev {
   int B, H, Hkv, g, NQB, NKB;
   int qu, rq, sq, ku, rk, sk;
   int NQT, NKU, rows, urows, nkeys, groups;
+  const int32_t* seg;      // affine row segments [nseg][4] = {a, b, stride, count}, or nullptr
+  const int32_t* seg_ptr;  // [H + 1]: head h owns segments seg_ptr[h] .. seg_ptr[h+1]-1
+  int nseg;
   int W;    // bitmap words per q-unit: ceil(NKU / 32)
   int vec;  // mask rows may be read 16 bytes at a time (16-byte aligned mask, NKB % 16 == 0)
 };

@@ -95,10 +95,12 @@ __device__ uint32_t slow_bits(const uint8_t* row, const PlanDev& p, int w, int s
 }
 
 // Selected-unit words (k-units 32w .. 32w+31) of up to four mask rows, all
-// loads issued before any is used.  Rows with index >= n give 0.
+// loads issued before any is used.  Rows with index >= n (and every row when
+// the plan has no mask bytes) give 0.
 __device__ __forceinline__ void row_words(const uint8_t* const (&rows)[4], int n, const PlanDev& p,
                                           int w, uint32_t (&out)[4]) {
   const int sk_sh = p.sk >> 1;
+  if (p.mask == nullptr) n = 0;
   const bool fast = p.vec && 32 * (w + 1) <= p.NKU;
   Raw raw[4];
 #pragma unroll
@@ -109,6 +111,64 @@ __device__ __forceinline__ void row_words(const uint8_t* const (&rows)[4], int n
     out[i] = 0u;
     if (i < n && w < p.W) out[i] = fast ? raw_bits(raw[i], sk_sh) : slow_bits(rows[i], p, w, sk_sh);
   }
+}
+
+// Segments of head h: [s0, s1) clamped to the array (empty: the head's
+// selection is its mask rows).
+__device__ __forceinline__ void head_segments(const PlanDev& p, int h, int& s0, int& s1) {
+  s0 = 0;
+  s1 = 0;
+  if (p.seg_ptr == nullptr) return;
+  s0 = max(__ldg(p.seg_ptr + h), 0);
+  s1 = min(__ldg(p.seg_ptr + h + 1), p.nseg);
+}
+
+__device__ __forceinline__ int floor_div(int a, int b) {  // b > 0
+  return a >= 0 ? a / b : -((b - 1 - a) / b);
+}
+
+// Word w (k-units 32w .. 32w+31) of the k-units that segments [s0, s1)
+// select for logical query block qb ("SPLAT", abstract: the
+// affine-compressed-sparse-row format).  Segment (a, b, stride, count)
+// selects key blocks a*qb + b + stride*t, t = 0 .. count-1, inside
+// [0, NKB).  A negative stride is turned around (same set), stride 0 is one
+// block.  Only the t whose block falls in this word are visited: by 32-bit
+// arithmetic when the segment starts at or after -2^28 with a stride of at
+// most 2^28 (so no intermediate value leaves int), else by stepping from the
+// first block at or after the word in 64 bits.
+__device__ uint32_t segment_word(const PlanDev& p, int s0, int s1, int qb, int w) {
+  const int sk_sh = p.sk >> 1;
+  const int kb_lo = (32 * w) >> sk_sh;
+  const int kb_hi = min((32 * w + 31) >> sk_sh, p.NKB - 1);
+  const uint32_t unit_bits = sk_sh ? 3u : 1u;
+  uint32_t bits = 0u;
+  for (int s = s0; s < s1; ++s) {
+    const int4 sg = __ldg(reinterpret_cast<const int4*>(p.seg) + s);  // a, b, stride, count
+    if (sg.w <= 0) continue;
+    long long start = (long long)sg.x * qb + sg.y;
+    long long stride = sg.z, count = sg.w;
+    if (stride == 0) {
+      count = 1;
+      stride = 1;
+    } else if (stride < 0) {
+      start += stride * (count - 1);
+      stride = -stride;
+    }
+    if (start + stride * (count - 1) < kb_lo || start > kb_hi) continue;  // misses this word
+    if (start < -(1ll << 28) || stride > (1ll << 28)) {
+      const long long t = start < kb_lo ? (kb_lo - start + stride - 1) / stride : 0;
+      for (long long x = start + stride * t, n = count - t; n > 0 && x <= kb_hi; x += stride, --n)
+        bits |= unit_bits << (int)((x << sk_sh) - 32ll * w);
+      continue;
+    }
+    const int st = (int)start, sd = (int)stride;
+    int t0 = -floor_div(st - kb_lo, sd);  // ceil((kb_lo - start) / stride)
+    int t1 = floor_div(kb_hi - st, sd);
+    t0 = max(t0, 0);
+    if ((long long)t1 > count - 1) t1 = (int)(count - 1);
+    for (int t = t0; t <= t1; ++t) bits |= unit_bits << (((st + sd * t) << sk_sh) - 32 * w);
+  }
+  return bits;
 }
 
 __global__ void __launch_bounds__(kThreads) plan_count_kernel(const PlanDev p) {
@@ -125,15 +185,18 @@ __global__ void __launch_bounds__(kThreads) plan_count_kernel(const PlanDev p) {
     // A logical block is counted once: at its first q-unit (x even when
     // sq = 2) and its first k-unit (even units when sk = 2).
     const uint32_t kfirst = p.sk == 2 ? 0x55555555u : 0xffffffffu;
+    int seg0, seg1;  // a head with segments is generated from them, else read from the mask
+    head_segments(p, bh % p.H, seg0, seg1);
     int cnt = 0, own = 0;
     for (int w0 = 0; w0 < p.W; w0 += 32) {
       const int w = w0 + lane;
       uint32_t words[4];
-      row_words(rows, p.rq, p, w, words);
+      row_words(rows, seg1 > seg0 ? 0 : p.rq, p, w, words);
       uint32_t u = 0u;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         if (i >= p.rq) break;
+        if (seg1 > seg0 && w < p.W) words[i] = segment_word(p, seg0, seg1, (qt * p.rq + i) >> (p.sq >> 1), w);
         if (w < p.W) p.qbits[((size_t)r * p.rq + i) * p.W + w] = words[i];
         u |= words[i];
         if (((qt * p.rq + i) & (p.sq >> 1)) == 0) own += __popc(words[i] & kfirst);
@@ -159,16 +222,23 @@ __global__ void __launch_bounds__(kThreads) plan_count_kernel(const PlanDev p) {
       const int w = w0 + lane;
       uint32_t u = 0u;
       for (int k0 = 0; k0 < nsrc; k0 += 4) {
-        const uint8_t* rows[4];
+        const uint8_t* rows[4] = {p.mask, p.mask, p.mask, p.mask};
+        int nmask = 0;  // sources read from the mask (heads without segments)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int k = k0 + i < nsrc ? k0 + i : k0;
           const int hh = k / p.rq, ii = k % p.rq;
-          const uint8_t* mbh = p.mask + ((size_t)(b * p.H + hk * p.g + hh)) * p.NQB * p.NKB;
-          rows[i] = qunit_row(mbh, p, qt * p.rq + ii);
+          int s0, s1;
+          head_segments(p, hk * p.g + hh, s0, s1);
+          if (k0 + i < nsrc && s1 > s0) {
+            if (w < p.W) u |= segment_word(p, s0, s1, (qt * p.rq + ii) >> (p.sq >> 1), w);
+          } else if (k0 + i < nsrc) {
+            const uint8_t* mbh = p.mask + ((size_t)(b * p.H + hk * p.g + hh)) * p.NQB * p.NKB;
+            rows[nmask++] = qunit_row(mbh, p, qt * p.rq + ii);
+          }
         }
         uint32_t words[4];
-        row_words(rows, nsrc - k0 < 4 ? nsrc - k0 : 4, p, w, words);
+        row_words(rows, nmask, p, w, words);
         u |= words[0] | words[1] | words[2] | words[3];
       }
       if (w < p.W) p.ubits[(size_t)ur * p.W + w] = u;

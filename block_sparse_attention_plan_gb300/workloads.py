@@ -173,6 +173,27 @@ def regular_mask(gen: torch.Generator, B: int, H: int, NB: int, window: int = 16
     return m
 
 
+def regular_segments(H: int, NB: int, window: int = 16, stride: int = 8, dil_reach: int = 192,
+                     glob: int = 8, bb_window: int = 16):
+    """The regular patterns of ``regular_mask`` as affine row segments
+    (a, b, stride, count) per head -- key blocks a*qb + b + stride*t -- plus
+    the heads that stay explicit mask rows: the BigBird-style heads
+    (h mod 4 = 3), whose random blocks have no affine form, get no segments.
+    Same parameters as ``regular_mask``; ``glob`` and ``bb_window`` are
+    accepted for symmetry with it."""
+    K = -(-NB // stride)
+    half = dil_reach // 2
+    per_kind = [
+        [(1, -(window - 1), 1, 2 * window - 1)],                                  # |D| < window
+        [(1, -(stride - 1), 1, 2 * stride - 1), (1, -stride * K, stride, 2 * K + 1)],  # |D| < s or s | D
+        [(1, -2 * half, 2, 2 * half + 1)],                                        # |D| <= reach, D even
+        [],                                                                       # explicit mask rows
+    ]
+    segs = [per_kind[h % 4] for h in range(H)]
+    mask_heads = [h for h in range(H) if h % 4 == 3]
+    return segs, mask_heads
+
+
 def long_video_dit_mask(gen: torch.Generator, B: int, H: int, latent: Tuple[int, int, int],
                         n_pad: int, blk: int = 128, rho: Tuple[float, float] = (0.05, 0.40),
                         aspect: Tuple[float, float] = (0.5, 2.0)):

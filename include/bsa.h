@@ -126,6 +126,37 @@ bsa_status bsa_plan_create(const uint8_t* mask, int B, int H, int NQB, int NKB, 
                            int bk, int gqa_group, void* workspace, size_t workspace_bytes,
                            int flags, void* stream, bsa_plan** out);
 
+/*
+ * bsa_plan_create_affine -- bsa_plan_create for a logical mask given (wholly
+ * or partly) by affine row descriptors ("SPLAT: A framework for optimised GPU
+ * code-generation for SParse reguLar ATtention", abstract: the
+ * affine-compressed-sparse-row format captures the regular geometry of
+ * sparse attention patterns, analysed just in time).  Each query head h owns
+ * segments seg_ptr[h] .. seg_ptr[h+1]-1 of `segments`; segment
+ * {a, b, stride, count} selects, for logical query block qb, the key blocks
+ *     a*qb + b + stride*t,  t = 0 .. count-1,  kept when in [0, NKB)
+ * (a = 1: relative to the query block -- sliding windows, strided and
+ * dilated patterns; a = 0: fixed key blocks -- global columns; stride may be
+ * negative, stride 0 repeats one block).  A head with segments selects their
+ * union, the same for every batch entry, generated by the plan kernels
+ * without reading mask bytes; a head without segments takes its rows of
+ * `mask` (irregular heads, e.g. random blocks).
+ * mask: device u8 [B][H][NQB][NKB] (only the rows of heads without segments
+ *   are read), or NULL when every head has segments (a head without
+ *   segments then selects nothing).
+ * segments: device int32 [nseg][4], 16-byte aligned (may be NULL if nseg = 0).
+ * seg_ptr: device int32 [H+1], non-decreasing; entries are clamped to
+ *   [0, nseg] on the device.  Both caller-owned; they are read by the plan
+ *   kernels of this call only.
+ * The plan and its arrays are exactly those bsa_plan_create builds from the
+ * expanded mask.  Other arguments and errors as bsa_plan_create.
+ */
+bsa_status bsa_plan_create_affine(const uint8_t* mask, const int32_t* segments,
+                                  const int32_t* seg_ptr, int nseg, int B, int H, int NQB,
+                                  int NKB, int bq, int bk, int gqa_group, void* workspace,
+                                  size_t workspace_bytes, int flags, void* stream,
+                                  bsa_plan** out);
+
 /* Copy the layout of an existing plan into *out. */
 bsa_status bsa_plan_get_layout(const bsa_plan* plan, bsa_plan_layout* out);
 

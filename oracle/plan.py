@@ -179,19 +179,23 @@ def affine_mask(segments, B: int, H: int, NQB: int, NKB: int, base=None) -> np.n
 
     a = 1 placing the segment relative to the query block (sliding windows,
     strided and dilated patterns), a = 0 at fixed key blocks (global
-    columns); stride may be negative, stride 0 repeats one block.  The mask
-    is the union over the head's segments, the same for every batch entry,
-    OR-ed with ``base`` ([B,H,NQB,NKB], any non-zero byte selects) when given.
+    columns); stride may be negative, stride 0 repeats one block.  A head
+    with segments selects their union, the same for every batch entry; a
+    head without any takes its rows of ``base`` ([B,H,NQB,NKB], any non-zero
+    byte selects; nothing when ``base`` is None), so irregular heads stay
+    explicit rows of a compressed-sparse-row mask.
     ``segments[h]`` is the list of (a, b, stride, count) of head h.
     """
     m = np.zeros((B, H, NQB, NKB), dtype=np.uint8)
     for h in range(H):
+        if not segments[h]:
+            if base is not None:
+                m[:, h] = (np.asarray(base)[:, h] != 0).astype(np.uint8)
+            continue
         for (a, b, stride, count) in segments[h]:
             for qb in range(NQB):
                 for t in range(count):
                     kb = a * qb + b + stride * t
                     if 0 <= kb < NKB:
                         m[:, h, qb, kb] = 1
-    if base is not None:
-        m |= (np.asarray(base) != 0).astype(np.uint8)
     return m

@@ -202,17 +202,20 @@ def test_affine_dilated_and_negative_stride():
     assert np.array_equal(fwd, rev)
 
 
-def test_affine_global_columns_zero_stride_union_with_base():
+def test_affine_global_columns_zero_stride_and_explicit_heads():
     NQB, NKB, G = 9, 20, 3
-    base = np.zeros((1, 2, NQB, NKB), dtype=np.uint8)
-    base[0, 1, 4, 17] = 9
-    segs = [[(0, 0, 1, G)], [(0, 11, 0, 4), (1, 100, 1, 3)]]  # head 1: one column (stride 0), one segment off the grid
-    m = OP.affine_mask(segs, 1, 2, NQB, NKB, base=base)
+    base = np.zeros((2, 3, NQB, NKB), dtype=np.uint8)
+    base[0, 1, 4, 17] = 9          # ignored: head 1 has segments
+    base[1, 2, 5, 6] = 1           # head 2 has none: its rows come from base
+    base[0, 2, 0, 0] = 200
+    segs = [[(0, 0, 1, G)], [(0, 11, 0, 4), (1, 100, 1, 3)], []]  # head 1: one column (stride 0), one segment off the grid
+    m = OP.affine_mask(segs, 2, 3, NQB, NKB, base=base)
     want0 = np.zeros((NQB, NKB), dtype=bool)
     want0[:, :G] = True
     want1 = np.zeros((NQB, NKB), dtype=bool)
     want1[:, 11] = True
-    want1[4, 17] = True
-    assert np.array_equal(m[0, 0] != 0, want0)
-    assert np.array_equal(m[0, 1] != 0, want1)
-    assert OP.affine_mask([[(1, 0, 1, 0)]], 1, 1, 4, 4).sum() == 0  # count 0 selects nothing
+    for b in range(2):
+        assert np.array_equal(m[b, 0] != 0, want0)
+        assert np.array_equal(m[b, 1] != 0, want1)
+    assert np.array_equal(m[:, 2] != 0, base[:, 2] != 0)
+    assert OP.affine_mask([[], [(1, 0, 1, 0)]], 1, 2, 4, 4).sum() == 0  # no base, count 0: nothing
