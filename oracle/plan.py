@@ -80,8 +80,51 @@ def unit_mask(mask: np.ndarray, mp: Mapping) -> np.ndarray:
     return np.repeat(np.repeat(sel, mp.sq, axis=2), mp.sk, axis=3)
 
 
-def build_plan(mask, bq: int, bk: int, gqa_group: int = 1) -> dict:
-    """Return every plan array as numpy (int32 / uint32 / int64)."""
+SIGMA_CANDIDATES = (1, 2, 4, 8, 16)
+
+
+def tile_qunits(t: int, sigma: int, rq: int):
+    """The rq q-units of q-tile t when a plane groups q-units with stride
+    sigma: tiles come in runs of sigma; tile t = run*sigma + r holds q-units
+    run*sigma*rq + r + i*sigma, i = 0 .. rq-1 (sigma = 1: t*rq + i)."""
+    run, r = divmod(t, sigma)
+    return [run * sigma * rq + r + i * sigma for i in range(rq)]
+
+
+def plane_slots(Up: np.ndarray, sigma: int, rq: int, rk: int) -> int:
+    """Slots a (b, h) plane needs (Up: bool [NQU, NKU]) with grouping stride
+    sigma: the sum over its q-tiles of ceil(|union of the tile's q-units| / rk)."""
+    NQT = Up.shape[0] // rq
+    total = 0
+    for t in range(NQT):
+        n = int(Up[tile_qunits(t, sigma, rq)].any(axis=0).sum())
+        total += -(-n // rk)
+    return total
+
+
+def choose_sigma(Up: np.ndarray, rq: int, rk: int) -> int:
+    """Physical-mapping choice of one plane (Tessera, abstract: logical blocks
+    are combined into physical tiles; reading: which q-units share a tile is
+    chosen per plane).  Among the strides that tile the plane exactly
+    (NQU divisible by sigma*rq), the one whose tiles need the fewest slots,
+    ties to the smaller stride."""
+    best, best_slots = 1, None
+    for sigma in SIGMA_CANDIDATES:
+        if Up.shape[0] % (sigma * rq):
+            continue
+        n = plane_slots(Up, sigma, rq, rk)
+        if best_slots is None or n < best_slots:
+            best, best_slots = sigma, n
+    return best
+
+
+def build_plan(mask, bq: int, bk: int, gqa_group: int = 1, remap: bool = False) -> dict:
+    """Return every plan array as numpy (int32 / uint32 / int64).
+
+    remap: choose each (b, h) plane's q-unit grouping stride (choose_sigma);
+    only when tiles combine several q-units (rq > 1) and without GQA
+    grouping (gqa_group = 1), otherwise every plane keeps stride 1.  The
+    strides are returned as plane_sigma [B*H]."""
     if hasattr(mask, "detach"):
         mask = mask.detach().cpu().numpy()
     mask = np.asarray(mask)
@@ -96,8 +139,17 @@ def build_plan(mask, bq: int, bk: int, gqa_group: int = 1) -> dict:
     NQT = NQU // mp.rq
     R = B * H * NQT
 
+    # Grouping stride of each plane, then the q-units of each plane's tiles.
+    sigma = np.ones(B * H, dtype=np.int64)
+    if remap and mp.rq > 1 and gqa_group == 1:
+        for bh in range(B * H):
+            sigma[bh] = choose_sigma(U[bh // H, bh % H], mp.rq, mp.rk)
+    Ut = np.empty((B, H, NQT, mp.rq, NKU), dtype=bool)
+    for bh in range(B * H):
+        for t in range(NQT):
+            Ut[bh // H, bh % H, t] = U[bh // H, bh % H, tile_qunits(t, int(sigma[bh]), mp.rq)]
     # Q-block union over the q-units of each q-tile.
-    u = U.reshape(B, H, NQT, mp.rq, NKU).any(axis=3)          # [B,H,NQT,NKU]
+    u = Ut.any(axis=3)                                         # [B,H,NQT,NKU]
     cnt = u.sum(axis=3).reshape(R)
     slots = (cnt + mp.rk - 1) // mp.rk
     row_ptr = np.zeros(R + 1, dtype=np.int64)
@@ -106,7 +158,7 @@ def build_plan(mask, bq: int, bk: int, gqa_group: int = 1) -> dict:
     slot_ku = np.full((S, mp.rk), -1, dtype=np.int64)
     slot_mask = np.zeros(S, dtype=np.uint64)
     ur = u.reshape(R, NKU)
-    Ur = U.reshape(B, H, NQT, mp.rq, NKU).reshape(R, mp.rq, NKU)
+    Ur = Ut.reshape(R, mp.rq, NKU)
     for r in range(R):
         ys = np.flatnonzero(ur[r])
         n = int(slots[r])
@@ -161,6 +213,7 @@ def build_plan(mask, bq: int, bk: int, gqa_group: int = 1) -> dict:
         "ukb": ukb.astype(np.int32),
         "order": order.astype(np.int32),
         "totals": totals,
+        "plane_sigma": sigma.astype(np.int32),
     }
 
 

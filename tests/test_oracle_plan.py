@@ -15,12 +15,21 @@ import os
 
 import numpy as np
 import pytest
+import torch
 
 from oracle import plan as OP
 from block_sparse_attention_plan_gb300 import workloads as W
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "plan_hand_examples.json")
 KEYS = ("row_ptr", "slot_ku", "slot_mask", "urow_ptr", "ukb", "order", "totals")
+
+
+def tile_rows(qt: int, sigma: int, rq: int):
+    """Plan format: the q-units row qt of a plane with grouping stride sigma
+    covers (runs of sigma tiles; tile run*sigma + r holds q-units
+    run*sigma*rq + r + i*sigma)."""
+    run, r = qt // sigma, qt % sigma
+    return [run * sigma * rq + r + i * sigma for i in range(rq)]
 
 
 def check_plan_invariants(mask: np.ndarray, bq: int, bk: int, g: int, p: dict):
@@ -41,9 +50,14 @@ def check_plan_invariants(mask: np.ndarray, bq: int, bk: int, g: int, p: dict):
     for b, h, qb, kb in zip(*np.nonzero(sel)):
         want[b, h, qb * bq:(qb + 1) * bq, kb * bk:(kb + 1) * bk] = True
     got = np.zeros_like(want)
+    sig = p.get("plane_sigma", np.ones(B * H, dtype=np.int32))
+    for bh in range(B * H):  # every plane's tiles partition its q-units
+        units = sorted(x for qt in range(NQT) for x in tile_rows(qt, int(sig[bh]), rq))
+        assert units == list(range(NQT * rq))
     for r in range(R):
         b, rem = divmod(r, H * NQT)
         h, qt = divmod(rem, NQT)
+        xs = tile_rows(qt, int(sig[b * H + h]), rq)
         ks = sk[rp[r]:rp[r + 1]].ravel()
         valid = ks[ks >= 0]
         # ascending, unique, padding only at the tail of the last slot
@@ -63,7 +77,7 @@ def check_plan_invariants(mask: np.ndarray, bq: int, bk: int, g: int, p: dict):
                 for i in range(rq):
                     if (bits >> (i * rk + j)) & 1:
                         col_on = True
-                        q0 = qt * 128 + i * qu
+                        q0 = xs[i] * qu
                         got[b, h, q0:q0 + qu, y * ku:(y + 1) * ku] = True
                 assert col_on, "a listed k-unit must be selected by some q-unit of the tile"
     np.testing.assert_array_equal(got, want)
@@ -219,3 +233,60 @@ def test_affine_global_columns_zero_stride_and_explicit_heads():
         assert np.array_equal(m[b, 1] != 0, want1)
     assert np.array_equal(m[:, 2] != 0, base[:, 2] != 0)
     assert OP.affine_mask([[], [(1, 0, 1, 0)]], 1, 2, 4, 4).sum() == 0  # no base, count 0: nothing
+
+
+# ---- per-plane q-unit grouping (physical mapping chosen at plan time) -----
+
+def test_remap_hand_example():
+    # 8 query blocks of 32 rows (four q-units per tile), 8 key blocks of 128
+    # (one unit per slot).  Query block x selects key block x % 2.
+    # Stride 1: tiles {0,1,2,3} and {4,5,6,7} each need key blocks {0,1}: 4 slots.
+    # Stride 2: tiles {0,2,4,6} -> {0} and {1,3,5,7} -> {1}: 2 slots.
+    # Stride 4 would need 16 q-units.  So stride 2: rows [0], [1], each slot's
+    # sub-mask has all four q-units (bits 0..3).
+    m = np.zeros((1, 1, 8, 8), dtype=np.uint8)
+    for x in range(8):
+        m[0, 0, x, x % 2] = 1
+    p = OP.build_plan(m, 32, 128, 1, remap=True)
+    assert p["plane_sigma"].tolist() == [2]
+    assert p["row_ptr"].tolist() == [0, 1, 2]
+    assert p["slot_ku"].tolist() == [0, 1]
+    assert p["slot_mask"].tolist() == [0b1111, 0b1111]
+    assert OP.build_plan(m, 32, 128, 1)["plane_sigma"].tolist() == [1]
+    check_plan_invariants(m, 32, 128, 1, p)
+
+
+def test_remap_tie_keeps_stride_one():
+    m = np.ones((1, 2, 16, 4), dtype=np.uint8)  # every grouping needs the same slots
+    assert OP.build_plan(m, 32, 128, 1, remap=True)["plane_sigma"].tolist() == [1, 1]
+
+
+def _slots_by_sets(sel, sigma, rq, rk):
+    NQT = sel.shape[0] // rq
+    total = 0
+    for qt in range(NQT):
+        cols = set()
+        for x in tile_rows(qt, sigma, rq):
+            cols |= set(np.flatnonzero(sel[x]).tolist())
+        total += -(-len(cols) // rk)
+    return total
+
+
+@pytest.mark.parametrize("bq,bk", [(32, 32), (64, 128), (32, 256), (64, 64)])
+def test_remap_choice_is_minimal_and_plan_valid(bq, bk):
+    W_ = W.regular_mask(torch.Generator().manual_seed(bq + bk), 1, 4, 64 if bq == 32 else 32,
+                        window=3, stride=4, dil_reach=9, glob=2, bb_window=2, bb_p=0.1)
+    m = W_.numpy()
+    if bk != bq:  # reshape the key axis to bk-sized blocks: keep NKB = Nk / bk
+        NKB = m.shape[2] * bq // bk
+        m = m[..., :NKB]
+    p = OP.build_plan(m, bq, bk, 1, remap=True)
+    check_plan_invariants(m, bq, bk, 1, p)
+    mp = OP.mapping(bq, bk)
+    U = OP.unit_mask(m, mp)
+    for h in range(m.shape[1]):
+        cand = {s: _slots_by_sets(U[0, h], s, mp.rq, mp.rk) for s in OP.SIGMA_CANDIDATES
+                if U.shape[2] % (s * mp.rq) == 0}
+        best = min(cand, key=lambda s: (cand[s], s))
+        assert int(p["plane_sigma"][h]) == best, (h, cand)
+    assert int(np.diff(p["row_ptr"]).sum()) <= int(np.diff(OP.build_plan(m, bq, bk, 1)["row_ptr"]).sum())
