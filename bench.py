@@ -278,6 +278,7 @@ def run_gb300(args):
     wsbuf = torch.empty(int(L.workspace_bytes), dtype=torch.uint8, device=dev)
     flop = w.active_flop
 
+    plan_flags = bsa.PLAN_REMAP if args.remap else 0
     affine = None
     if args.affine:
         # sliding, strided and dilated heads as affine row segments, the
@@ -292,9 +293,9 @@ def run_gb300(args):
             ev[2].record(stream)
         if affine is not None:
             p = bsa.plan_affine(affine[0], w.B, w.mask.shape[2], w.mask.shape[3], w.bq, w.bk,
-                                w.gqa_group, mask=affine[1], workspace=wsbuf)
+                                w.gqa_group, mask=affine[1], workspace=wsbuf, flags=plan_flags)
         else:
-            p = bsa.plan(mask_d, w.bq, w.bk, w.gqa_group, workspace=wsbuf)
+            p = bsa.plan(mask_d, w.bq, w.bk, w.gqa_group, workspace=wsbuf, flags=plan_flags)
         if ev is not None:
             ev[0].record(stream)
         bsa.forward(p, q, k, v, out=o, lse=lse, **fwd_extra)
@@ -375,6 +376,8 @@ def run_gb300(args):
     if args.page_size:
         cfg["kv_pages"] = (f"page_size {args.page_size}, pages shuffled across the pool, read "
                            "through a block table (e2e stays on contiguous host buffers)")
+    if args.remap:
+        cfg["plan_flags"] = "BSA_PLAN_REMAP: per-plane q-unit grouping stride chosen by slot count"
     if args.affine:
         cfg["plan_input"] = ("affine row segments for the sliding, strided and dilated heads; the "
                              "BigBird-style heads' rows read from the mask")
@@ -424,6 +427,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--page-size", type=int, default=0,
                     help="read K/V through a block table of pages of this many keys (0: contiguous)")
+    ap.add_argument("--remap", action="store_true",
+                    help="plan with BSA_PLAN_REMAP (per-plane q-unit grouping stride)")
     ap.add_argument("--affine", action="store_true",
                     help="regular workload: plan from affine row segments (+ residual mask bytes)")
     ap.add_argument("--causal", action="store_true",

@@ -19,6 +19,7 @@ STATUS_NAMES = {
     -4: "BSA_ERR_CUDA", -5: "BSA_ERR_WORKSPACE", -6: "BSA_ERR_TIMEOUT", -7: "BSA_ERR_PLAN_MISMATCH",
 }
 PLAN_NO_UNION = 0x1
+PLAN_REMAP = 0x2
 FWD_CAUSAL = 0x1
 
 
@@ -43,7 +44,7 @@ class Layout(ctypes.Structure):
         ("slot_capacity", ctypes.c_int64), ("union_capacity", ctypes.c_int64)] + [
         (n, ctypes.c_uint64) for n in (
             "off_row_ptr", "off_slot_ku", "off_slot_mask", "off_urow_ptr", "off_ukb",
-            "off_order", "off_totals", "off_control", "off_scratch", "workspace_bytes")]
+            "off_order", "off_totals", "off_control", "off_scratch", "workspace_bytes", "off_sigma")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -156,6 +157,7 @@ class Plan:
             "ukb": self._view(L.off_ukb, U, torch.int32),
             "order": self._view(L.off_order, L.rows, torch.int32),
             "totals": totals,
+            "plane_sigma": self._view(L.off_sigma, L.B * L.H, torch.int32),
         }
 
     def control(self) -> torch.Tensor:

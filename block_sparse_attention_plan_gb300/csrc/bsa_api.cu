@@ -35,7 +35,7 @@ bsa_status compute_layout(int B, int H, int NQB, int NKB, int bq, int bk, int g,
   if (B < 1 || H < 1 || NQB < 1 || NKB < 1 || g < 1) return BSA_ERR_INVALID_ARG;
   if (!supported_block(bq) || !supported_block(bk)) return BSA_ERR_UNSUPPORTED;
   if (H % g) return BSA_ERR_INVALID_ARG;
-  if (flags & ~BSA_PLAN_NO_UNION) return BSA_ERR_INVALID_ARG;
+  if (flags & ~(BSA_PLAN_NO_UNION | BSA_PLAN_REMAP)) return BSA_ERR_INVALID_ARG;
   bsa_plan_layout l;
   std::memset(&l, 0, sizeof(l));
   l.B = B; l.H = H; l.Hkv = H / g; l.NQB = NQB; l.NKB = NKB; l.bq = bq; l.bk = bk; l.gqa_group = g;
@@ -76,6 +76,7 @@ bsa_status compute_layout(int B, int H, int NQB, int NKB, int bq, int bk, int g,
   l.off_order = off;     off = align256(off + 4ull * rows);
   l.off_totals = off;    off = align256(off + 8ull * 4);
   l.off_control = off;   off = align256(off + 4ull * 16);
+  l.off_sigma = off;     off = align256(off + 4ull * (uint64_t)B * H);
   l.off_scratch = off;
   l.workspace_bytes = fwd_scratch(l).end;  // plan scratch, then forward scratch
   *L = l;
@@ -207,6 +208,7 @@ bsa_status create_plan(const uint8_t* mask, const int32_t* seg, const int32_t* s
   d.qu = L.qu; d.rq = L.rq; d.sq = L.sq; d.ku = L.ku; d.rk = L.rk; d.sk = L.sk;
   d.NQT = L.NQT; d.NKU = L.NKU; d.rows = L.rows; d.urows = L.urows;
   d.nkeys = nkeys; d.groups = L.groups;
+  d.remap = ((flags & BSA_PLAN_REMAP) && L.rq > 1 && gqa_group == 1 && L.NQT <= kMaxRemapTiles) ? 1 : 0;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(d.control, 0, 64, s) != cudaSuccess || launch_plan(d, s) != cudaSuccess) {
@@ -301,6 +303,7 @@ bsa_status bsa_forward_ex(const bsa_plan* plan, const void* Q, const void* K, co
   FwdParams fp;
   std::memset(&fp, 0, sizeof(fp));
   if (!encode_map(&fp.tmQ, Q, (uint64_t)qrows, d, kTile) ||
+      !encode_map(&fp.tmQu, Q, (uint64_t)qrows, d, L.qu) ||
       !encode_map(&fp.tmK, K, (uint64_t)kvrows, d, L.ku) ||
       !encode_map(&fp.tmV, V, (uint64_t)kvrows, d, L.ku))
     return BSA_ERR_CUDA;
@@ -318,6 +321,7 @@ bsa_status bsa_forward_ex(const bsa_plan* plan, const void* Q, const void* K, co
   fp.rowk = reinterpret_cast<float*>(p->ws + fs.off_rowk);
   fp.fb_flag = reinterpret_cast<int32_t*>(p->ws + fs.off_fb_flag);
   fp.fb_list = reinterpret_cast<int32_t*>(p->ws + fs.off_fb_list);
+  fp.sigma = p->dev.remap ? reinterpret_cast<const int32_t*>(p->ws + L.off_sigma) : nullptr;
   fp.slot_capacity = L.slot_capacity;
   fp.watchdog_ns = env_ll("BSA_WATCHDOG_MS", 1000) * 1000000ll;
   if (pages) {

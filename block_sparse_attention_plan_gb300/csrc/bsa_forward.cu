@@ -123,7 +123,8 @@ struct Item {
   int n;       // slots of the row (0 = empty or rejected)
   int s0;      // first slot index
   int bh;      // b*H + h
-  int qt;      // q-tile
+  int qx;      // first q-unit of the row's q-tile (its q-unit i is qx + i*qs)
+  int qs;      // q-unit stride of the plane (1 unless the plan regrouped it)
   int kvrow0;  // first K/V row of the head's sequence in the [B*Hkv*Nk, d] view
   bool valid;  // the schedule entry named a plan row
   int row;     // plan row
@@ -139,7 +140,7 @@ __device__ __forceinline__ void record_status(int32_t* ctl, int code, int site) 
 // Decode one schedule entry, rejecting out-of-range plan data (the row is then
 // treated as empty and BSA_ERR_PLAN_MISMATCH is recorded).
 __device__ __forceinline__ Item load_item(const FwdParams& p, int it, bool report) {
-  Item m{0, 0, 0, 0, 0, false, 0, it, 0.f};
+  Item m{0, 0, 0, 0, 1, 0, false, 0, it, 0.f};
   const int row = __ldg(p.order + it);
   if (row < 0 || row >= p.rows) {
     if (report) record_status(p.control, -7, kSitePlanRange);
@@ -149,7 +150,18 @@ __device__ __forceinline__ Item load_item(const FwdParams& p, int it, bool repor
   m.row = row;
   const int s0 = __ldg(p.row_ptr + row), s1 = __ldg(p.row_ptr + row + 1);
   m.bh = row / p.NQT;
-  m.qt = row % p.NQT;
+  const int qt = row % p.NQT;
+  m.qs = 1;
+  m.qx = qt * p.rq;
+  if (p.sigma != nullptr) {  // a plan built with regrouping
+    int sig = __ldg(p.sigma + m.bh);
+    if (!(sig == 1 || sig == 2 || sig == 4 || sig == 8 || sig == 16) || p.NQT % sig) {
+      if (report) record_status(p.control, -7, kSitePlanRange + 5);
+      sig = 1;
+    }
+    m.qs = sig;
+    m.qx = (qt / sig) * sig * p.rq + qt % sig;
+  }
   if (s0 < 0 || s1 < s0 || (long long)s1 > p.slot_capacity) {
     if (report) record_status(p.control, -7, kSitePlanRange + 1);
     return m;
@@ -182,7 +194,7 @@ __device__ __forceinline__ void sched_publish(uint8_t* smem, int slot, const Ite
   e[1] = m.n;
   e[2] = m.s0;
   e[3] = m.bh;
-  e[4] = m.qt;
+  e[4] = (m.qx << 5) | m.qs;
   e[5] = m.kvrow0;
   e[6] = m.valid ? m.row : -1;
   e[7] = __float_as_int(m.kb);
@@ -194,7 +206,7 @@ template <int D>
 __device__ __forceinline__ Item sched_take(const Smem<D>& sm, const uint8_t* smem, uint32_t t,
                                            bool lane_arrives, bool warp_sync, const Watchdog& wd) {
   using C = Cfg<D>;
-  Item m{0, 0, 0, 0, 0, false, 0, -2, 0.f};
+  Item m{0, 0, 0, 0, 1, 0, false, 0, -2, 0.f};
   const int slot = (int)(t % kSchedSlots);
   bool ok = mbar_wait(sm.bar(C::kBarSchedFull + slot), (t / kSchedSlots) & 1u, wd, kSiteSched);
   if (warp_sync) ok = __all_sync(0xffffffffu, ok);
@@ -204,7 +216,8 @@ __device__ __forceinline__ Item sched_take(const Smem<D>& sm, const uint8_t* sme
   m.n = e[1];
   m.s0 = e[2];
   m.bh = e[3];
-  m.qt = e[4];
+  m.qx = e[4] >> 5;
+  m.qs = e[4] & 31;
   m.kvrow0 = e[5];
   const int row = e[6];
   m.valid = row >= 0;
@@ -295,7 +308,10 @@ __device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, co
                                            const Watchdog wd, bool kside) {
   using C = Cfg<D>;
   const CUtensorMap* map = kside ? &p.tmK : &p.tmV;
-  if (kside) tma_prefetch_desc(&p.tmQ);
+  if (kside) {
+    tma_prefetch_desc(&p.tmQ);
+    tma_prefetch_desc(&p.tmQu);
+  }
   tma_prefetch_desc(map);
   const uint64_t pol_q = policy_evict_first();
   const uint64_t pol_kv = policy_evict_last();
@@ -318,7 +334,7 @@ __device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, co
         m = load_item(p, it, true);
         if (m.n > 0) m.kb = __ldg(p.rowk + m.row);
       } else {
-        m = Item{0, 0, 0, 0, 0, false, 0, -1, 0.f};
+        m = Item{0, 0, 0, 0, 1, 0, false, 0, -1, 0.f};
       }
       sched_publish<D>(smem, slot, m);
       mbar_arrive(sm.bar(C::kBarSchedFull + slot));
@@ -331,11 +347,21 @@ __device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, co
       const int qb = q_buf<D>(q_it);
       if (!mbar_wait(sm.bar(C::kBarQEmpty + qb), q_par<D>(q_it) ^ 1u, wd, kSiteQEmpty)) break;
       mbar_arrive_expect_tx(sm.bar(C::kBarQFull + qb), C::kTileBytes);
-      const int qrow = m.bh * p.Nq + m.qt * 128;
+      if (m.qs == 1) {  // the tile's q-units are contiguous: one 128-row box
+        const int qrow = m.bh * p.Nq + m.qx * p.qu;
 #pragma unroll
-      for (int c = 0; c < C::kChunks; ++c)
-        tma_load_2d(sm.q(qb) + c * C::kChunkBytes, &p.tmQ, c * 64, qrow,
-                    sm.bar(C::kBarQFull + qb), pol_q);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_2d(sm.q(qb) + c * C::kChunkBytes, &p.tmQ, c * 64, qrow,
+                      sm.bar(C::kBarQFull + qb), pol_q);
+      } else {  // q-unit i (qu rows) into tile rows [i*qu, (i+1)*qu)
+        for (int i = 0; i < p.rq; ++i) {
+          const int qrow = m.bh * p.Nq + (m.qx + i * m.qs) * p.qu;
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_2d(sm.q(qb) + c * C::kChunkBytes + i * p.qu * 128, &p.tmQu, c * 64, qrow,
+                        sm.bar(C::kBarQFull + qb), pol_q);
+        }
+      }
       ++q_it;
     }
     SlotKeys k0 = fetch_keys<kGeneral>(p, m, 0), k1 = k0;
@@ -644,7 +670,10 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     const Item m = sched_take<D>(sm, smem, t, lane == 0, true, wd);
     if (m.it < 0) break;
     if (!m.valid) continue;
-    const size_t orow = (size_t)m.bh * p.Nq + (size_t)m.qt * 128 + rloc;
+    // Query position of this thread's row: q-unit qi of the tile is q-unit
+    // qx + qi*qs of the head.
+    const int qpos = (m.qx + qi * m.qs) * p.qu + (rloc & (p.qu - 1));
+    const size_t orow = (size_t)m.bh * p.Nq + qpos;
     uint4* optr = reinterpret_cast<uint4*>(p.O + orow * D + h * (D / 2));
     if (m.n == 0) {  // no selected key: O = 0, LSE = -inf
 #pragma unroll
@@ -683,7 +712,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     if (lane == 0) mbar_arrive(sm.bar(C::kBarQEmpty + qb));
     ++q_it;
     if (kGeneral && p.elem_mask) {
-      const int qpos = m.qt * 128 + rloc, qmin = m.qt * 128 + quad * 32;
+      const int qmin = qpos - lane;  // the warp's 32 rows lie in one q-unit (qu >= 32)
       const int kvl = p.kv_lens ? __ldg(p.kv_lens + m.bh / p.H) : 0x7fffffff;
       lim_row = min(p.causal ? qpos + p.causal_off : 0x7fffffff, kvl - 1);
       lim_warp = min(p.causal ? qmin + p.causal_off : 0x7fffffff, kvl - 1);

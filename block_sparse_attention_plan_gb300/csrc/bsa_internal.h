@@ -12,6 +12,7 @@ namespace bsa {
 constexpr int kTile = 128;            // physical q-tile rows and K/V slot rows
 constexpr int kMaxKeys = 12288;       // bound on (slots per row + 1) for the sort
 constexpr int kMaxGroups = 8192;      // bound on K/V-head groups (B * Hkv)
+constexpr int kMaxRemapTiles = 8192;  // planes with more q-tiles keep grouping stride 1
 constexpr int kCtlWorkCounter = 0;    // control word indices
 constexpr int kCtlStatus = 1;
 constexpr int kCtlDetail = 2;
@@ -47,6 +48,8 @@ struct PlanDev {
   const int32_t* seg;      // affine row segments [nseg][4] = {a, b, stride, count}, or nullptr
   const int32_t* seg_ptr;  // [H + 1]: head h owns segments seg_ptr[h] .. seg_ptr[h+1]-1
   int nseg;
+  int32_t* sigma;  // [B*H] q-unit grouping stride of each plane
+  int remap;       // choose the strides (else all 1)
   int W;    // bitmap words per q-unit: ceil(NKU / 32)
   int vec;  // mask rows may be read 16 bytes at a time (16-byte aligned mask, NKB % 16 == 0)
 };
@@ -81,6 +84,7 @@ inline void set_plan_views(PlanDev& d, uint8_t* ws, const bsa_plan_layout& L) {
   d.order = reinterpret_cast<int32_t*>(ws + L.off_order);
   d.totals = reinterpret_cast<long long*>(ws + L.off_totals);
   d.control = reinterpret_cast<int32_t*>(ws + L.off_control);
+  d.sigma = reinterpret_cast<int32_t*>(ws + L.off_sigma);
   const PlanScratch s = plan_scratch(L);
   d.slots = reinterpret_cast<int32_t*>(ws + s.off_slots);
   d.lcnt = reinterpret_cast<int32_t*>(ws + s.off_lcnt);
@@ -116,6 +120,7 @@ struct FwdParams {
   CUtensorMap tmQ;   // Q viewed as [B*Hq*Nq, d], box {64, 128}, 128B swizzle
   CUtensorMap tmK;   // K viewed as [B*Hkv*Nk, d], box {64, ku}
   CUtensorMap tmV;   // V likewise
+  CUtensorMap tmQu;  // Q viewed as [B*Hq*Nq, d], box {64, qu}: one q-unit (regrouped tiles)
   const int32_t* row_ptr;
   const int32_t* slot_ku;
   const uint32_t* slot_mask;
@@ -135,6 +140,8 @@ struct FwdParams {
   // or an entry out of range), written by the row-bound pass; nullptr when
   // contiguous.
   int32_t* prow;
+  const int32_t* sigma;  // [B*H] q-unit grouping stride of each plane (plan array);
+                         // nullptr when the plan was built without regrouping
   // Element mask inside selected blocks.
   const int32_t* kv_lens;        // [B] or nullptr
   int causal;                    // key j visible to query i iff j <= i + causal_off

@@ -122,6 +122,7 @@ extern "C" bsa_status bsa_attention_static(const uint8_t* mask, int B, int H, in
   FwdParams fp;
   std::memset(&fp, 0, sizeof(fp));
   if (!encode_2d(&fp.tmQ, Q, (uint64_t)qrows, d, kTile) ||
+      !encode_2d(&fp.tmQu, Q, (uint64_t)qrows, d, L.qu) ||
       !encode_2d(&fp.tmK, K, (uint64_t)kvrows, d, L.ku) ||
       !encode_2d(&fp.tmV, V, (uint64_t)kvrows, d, L.ku))
     return BSA_ERR_CUDA;

@@ -208,8 +208,9 @@ __global__ void __launch_bounds__(kThreads) plan_count_kernel(const PlanDev p) {
       own += __shfl_xor_sync(0xffffffffu, own, s);
     }
     if (lane == 0) {
-      p.slots[r] = (cnt + p.rk - 1) / p.rk;
+      p.slots[r] = (cnt + p.rk - 1) / p.rk;  // grouping stride 1 (the choose kernel may redo it)
       p.lcnt[r] = own;
+      if (qt == 0) p.sigma[bh] = 1;
     }
   } else {
     const int ur = (blockIdx.x - row_ctas) * kWarps + warp;
@@ -247,6 +248,75 @@ __global__ void __launch_bounds__(kThreads) plan_count_kernel(const PlanDev p) {
     for (int s = 16; s > 0; s >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, s);
     if (lane == 0) p.ucnt[ur] = cnt;
   }
+}
+
+// q-unit i of q-tile qt in a plane grouped with stride s: tiles come in runs
+// of s, tile run*s + r holding q-units run*s*rq + r + i*s.
+__device__ __forceinline__ int tile_qunit(int qt, int s, int rq, int i) {
+  return (qt / s) * s * rq + qt % s + i * s;
+}
+
+// Grouping stride of a plane as the plan stores it (1 if out of range).
+__device__ __forceinline__ int plane_sigma(const PlanDev& p, int bh) {
+  const int s = p.sigma[bh];
+  return (s == 1 || s == 2 || s == 4 || s == 8 || s == 16) && p.NQT % s == 0 ? s : 1;
+}
+
+// Block-wide sum of one value per thread; every thread gets the total.
+__device__ long long block_sum(long long v, long long* red) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  long long t = 0;
+  for (int w = 0; w < (int)blockDim.x / 32; ++w) t += red[w];
+  __syncthreads();
+  return t;
+}
+
+// Per-plane choice of the q-unit grouping stride (physical mapping of
+// combined blocks, "Decoupling Logical Masks from GPU Execution for Dynamic
+// Block-Sparse Attention" (Tessera), abstract: logical blocks are combined
+// into physical tiles).  One CTA per (b, h) plane: for each stride s in
+// {1, 2, 4, 8, 16} dividing the plane's q-tiles, the slots its tiles need
+// (the sum over tiles of ceil(|OR of the tile's q-unit bitmaps| / rk)); the
+// fewest wins, ties to the smaller stride.  Writes the stride and the plane's
+// per-row slot counts for it.  Launched only with BSA_PLAN_REMAP.
+__global__ void __launch_bounds__(kThreads) plan_choose_kernel(const PlanDev p) {
+  extern __shared__ int tile_cnt[];  // [NQT] set bits of each tile's union
+  __shared__ long long red[kWarps];
+  const int bh = blockIdx.x;
+  const int NQU = p.NQT * p.rq;
+  const uint32_t* qb = p.qbits + (size_t)bh * NQU * p.W;
+  const long long pairs = (long long)p.NQT * p.W;
+  auto count_tiles = [&](int s) {
+    for (int t = threadIdx.x; t < p.NQT; t += kThreads) tile_cnt[t] = 0;
+    __syncthreads();
+    for (long long k = threadIdx.x; k < pairs; k += kThreads) {
+      const int t = (int)(k / p.W), w = (int)(k % p.W);
+      uint32_t u = 0u;
+      for (int i = 0; i < p.rq; ++i) u |= qb[(size_t)tile_qunit(t, s, p.rq, i) * p.W + w];
+      if (u) atomicAdd(&tile_cnt[t], __popc(u));
+    }
+    __syncthreads();
+  };
+  int best = 1;
+  long long best_slots = -1;
+  for (int s = 1; s <= 16; s <<= 1) {
+    if (p.NQT % s) continue;
+    count_tiles(s);
+    long long mine = 0;
+    for (int t = threadIdx.x; t < p.NQT; t += kThreads) mine += (tile_cnt[t] + p.rk - 1) / p.rk;
+    const long long total = block_sum(mine, red);
+    if (best_slots < 0 || total < best_slots) {
+      best = s;
+      best_slots = total;
+    }
+  }
+  count_tiles(best);
+  for (int t = threadIdx.x; t < p.NQT; t += kThreads)
+    p.slots[(size_t)bh * p.NQT + t] = (tile_cnt[t] + p.rk - 1) / p.rk;
+  if (threadIdx.x == 0) p.sigma[bh] = best;
 }
 
 // Block-wide exclusive scan of one value per thread (blockDim.x = 32 * nwarps);
@@ -369,13 +439,18 @@ __device__ void fill_row(const PlanDev& p, int r, int lane) {
   const int n = p.row_ptr[r + 1] - s0;
   const int cap = n * p.rk;
   int32_t* out = p.slot_ku + (size_t)s0 * p.rk;
-  const uint32_t* qb = p.qbits + (size_t)r * p.rq * p.W;
+  // Bitmaps of the tile's q-units (the plane's grouping stride decides which).
+  const int bh = r / p.NQT, qt = r % p.NQT, sig = plane_sigma(p, bh);
+  const uint32_t* qb[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    qb[i] = p.qbits + ((size_t)bh * p.NQT * p.rq + tile_qunit(qt, sig, p.rq, i < p.rq ? i : 0)) * p.W;
   int pos = 0;
   for (int w0 = 0; w0 < p.W; w0 += 32) {
     const int w = w0 + lane;
     uint32_t u = 0u;
     if (w < p.W) {
-      for (int i = 0; i < p.rq; ++i) u |= qb[(size_t)i * p.W + w];
+      for (int i = 0; i < p.rq; ++i) u |= qb[i][w];
     }
     pos += compact_word(u, w, lane, out, pos, cap);
   }
@@ -389,7 +464,7 @@ __device__ void fill_row(const PlanDev& p, int r, int lane) {
       const int y = out[s * p.rk + j];
       if (y < 0) continue;
       for (int i = 0; i < p.rq; ++i)
-        if ((qb[(size_t)i * p.W + (y >> 5)] >> (y & 31)) & 1u) bits |= 1u << (i * p.rk + j);
+        if ((qb[i][y >> 5] >> (y & 31)) & 1u) bits |= 1u << (i * p.rk + j);
     }
     p.slot_mask[s0 + s] = bits;
   }
@@ -480,6 +555,15 @@ cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream) {
   plan_count_kernel<<<row_ctas + union_ctas, kThreads, 0, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (p.remap) {
+    const size_t tiles_smem = (size_t)p.NQT * sizeof(int);
+    e = cudaFuncSetAttribute(plan_choose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxRemapTiles * (int)sizeof(int));
+    if (e != cudaSuccess) return e;
+    plan_choose_kernel<<<p.B * p.H, kThreads, tiles_smem, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   plan_scan_kernel<<<1, kScanThreads, groups_smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

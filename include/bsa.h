@@ -94,10 +94,22 @@ typedef struct bsa_plan_layout {
   uint64_t off_control;   /* int32 [16]: [0] work counter, [1] status, [2] status detail */
   uint64_t off_scratch;   /* plan-construction scratch */
   uint64_t workspace_bytes; /* total bytes the caller must provide */
+  uint64_t off_sigma;     /* int32 [B*H] q-unit grouping stride of each (b, h) plane:
+                           * q-tile t = run*s + r of a plane with stride s holds
+                           * q-units run*s*rq + r + i*s, i < rq (s = 1: t*rq + i) */
 } bsa_plan_layout;
 
 /* Plan flags */
 #define BSA_PLAN_NO_UNION 0x1   /* skip the GQA union table even when gqa_group > 1 */
+/* Choose each (b, h) plane's q-unit grouping stride among 1, 2, 4, 8, 16
+ * (those dividing the plane's q-tiles) by the slots its tiles need, fewest
+ * first, ties to the smaller stride -- the physical mapping of combined
+ * blocks ("Decoupling Logical Masks from GPU Execution for Dynamic
+ * Block-Sparse Attention" (Tessera), abstract: logical blocks are combined
+ * into physical tiles).  Only when tiles combine several q-units (bq < 128),
+ * gqa_group == 1 and the plane has at most 8192 q-tiles; otherwise (and
+ * without the flag) every stride is 1.  One extra kernel launch. */
+#define BSA_PLAN_REMAP 0x2
 
 /*
  * bsa_plan_layout_query -- sizes and workspace layout for a plan.

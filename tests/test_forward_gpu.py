@@ -146,3 +146,38 @@ def test_forward_long_video_sampled(bsa):
     e = assert_attention_close(og, lg, Oref, Lref, "long_video_dit sampled", scale=sc)
     print("long_video_dit", e)
     assert torch.all(o[0, :, -128:] == 0) and torch.all(torch.isneginf(lse[0, :, -128:]))
+
+
+
+@pytest.mark.parametrize("bq,bk,d", [(32, 32, 64), (64, 128, 128), (32, 256, 128)])
+def test_forward_remapped_plan_vs_oracle(bsa, bq, bk, d):
+    # Planes regrouped by the plan (q-units of a tile strided through the
+    # head): Q loads per q-unit, O/LSE rows written back to their positions.
+    w = W.random_problem(61 + bq, 2, 4, 4, 1024, 1024, d, bq, bk, 0.05)
+    NQB, NKB = 1024 // bq, 1024 // bk
+    x = torch.arange(NQB).view(NQB, 1)
+    kb = torch.arange(NKB).view(1, NKB)
+    w.mask[:, 1] |= ((kb % 4) == (x % 4)).to(torch.uint8)
+    w.mask[:, 2] |= ((kb % 2) == (x % 2)).to(torch.uint8)
+    p = bsa.plan(w.mask.cuda(), bq, bk, 1, flags=bsa.PLAN_REMAP)
+    assert max(p.arrays()["plane_sigma"].tolist()) > 1
+    o, lse = bsa.forward(p, w.q.cuda(), w.k.cuda(), w.v.cuda())
+    st, det = bsa.sync_status(p)
+    assert st == 0, (st, hex(det))
+    O, L = OA.block_gather(w.q, w.k, w.v, w.mask, bq, bk)
+    assert_attention_close(o, lse, O, L, f"remapped {bq}x{bk} d{d}")
+
+
+def test_forward_remapped_plan_causal_kv_lens(bsa):
+    w = W.random_problem(71, 2, 2, 2, 512, 1024, 64, 64, 64, 0.3)
+    NQB, NKB = 512 // 64, 1024 // 64
+    x = torch.arange(NQB).view(NQB, 1)
+    kb = torch.arange(NKB).view(1, NKB)
+    w.mask[:, 0] |= ((kb % 2) == (x % 2)).to(torch.uint8)
+    lens = torch.tensor([1000, 700], dtype=torch.int32)
+    p = bsa.plan(w.mask.cuda(), 64, 64, 1, flags=bsa.PLAN_REMAP)
+    o, lse = bsa.forward(p, w.q.cuda(), w.k.cuda(), w.v.cuda(), causal=True, kv_lens=lens.cuda())
+    st, det = bsa.sync_status(p)
+    assert st == 0, (st, hex(det))
+    O, L = OA.block_gather(w.q, w.k, w.v, w.mask, 64, 64, causal=True, kv_lens=lens.tolist())
+    assert_attention_close(o, lse, O, L, "remapped causal kv_lens")

@@ -21,7 +21,10 @@ def gpu_plan_arrays(bsa, mask, bq, bk, g):
 
 def assert_plan_equal(a, ref):
     assert int(a["totals"][3]) == 0  # reserved word
-    for k in ("row_ptr", "slot_ku", "slot_mask", "urow_ptr", "ukb", "order", "totals"):
+    keys = ["row_ptr", "slot_ku", "slot_mask", "urow_ptr", "ukb", "order", "totals"]
+    if "plane_sigma" in a and "plane_sigma" in ref:
+        keys.append("plane_sigma")
+    for k in keys:
         got = np.asarray(a[k]).astype(np.int64)
         want = np.asarray(ref[k]).astype(np.int64)
         if k == "totals":
@@ -94,3 +97,39 @@ def test_plan_long_rows_and_unaligned_mask(bsa, bq, bk):
     a2["slot_mask"] = a2["slot_mask"].astype(np.int64) & 0xFFFFFFFF
     assert bsa.plan_check(p) == 0
     assert_plan_equal(a2, ref)
+
+
+
+@pytest.mark.parametrize("name", ["tiny", "regular_small", "regular", "chunked_prefill_small"])
+def test_plan_remap_workloads_bit_exact(bsa, name):
+    w = W.make_workload(name, data=False)
+    p = bsa.plan(w.mask.cuda(), w.bq, w.bk, w.gqa_group, flags=bsa.PLAN_REMAP)
+    a = {k: (v.cpu().numpy() if torch.is_tensor(v) else v) for k, v in p.arrays().items()}
+    a["slot_mask"] = a["slot_mask"].astype(np.int64) & 0xFFFFFFFF
+    assert bsa.plan_check(p) == 0
+    ref = OP.build_plan(w.mask.numpy(), w.bq, w.bk, w.gqa_group, remap=True)
+    assert_plan_equal(a, ref)
+    if w.gqa_group > 1 or w.bq >= 128:
+        assert set(a["plane_sigma"].tolist()) == {1}
+
+
+@pytest.mark.parametrize("bq,bk,g", [(32, 32, 1), (32, 128, 1), (64, 64, 1), (64, 256, 1), (32, 64, 2)])
+def test_plan_remap_random_masks(bsa, bq, bk, g):
+    # strided rows (query block x selects key blocks = x mod 4, plus noise):
+    # grouping strides other than 1 win on some planes
+    B, H, Nq, Nk = 2, 4, 2048, 2048
+    NQB, NKB = Nq // bq, Nk // bk
+    gen = torch.Generator().manual_seed(bq * 5 + bk + g)
+    m = (torch.rand(B, H, NQB, NKB, generator=gen) < 0.04).to(torch.uint8)
+    x = torch.arange(NQB).view(NQB, 1)
+    kb = torch.arange(NKB).view(1, NKB)
+    m[:, 1] |= ((kb % 4) == (x % 4)).to(torch.uint8)
+    m[:, 2] |= ((kb % 2) == (x % 2)).to(torch.uint8)
+    p = bsa.plan(m.cuda(), bq, bk, g, flags=bsa.PLAN_REMAP)
+    a = {k: (v.cpu().numpy() if torch.is_tensor(v) else v) for k, v in p.arrays().items()}
+    a["slot_mask"] = a["slot_mask"].astype(np.int64) & 0xFFFFFFFF
+    assert bsa.plan_check(p) == 0
+    ref = OP.build_plan(m.numpy(), bq, bk, g, remap=True)
+    assert_plan_equal(a, ref)
+    if g == 1:
+        assert max(a["plane_sigma"].tolist()) > 1
