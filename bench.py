@@ -73,6 +73,14 @@ UNIT = "TFLOP/s"
 L2_BYTES = 129e6
 
 
+def _hbm_gbs() -> float:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"])
+    except Exception:
+        return 6800.0  # fallback figure
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -240,9 +248,14 @@ def run_gb300(args):
         # before any CUDA work: the oracle on the host cores, bounded sample
         r, dt, n, _ = oracle_sample_rate(w, args.cpu_seconds)
         B, H, NQB = w.mask.shape[:3]
+        from oracle import plan as OP
+        t0 = time.perf_counter()
+        OP.build_plan(w.mask.numpy(), w.bq, w.bk, w.gqa_group)
+        plan_s = time.perf_counter() - t0
         cpu = {"value": r, "unit": UNIT, "cores": _cores(), "kind": "oracle",
                "sample": f"{n} of {B * H * NQB} (b,h,q-block) rows of the same workload, seeded "
-                         f"permutation, {dt:.1f} s, fp64 NumPy oracle"}
+                         f"permutation, {dt:.1f} s, fp64 NumPy oracle",
+               "plan_oracle_s": plan_s, "plan_oracle_cores": 1}
 
     dist = ws > 1
     if dist:
@@ -279,6 +292,7 @@ def run_gb300(args):
     flop = w.active_flop
 
     plan_flags = bsa.PLAN_REMAP if args.remap else 0
+    remap_active = bool(args.remap and w.bq < 128 and w.gqa_group == 1 and w.Nq // 128 <= 8192)
     affine = None
     if args.affine:
         # sliding, strided and dilated heads as affine row segments, the
@@ -338,6 +352,13 @@ def run_gb300(args):
     st, det = bsa.sync_status(p)
     if st != 0:
         raise RuntimeError(f"device status {st} detail {det:#x} in the timed region")
+    # plan bytes (algorithmic): the mask read once (none for affine heads'
+    # rows, counted anyway), the plan arrays written once
+    tot = p.arrays()["totals"]
+    S_, U_ = int(tot[0]), int(tot[2])
+    R_ = p.layout.rows
+    plan_bytes = (w.mask.numel() + 4 * (R_ + 1) + 4 * S_ * p.layout.rk + 4 * S_ + 4 * R_
+                  + 4 * (p.layout.urows + 1) + 4 * U_)
     # a step = plan start -> forward end, timed with events on the launching stream
     ms = float(np.mean([c.elapsed_time(b) for _, b, c in fev]))
     fwd_ms = float(np.mean([a.elapsed_time(b) for a, b, _ in fev]))
@@ -402,8 +423,13 @@ def run_gb300(args):
         "e2e": {"value": flop * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
         "plan_ms": plan_ms,
-        # per step: 3 plan kernels + key norms, row bounds, bounded pass, exact pass
-        "gpu_launches": 7 * args.steps,
+        "plan": {"ms": plan_ms, "bytes": int(plan_bytes),
+                 "gbs": plan_bytes / (plan_ms * 1e-3) / 1e9,
+                 "frac_of_hbm": plan_bytes / (plan_ms * 1e-3) / 1e9 / _hbm_gbs(),
+                 "note": "plan kernels are latency-bound at these sizes (a few MB)"},
+        # per step: 3 plan kernels (+1 when regrouping is active) + key norms,
+        # row bounds, bounded pass, exact pass
+        "gpu_launches": (7 + int(remap_active)) * args.steps,
         "clocks": clk,
     }
     if cpu is not None:

@@ -46,7 +46,8 @@ def test_layout_matches_mapping_rule(bsa, name):
     assert L.urows == (B * w.Hkv * L.NQT if w.gqa_group > 1 else 0)
     assert L.max_row_slots == -(-L.NKU // L.rk)
     offs = [L.off_row_ptr, L.off_slot_ku, L.off_slot_mask, L.off_urow_ptr, L.off_ukb, L.off_order,
-            L.off_totals, L.off_control, L.off_scratch]
+            L.off_totals, L.off_control, L.off_sigma, L.off_scratch]
+    assert L.off_scratch - L.off_sigma >= 4 * B * H
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert L.off_slot_ku - L.off_slot_mask <= 0 and L.workspace_bytes > L.off_scratch
     assert L.off_slot_mask - L.off_slot_ku >= 4 * L.slot_capacity * L.rk
@@ -100,3 +101,33 @@ def test_create_and_forward_argument_errors_without_device(bsa_lib, bsa):
     assert bsa_lib.bsa_plan_check(None, None) == -1
     assert bsa_lib.bsa_watchdog_selftest(None, 1000, None) == -1
     bsa_lib.bsa_plan_destroy(None)  # no-op
+
+
+
+def test_plan_flags_and_layout_independent_of_remap(bsa):
+    L0 = bsa.plan_layout(2, 16, 256, 256, 32, 32, 1)
+    L1 = bsa.plan_layout(2, 16, 256, 256, 32, 32, 1, bsa.PLAN_REMAP)
+    assert L0.as_dict() == L1.as_dict()  # regrouping needs no extra workspace
+    with pytest.raises(bsa.BsaError) as e:
+        bsa.plan_layout(2, 16, 256, 256, 32, 32, 1, 0x4)  # unknown flag
+    assert e.value.status == -1
+
+
+def test_host_pipeline_buffer_sizes(bsa):
+    from block_sparse_attention_plan_gb300 import _lib as L
+    # video-DiT geometry: 24 units; chunks clamp to [1, units]; two slots
+    # from two chunks on; each slot holds one chunk's inputs, outputs and plan.
+    one = L.host_buffer_bytes(1, 24, 128, 128, 128, 128, 1, 128, 1)
+    two = L.host_buffer_bytes(1, 24, 128, 128, 128, 128, 1, 128, 2)
+    eight = L.host_buffer_bytes(1, 24, 128, 128, 128, 128, 1, 128, 8)
+    many = L.host_buffer_bytes(1, 24, 128, 128, 128, 128, 1, 128, 1000)
+    per_unit = 3 * 16384 * 128 * 2 + 16384 * 128 * 2 + 16384 * 4 + 128 * 128  # Q, K, V, O, LSE, mask
+    assert one >= 24 * per_unit
+    assert two >= 2 * 12 * per_unit and two < one * 1.2
+    assert eight >= 2 * 3 * per_unit and eight < two
+    assert many == L.host_buffer_bytes(1, 24, 128, 128, 128, 128, 1, 128, 24)
+    for bad in ((0,), (-3,)):
+        with pytest.raises(bsa.BsaError):
+            L.host_buffer_bytes(1, 24, 128, 128, 128, 128, 1, 128, *bad)
+    with pytest.raises(bsa.BsaError):
+        L.host_buffer_bytes(1, 24, 128, 128, 128, 128, 1, 96, 8)  # d not 64 / 128
