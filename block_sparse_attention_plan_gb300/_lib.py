@@ -20,6 +20,7 @@ STATUS_NAMES = {
 }
 PLAN_NO_UNION = 0x1
 PLAN_REMAP = 0x2
+STAGE_PREPARE, STAGE_BOUNDED, STAGE_EXACT, STAGE_ALL = 0x1, 0x2, 0x4, 0x7
 FWD_CAUSAL = 0x1
 
 
@@ -82,6 +83,8 @@ def library() -> ctypes.CDLL:
     lib.bsa_forward.argtypes = [P, VP, VP, VP, VP, VP, I, F, VP]
     lib.bsa_forward_ex.restype = I
     lib.bsa_forward_ex.argtypes = [P, VP, VP, VP, ctypes.POINTER(KVPagesC), VP, I, VP, VP, I, F, VP]
+    lib.bsa_forward_stage.restype = I
+    lib.bsa_forward_stage.argtypes = [P, VP, VP, VP, ctypes.POINTER(KVPagesC), VP, I, VP, VP, I, F, I, VP]
     lib.bsa_sync_status.restype = I
     lib.bsa_sync_status.argtypes = [P, VP, ctypes.POINTER(ctypes.c_int32)]
     lib.bsa_plan_check.restype = I
@@ -241,13 +244,15 @@ def forward(p: Plan, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
             stream: Optional[torch.cuda.Stream] = None,
             block_table: Optional[torch.Tensor] = None,
             kv_lens: Optional[torch.Tensor] = None,
-            causal: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
+            causal: bool = False, stages: Optional[int] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Block-sparse attention over plan ``p``.  Returns (O, LSE).
 
     Contiguous K/V: k, v [B, Hkv, Nk, d].  Paged K/V (``block_table`` given,
     int32 CUDA [B, max_pages]): k, v are pools [num_pages, Hkv, page_size, d].
     ``kv_lens`` (int32 CUDA [B]) and ``causal`` mask keys inside the selected
-    blocks (bsa_forward_ex)."""
+    blocks (bsa_forward_ex).  ``stages`` (STAGE_* bits) enqueues only those
+    stages of the forward (bsa_forward_stage); O and LSE are complete once
+    all three have run, in order."""
     L = p.layout
     for name, t in (("q", q), ("k", k), ("v", v)):
         if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
@@ -276,7 +281,14 @@ def forward(p: Plan, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     if lse is None:
         lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device)
     sc = 0.0 if scale is None else float(scale)
-    if pages is None and kv_lens is None and not causal:
+    if stages is not None:
+        _check(library().bsa_forward_stage(
+            p.handle, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+            ctypes.c_void_p(v.data_ptr()), ctypes.byref(pages) if pages is not None else None,
+            ctypes.c_void_p(kv_lens.data_ptr()) if kv_lens is not None else None,
+            FWD_CAUSAL if causal else 0, ctypes.c_void_p(out.data_ptr()),
+            ctypes.c_void_p(lse.data_ptr()), d, sc, int(stages), _stream_ptr(stream)), "bsa_forward_stage")
+    elif pages is None and kv_lens is None and not causal:
         _check(library().bsa_forward(
             p.handle, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
             ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),

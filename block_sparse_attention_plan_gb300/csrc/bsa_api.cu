@@ -272,6 +272,14 @@ bsa_status bsa_forward(const bsa_plan* plan, const void* Q, const void* K, const
 bsa_status bsa_forward_ex(const bsa_plan* plan, const void* Q, const void* K, const void* V,
                           const bsa_kv_pages* pages, const int32_t* kv_lens, int flags,
                           void* O, float* LSE, int d, float scale, void* stream) {
+  return bsa_forward_stage(plan, Q, K, V, pages, kv_lens, flags, O, LSE, d, scale,
+                           BSA_STAGE_ALL, stream);
+}
+
+bsa_status bsa_forward_stage(const bsa_plan* plan, const void* Q, const void* K, const void* V,
+                             const bsa_kv_pages* pages, const int32_t* kv_lens, int flags,
+                             void* O, float* LSE, int d, float scale, int stages, void* stream) {
+  if (stages <= 0 || (stages & ~BSA_STAGE_ALL)) return BSA_ERR_INVALID_ARG;
   const PlanImpl* p = as_impl(plan);
   if (!plan) return BSA_ERR_INVALID_ARG;
   if (!p) return BSA_ERR_PLAN_MISMATCH;
@@ -349,8 +357,9 @@ bsa_status bsa_forward_ex(const bsa_plan* plan, const void* Q, const void* K, co
   if (grid > L.rows) grid = L.rows;
   if (grid < 1) grid = 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(pd.control, 0, 64, s) != cudaSuccess) return BSA_ERR_CUDA;
-  if (launch_forward(fp, d, (int)grid, s) != cudaSuccess) return BSA_ERR_CUDA;
+  if ((stages & BSA_STAGE_PREPARE) && cudaMemsetAsync(pd.control, 0, 64, s) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  if (launch_forward(fp, d, (int)grid, s, stages) != cudaSuccess) return BSA_ERR_CUDA;
   return BSA_OK;
 }
 

@@ -1185,13 +1185,16 @@ __global__ void __launch_bounds__(256) rowbound_kernel(const FwdParams p) {
 }
 
 template <int D>
-cudaError_t launch_passes(const FwdParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_passes(const FwdParams& p, int grid, cudaStream_t stream, int stages) {
+  cudaError_t e = cudaSuccess;
+  const bool general = p.block_table != nullptr || p.elem_mask;
+  if (stages & BSA_STAGE_PREPARE) {
   const long long units = (long long)p.B * p.Hkv * p.NKU;
   const long long kgroups = (units + (kKmaxGroupBytes / (p.ku * D * 2)) - 1) / (kKmaxGroupBytes / (p.ku * D * 2));
   long long kgrid = 2ll * (p.sms > 0 ? p.sms : 1);
   if (kgrid > kgroups) kgrid = kgroups;
   if (kgrid < 1) kgrid = 1;
-  cudaError_t e = cudaFuncSetAttribute(kmax_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kKmaxSmem);
+  e = cudaFuncSetAttribute(kmax_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kKmaxSmem);
   if (e != cudaSuccess) return e;
   kmax_kernel<D><<<(unsigned)kgrid, kKmaxThreads, kKmaxSmem, stream>>>(p);
   e = cudaGetLastError();
@@ -1199,27 +1202,32 @@ cudaError_t launch_passes(const FwdParams& p, int grid, cudaStream_t stream) {
   rowbound_kernel<<<(unsigned)((p.rows + 7) / 8), 256, 0, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  FwdParams a = p;
-  a.work_counter = p.control + kCtlWorkCounter;
-  a.work_count = nullptr;
-  const bool general = p.block_table != nullptr || p.elem_mask;
-  e = general ? launch_d<D, false, true>(a, grid, stream) : launch_d<D, false, false>(a, grid, stream);
-  if (e != cudaSuccess) return e;
-  // Exact pass over the queued rows (exits at once when none was queued).
-  FwdParams x = p;
-  x.order = p.fb_list;
-  x.work_counter = p.control + kCtlFallbackWork;
-  x.work_count = p.control + kCtlFallbackCount;
-  return general ? launch_d<D, true, true>(x, grid, stream) : launch_d<D, true, false>(x, grid, stream);
+  }
+  if (stages & BSA_STAGE_BOUNDED) {
+    FwdParams a = p;
+    a.work_counter = p.control + kCtlWorkCounter;
+    a.work_count = nullptr;
+    e = general ? launch_d<D, false, true>(a, grid, stream) : launch_d<D, false, false>(a, grid, stream);
+    if (e != cudaSuccess) return e;
+  }
+  if (stages & BSA_STAGE_EXACT) {
+    // Exact pass over the queued rows (exits at once when none was queued).
+    FwdParams x = p;
+    x.order = p.fb_list;
+    x.work_counter = p.control + kCtlFallbackWork;
+    x.work_count = p.control + kCtlFallbackCount;
+    e = general ? launch_d<D, true, true>(x, grid, stream) : launch_d<D, true, false>(x, grid, stream);
+  }
+  return e;
 }
 
 }  // namespace
 
 int forward_smem_bytes(int d) { return d == 64 ? Cfg<64>::kSmemBytes : Cfg<128>::kSmemBytes; }
 
-cudaError_t launch_forward(const FwdParams& p, int d, int grid, cudaStream_t stream) {
-  if (d == 64) return launch_passes<64>(p, grid, stream);
-  return launch_passes<128>(p, grid, stream);
+cudaError_t launch_forward(const FwdParams& p, int d, int grid, cudaStream_t stream, int stages) {
+  if (d == 64) return launch_passes<64>(p, grid, stream, stages);
+  return launch_passes<128>(p, grid, stream, stages);
 }
 
 cudaError_t launch_watchdog_selftest(int32_t* status, long long limit_ns, cudaStream_t stream) {

@@ -159,7 +159,10 @@ struct FwdParams {
 cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream);
 // Key-norm pass, bounded-reference pass over every plan row, then the exact
 // pass over the rows the first one queued (see bsa_forward.cu).
-cudaError_t launch_forward(const FwdParams& p, int d, int grid, cudaStream_t stream);
+// `stages`: BSA_STAGE_* bits (the key-norm and row-bound passes, the bounded
+// pass, the exact pass), launched in that order.
+cudaError_t launch_forward(const FwdParams& p, int d, int grid, cudaStream_t stream,
+                           int stages = BSA_STAGE_ALL);
 int forward_smem_bytes(int d);
 cudaError_t launch_watchdog_selftest(int32_t* status, long long limit_ns, cudaStream_t stream);
 

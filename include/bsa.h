@@ -243,6 +243,25 @@ bsa_status bsa_forward_ex(const bsa_plan* plan, const void* Q, const void* K, co
                           void* O, float* LSE, int d, float scale, void* stream);
 
 /*
+ * bsa_forward_stage -- bsa_forward_ex in stages, so that a caller can time
+ * or interleave them: BSA_STAGE_PREPARE (reset the pass counters, the
+ * key-norm pass and the row-bound pass), BSA_STAGE_BOUNDED (the bounded
+ * pass over every plan row), BSA_STAGE_EXACT (the exact pass over the rows
+ * the bounded pass queued).  `stages` is a non-empty OR of them; the stages
+ * of one forward must be enqueued in that order on one stream, with the same
+ * arguments, and no other forward on the same plan in between.  Calling all
+ * three at once (BSA_STAGE_ALL) is bsa_forward_ex.  Errors as bsa_forward_ex,
+ * plus BSA_ERR_INVALID_ARG for an empty or unknown stage set.
+ */
+#define BSA_STAGE_PREPARE 0x1
+#define BSA_STAGE_BOUNDED 0x2
+#define BSA_STAGE_EXACT 0x4
+#define BSA_STAGE_ALL 0x7
+bsa_status bsa_forward_stage(const bsa_plan* plan, const void* Q, const void* K, const void* V,
+                             const bsa_kv_pages* pages, const int32_t* kv_lens, int flags,
+                             void* O, float* LSE, int d, float scale, int stages, void* stream);
+
+/*
  * bsa_sync_status -- synchronise `stream`, then report the status word the
  * last bsa_forward on this plan left: BSA_OK, BSA_ERR_TIMEOUT (a wait in the
  * kernel ran past the watchdog limit; the kernel stopped cleanly) or

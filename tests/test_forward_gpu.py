@@ -181,3 +181,23 @@ def test_forward_remapped_plan_causal_kv_lens(bsa):
     assert st == 0, (st, hex(det))
     O, L = OA.block_gather(w.q, w.k, w.v, w.mask, 64, 64, causal=True, kv_lens=lens.tolist())
     assert_attention_close(o, lse, O, L, "remapped causal kv_lens")
+
+
+@pytest.mark.parametrize("name", ["video_dit_small", "chunked_prefill_small"])
+def test_forward_in_stages_equals_forward(bsa, name):
+    w = W.make_workload(name)
+    p = bsa.plan(w.mask.cuda(), w.bq, w.bk, w.gqa_group)
+    q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    o1, l1 = bsa.forward(p, q, k, v)
+    o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
+    for st in (bsa.STAGE_PREPARE, bsa.STAGE_BOUNDED, bsa.STAGE_EXACT):
+        bsa.forward(p, q, k, v, out=o2, lse=l2, stages=st)
+    assert bsa.sync_status(p)[0] == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    o3, l3 = torch.empty_like(o1), torch.empty_like(l1)
+    bsa.forward(p, q, k, v, out=o3, lse=l3, stages=bsa.STAGE_PREPARE | bsa.STAGE_BOUNDED)
+    bsa.forward(p, q, k, v, out=o3, lse=l3, stages=bsa.STAGE_EXACT)
+    assert torch.equal(o1, o3)
+    for bad in (0, 0x8):
+        with pytest.raises(bsa.BsaError):
+            bsa.forward(p, q, k, v, stages=bad)
