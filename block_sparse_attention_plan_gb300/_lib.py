@@ -340,11 +340,12 @@ def attention(mask: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Ten
     overlapping streams; pinned memory keeps the copies asynchronous), with a
     device scratch buffer cached per shape; O and LSE come back in pinned host
     tensors (or ``out`` / ``lse_out``).  Device tensors: plan + forward.
+    Plans regroup q-units where that saves tiles (PLAN_REMAP).
     Returns (O, LSE) on the inputs' device."""
     host = not q.is_cuda
     g = q.shape[1] // k.shape[1]
     if not host:
-        pl = plan(mask, bq, bk, g, stream=stream)
+        pl = plan(mask, bq, bk, g, flags=PLAN_REMAP, stream=stream)
         return forward(pl, q, k, v, scale=scale, stream=stream)
     B, H, NQB, NKB = mask.shape
     d = q.shape[3]

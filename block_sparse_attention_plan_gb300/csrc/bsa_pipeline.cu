@@ -159,7 +159,8 @@ extern "C" bsa_status bsa_attention_host(const uint8_t* mask, int B, int H, int 
     if (i >= 2 && cudaStreamWaitEvent(user, P.d2h[s], 0) != cudaSuccess) return BSA_ERR_CUDA;
     bsa_plan* plan = nullptr;
     st = bsa_plan_create(sb + G.slot.mask, 1, nu * g, NQB, NKB, bq, bk, g, sb + G.slot.ws,
-                         (size_t)(G.slot.bytes - G.slot.ws), BSA_PLAN_NO_UNION, user, &plan);
+                         (size_t)(G.slot.bytes - G.slot.ws), BSA_PLAN_NO_UNION | BSA_PLAN_REMAP, user,
+                         &plan);
     if (st != BSA_OK) return st;
     bsa_plan_layout L;
     bsa_plan_get_layout(plan, &L);

@@ -339,7 +339,8 @@ bsa_status bsa_attention_static(const uint8_t* mask, int B, int H, int NQB, int 
  * buffer: device scratch of at least bsa_attention_host_buffer_bytes(...)
  * bytes, 256-byte aligned, owned by the caller (two chunk slots: inputs,
  * outputs, plan workspace; and one status word per chunk).
- * The GQA union table is not built (the forward does not read it).
+ * Plans are built with BSA_PLAN_REMAP and without the GQA union table (the
+ * forward does not read it).
  * Synchronous: returns once O and LSE are in host memory (it synchronises
  * `stream`).  Errors: BSA_ERR_INVALID_ARG, BSA_ERR_UNSUPPORTED,
  * BSA_ERR_WORKSPACE (buffer too small), BSA_ERR_ARCH, BSA_ERR_CUDA, and the
