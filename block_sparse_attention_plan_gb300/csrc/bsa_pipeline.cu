@@ -17,8 +17,9 @@
 // The pages describe the attention computation and its GPU execution, not
 // host transfers: this entry point is plumbing around the same plan and
 // forward kernels (each chunk is planned and run exactly as bsa_plan_create
-// + bsa_forward would run it, so every row's result is bit-identical to a
-// single device-resident call).
+// with BSA_PLAN_REMAP + bsa_forward would run it -- the stride choice is per
+// (b, h) plane, so chunking does not change it -- and every row's result is
+// bit-identical to a single device-resident call).
 #include <cstdint>
 #include <cstring>
 
