@@ -175,6 +175,25 @@ def oracle_sample_rate(w, budget_s: float, seed: int = 0, start: int = 0):
     return flop / dt / 1e12, dt, done, i
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of ``values`` over the ranks of the default
+    process group (identity without one): the job's time is its slowest
+    rank's."""
+    import torch
+    import torch.distributed as td
+    if not (td.is_available() and td.is_initialized()) or td.get_world_size() == 1:
+        return [float(x) for x in values]
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    td.all_reduce(t, op=td.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def whole_job_tflops(flop_per_rank: float, ms: float, world: int) -> float:
+    """Replicas (weak scaling): every rank runs the same workload, so the
+    job does world x the FLOP of one rank in the slowest rank's time."""
+    return flop_per_rank * world / (ms * 1e-3) / 1e12
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -372,10 +391,7 @@ def run_gb300(args):
     fwd_ms = float(np.mean([e[1].elapsed_time(e[4]) for e in fev]))
     plan_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in fev]))
     bounded_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in fev]))
-    if dist:
-        t = torch.tensor([ms, fwd_ms, bounded_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, fwd_ms, bounded_ms = float(t[0]), float(t[1]), float(t[2])
+    ms, fwd_ms, bounded_ms = max_over_ranks([ms, fwd_ms, bounded_ms], dev)
     clk = clocks.summary(t_wall0, t_wall1)
 
     # end to end through the public API, host (pinned) buffers, copies timed
@@ -392,15 +408,12 @@ def run_gb300(args):
         oh, lh = bsa.attention(mask_h, q_h, k_h, v_h, w.bq, w.bk, out=o_pin, lse_out=l_pin)
     torch.cuda.synchronize()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    (e2e_ms,) = max_over_ranks([e2e_ms], dev)
     clocks.stop()
     h2d = mask_h.numel() + (q_h.numel() + k_h.numel() + v_h.numel()) * 2
     d2h = oh.numel() * 2 + lh.numel() * 4
 
-    value = flop * ws / (ms * 1e-3) / 1e12
+    value = whole_job_tflops(flop, ms, ws)
     achieved = flop / (bounded_ms * 1e-3) / 1e12      # the dominant kernel's launch
     achieved_fwd = flop / (fwd_ms * 1e-3) / 1e12      # the whole bsa_forward
     cfg = _config(w)
@@ -432,7 +445,7 @@ def run_gb300(args):
                      "forward_ms": fwd_ms, "forward_achieved": achieved_fwd,
                      "forward_frac": achieved_fwd / peak, "peak_source": f"{peak_src} bf16 burst",
                      "frac_of_sustained": achieved / peak_sus},
-        "e2e": {"value": flop * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": whole_job_tflops(flop, e2e_ms, ws), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
         "plan_ms": plan_ms,
         "plan": {"ms": plan_ms, "bytes": int(plan_bytes),

@@ -1,0 +1,50 @@
+"""The multi-process path of bench.py on CPU: replicas only (no data-path
+collective), so what N > 1 adds is the job's timing -- the slowest rank's
+time, world x one rank's work -- computed with a gloo process group of two
+ranks here exactly as the NCCL group does it on GPUs."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, out):
+    import torch.distributed as td
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    td.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank r took (r + 1) ms per step and 10 - r ms end to end
+        ms, e2e = bench.max_over_ranks([1.0 + rank, 10.0 - rank])
+        out.put((rank, ms, e2e, bench.whole_job_tflops(6.0e11, ms, world)))
+    finally:
+        td.destroy_process_group()
+
+
+def test_max_over_ranks_and_whole_job_value_two_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, ms, e2e, tf in res:
+        assert ms == 2.0 and e2e == 10.0          # both ranks see the slowest rank's times
+        assert tf == pytest.approx(6.0e11 * 2 / 2.0e-3 / 1e12)
+
+
+def test_single_process_is_identity():
+    assert bench.max_over_ranks([3.5, 1.25]) == [3.5, 1.25]
+    assert bench.whole_job_tflops(1e12, 1.0, 1) == pytest.approx(1000.0)
