@@ -8,10 +8,11 @@ persistent tcgen05/TMA kernel over exactly those tiles.  Both run in libbsa.so
 generators.
 """
 from ._lib import (  # noqa: F401
-    BsaError, Layout, Plan, PLAN_NO_UNION, PLAN_REMAP, STAGE_ALL, STAGE_BOUNDED, STAGE_EXACT, STAGE_PREPARE, attention, attention_static, forward, library, plan, plan_affine,
+    BsaError, Layout, Plan, PLAN_NO_UNION, PLAN_REMAP, STAGE_ALL, STAGE_BOUNDED, STAGE_EXACT, STAGE_KNORM, STAGE_PREPARE,
+    STAGE_ROWBOUND, attention, attention_static, forward, library, plan, plan_affine,
     plan_check, plan_layout, sync_status, watchdog_selftest,
 )
 
 __all__ = ["BsaError", "Layout", "Plan", "PLAN_NO_UNION", "PLAN_REMAP", "STAGE_ALL", "STAGE_BOUNDED",
-           "STAGE_EXACT", "STAGE_PREPARE", "attention", "attention_static", "forward", "library",
+           "STAGE_EXACT", "STAGE_KNORM", "STAGE_PREPARE", "STAGE_ROWBOUND", "attention", "attention_static", "forward", "library",
            "plan", "plan_affine", "plan_check", "plan_layout", "sync_status", "watchdog_selftest"]

@@ -211,7 +211,10 @@ bsa_status create_plan(const uint8_t* mask, const int32_t* seg, const int32_t* s
   d.remap = ((flags & BSA_PLAN_REMAP) && L.rq > 1 && gqa_group == 1 && L.NQT <= kMaxRemapTiles) ? 1 : 0;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(d.control, 0, 64, s) != cudaSuccess || launch_plan(d, s) != cudaSuccess) {
+  // Pass counters and forward status only: a key-norm stage of this plan's
+  // forward may already be running on another stream.
+  if (cudaMemsetAsync(d.control, 0, 4 * (kCtlFallbackWork + 1), s) != cudaSuccess ||
+      launch_plan(d, s) != cudaSuccess) {
     delete impl;
     return BSA_ERR_CUDA;
   }
@@ -279,7 +282,8 @@ bsa_status bsa_forward_ex(const bsa_plan* plan, const void* Q, const void* K, co
 bsa_status bsa_forward_stage(const bsa_plan* plan, const void* Q, const void* K, const void* V,
                              const bsa_kv_pages* pages, const int32_t* kv_lens, int flags,
                              void* O, float* LSE, int d, float scale, int stages, void* stream) {
-  if (stages <= 0 || (stages & ~BSA_STAGE_ALL)) return BSA_ERR_INVALID_ARG;
+  constexpr int kAllBits = BSA_STAGE_ALL | BSA_STAGE_KNORM | BSA_STAGE_ROWBOUND;
+  if (stages <= 0 || (stages & ~kAllBits)) return BSA_ERR_INVALID_ARG;
   const PlanImpl* p = as_impl(plan);
   if (!plan) return BSA_ERR_INVALID_ARG;
   if (!p) return BSA_ERR_PLAN_MISMATCH;
@@ -357,7 +361,14 @@ bsa_status bsa_forward_stage(const bsa_plan* plan, const void* Q, const void* K,
   if (grid > L.rows) grid = L.rows;
   if (grid < 1) grid = 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((stages & BSA_STAGE_PREPARE) && cudaMemsetAsync(pd.control, 0, 64, s) != cudaSuccess)
+  // The key-norm stage resets its own status words, the row-bound stage the
+  // pass counters and the forward status (the two may run on different
+  // streams, the first beside the plan kernels).
+  if ((stages & (BSA_STAGE_PREPARE | BSA_STAGE_KNORM)) &&
+      cudaMemsetAsync(pd.control + kCtlKnormStatus, 0, 8, s) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  if ((stages & (BSA_STAGE_PREPARE | BSA_STAGE_ROWBOUND)) &&
+      cudaMemsetAsync(pd.control, 0, 4 * (kCtlFallbackWork + 1), s) != cudaSuccess)
     return BSA_ERR_CUDA;
   if (launch_forward(fp, d, (int)grid, s, stages) != cudaSuccess) return BSA_ERR_CUDA;
   return BSA_OK;
@@ -368,11 +379,12 @@ bsa_status bsa_sync_status(const bsa_plan* plan, void* stream, int32_t* detail) 
   if (!p) return BSA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return BSA_ERR_CUDA;
-  int32_t ctl[4] = {0, 0, 0, 0};
+  int32_t ctl[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   if (cudaMemcpy(ctl, p->dev.control, sizeof(ctl), cudaMemcpyDeviceToHost) != cudaSuccess)
     return BSA_ERR_CUDA;
-  if (detail) *detail = ctl[kCtlDetail];
-  return static_cast<bsa_status>(ctl[kCtlStatus]);
+  const bool knorm = ctl[kCtlStatus] == 0 && ctl[kCtlKnormStatus] != 0;
+  if (detail) *detail = knorm ? ctl[kCtlKnormDetail] : ctl[kCtlDetail];
+  return static_cast<bsa_status>(knorm ? ctl[kCtlKnormStatus] : ctl[kCtlStatus]);
 }
 
 bsa_status bsa_plan_check(const bsa_plan* plan, void* stream) {

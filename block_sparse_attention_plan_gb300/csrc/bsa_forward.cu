@@ -1030,7 +1030,7 @@ __global__ void __launch_bounds__(kKmaxThreads) kmax_kernel(const FwdParams p) {
   volatile int* abort_flag = reinterpret_cast<volatile int*>(kmax_smem + kKmaxStages * kKmaxGroupBytes + 64);
   int* skip_s = reinterpret_cast<int*>(kmax_smem + kKmaxStages * kKmaxGroupBytes + 128);  // [stages][32]
   float* rmax_s = reinterpret_cast<float*>(kmax_smem + kKmaxStages * kKmaxGroupBytes + 640);  // [8]
-  const Watchdog wd{abort_flag, p.control + kCtlStatus, p.control + kCtlDetail, p.watchdog_ns};
+  const Watchdog wd{abort_flag, p.control + kCtlKnormStatus, p.control + kCtlKnormDetail, p.watchdog_ns};
   const uint32_t ubytes = (uint32_t)p.ku * D * 2;
   const int G = (int)(kKmaxGroupBytes / ubytes);  // units per stage (1 .. 8)
   const long long units = (long long)p.B * p.Hkv * p.NKU;
@@ -1188,7 +1188,7 @@ template <int D>
 cudaError_t launch_passes(const FwdParams& p, int grid, cudaStream_t stream, int stages) {
   cudaError_t e = cudaSuccess;
   const bool general = p.block_table != nullptr || p.elem_mask;
-  if (stages & BSA_STAGE_PREPARE) {
+  if (stages & (BSA_STAGE_PREPARE | BSA_STAGE_KNORM)) {
   const long long units = (long long)p.B * p.Hkv * p.NKU;
   const long long kgroups = (units + (kKmaxGroupBytes / (p.ku * D * 2)) - 1) / (kKmaxGroupBytes / (p.ku * D * 2));
   long long kgrid = 2ll * (p.sms > 0 ? p.sms : 1);
@@ -1199,9 +1199,11 @@ cudaError_t launch_passes(const FwdParams& p, int grid, cudaStream_t stream, int
   kmax_kernel<D><<<(unsigned)kgrid, kKmaxThreads, kKmaxSmem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  rowbound_kernel<<<(unsigned)((p.rows + 7) / 8), 256, 0, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  }
+  if (stages & (BSA_STAGE_PREPARE | BSA_STAGE_ROWBOUND)) {
+    rowbound_kernel<<<(unsigned)((p.rows + 7) / 8), 256, 0, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
   if (stages & BSA_STAGE_BOUNDED) {
     FwdParams a = p;

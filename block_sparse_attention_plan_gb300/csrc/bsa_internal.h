@@ -18,6 +18,8 @@ constexpr int kCtlStatus = 1;
 constexpr int kCtlDetail = 2;
 constexpr int kCtlFallbackCount = 3;  // rows queued for the exact second pass
 constexpr int kCtlFallbackWork = 4;   // work counter of that pass
+constexpr int kCtlKnormStatus = 5;    // status / detail of the key-norm pass (its stage may
+constexpr int kCtlKnormDetail = 6;    // run beside the plan kernels; reset by that stage)
 
 // Wait sites recorded in the status detail word (low 8 bits).
 enum WaitSite : int {

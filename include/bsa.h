@@ -248,8 +248,9 @@ bsa_status bsa_forward_ex(const bsa_plan* plan, const void* Q, const void* K, co
  * key-norm pass and the row-bound pass), BSA_STAGE_BOUNDED (the bounded
  * pass over every plan row), BSA_STAGE_EXACT (the exact pass over the rows
  * the bounded pass queued).  `stages` is a non-empty OR of them; the stages
- * of one forward must be enqueued in that order on one stream, with the same
- * arguments, and no other forward on the same plan in between.  Calling all
+ * of one forward must run in that order, with the same arguments, and no
+ * other forward on the same plan in between (BSA_STAGE_KNORM may run on
+ * another stream, see below; the caller orders the streams).  Calling all
  * three at once (BSA_STAGE_ALL) is bsa_forward_ex.  Errors as bsa_forward_ex,
  * plus BSA_ERR_INVALID_ARG for an empty or unknown stage set.
  */
@@ -257,6 +258,12 @@ bsa_status bsa_forward_ex(const bsa_plan* plan, const void* Q, const void* K, co
 #define BSA_STAGE_BOUNDED 0x2
 #define BSA_STAGE_EXACT 0x4
 #define BSA_STAGE_ALL 0x7
+/* The two halves of BSA_STAGE_PREPARE: the key-norm pass (reads only K, so
+ * it may be enqueued on another stream before or while the plan is built,
+ * e.g. beside bsa_plan_create, as long as it completes before the row-bound
+ * pass starts) and the row-bound pass (needs the plan and the key norms). */
+#define BSA_STAGE_KNORM 0x8
+#define BSA_STAGE_ROWBOUND 0x10
 bsa_status bsa_forward_stage(const bsa_plan* plan, const void* Q, const void* K, const void* V,
                              const bsa_kv_pages* pages, const int32_t* kv_lens, int flags,
                              void* O, float* LSE, int d, float scale, int stages, void* stream);

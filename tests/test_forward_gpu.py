@@ -198,6 +198,29 @@ def test_forward_in_stages_equals_forward(bsa, name):
     bsa.forward(p, q, k, v, out=o3, lse=l3, stages=bsa.STAGE_PREPARE | bsa.STAGE_BOUNDED)
     bsa.forward(p, q, k, v, out=o3, lse=l3, stages=bsa.STAGE_EXACT)
     assert torch.equal(o1, o3)
-    for bad in (0, 0x8):
+    for bad in (0, 0x20):
         with pytest.raises(bsa.BsaError):
             bsa.forward(p, q, k, v, stages=bad)
+
+
+def test_key_norm_stage_beside_plan_creation(bsa):
+    # The key-norm stage reads only K: enqueued on a side stream that starts
+    # with the plan kernels (not after them), then the rest of the forward.
+    w = W.make_workload("chunked_prefill_small")
+    q, k, v, mask = w.q.cuda(), w.k.cuda(), w.v.cuda(), w.mask.cuda()
+    p0 = bsa.plan(mask, w.bq, w.bk, w.gqa_group)
+    o_ref, l_ref = bsa.forward(p0, q, k, v)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    fork = torch.cuda.Event()
+    for _ in range(3):
+        fork.record(main)
+        p = bsa.plan(mask, w.bq, w.bk, w.gqa_group)
+        side.wait_event(fork)
+        o, lse = torch.empty_like(o_ref), torch.empty_like(l_ref)
+        bsa.forward(p, q, k, v, out=o, lse=lse, stages=bsa.STAGE_KNORM, stream=side)
+        main.wait_stream(side)
+        bsa.forward(p, q, k, v, out=o, lse=lse,
+                    stages=bsa.STAGE_ROWBOUND | bsa.STAGE_BOUNDED | bsa.STAGE_EXACT)
+        assert bsa.sync_status(p)[0] == 0
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
