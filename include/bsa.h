@@ -334,8 +334,8 @@ bsa_status bsa_attention_static(const uint8_t* mask, int B, int H, int NQB, int 
  * bsa_attention_host -- plan + forward from HOST buffers, with the transfers
  * overlapped with the computation.  The pages describe the attention and its
  * GPU execution, not host transfers; this is plumbing around the same plan
- * and forward (each row's result is bit-identical to bsa_plan_create with
- * BSA_PLAN_REMAP + bsa_forward on device copies of the same inputs).
+ * and forward (each row's result is bit-identical to bsa_plan_create +
+ * bsa_forward on device copies of the same inputs).
  * The B*Hkv (batch, K/V head) units are cut into `chunks` contiguous chunks
  * (clamped to [1, B*Hkv]); chunk i is copied in on one stream, planned and
  * run on `stream`, and copied out on another, so that the copy-in of chunk
@@ -346,8 +346,8 @@ bsa_status bsa_attention_static(const uint8_t* mask, int B, int H, int NQB, int 
  * buffer: device scratch of at least bsa_attention_host_buffer_bytes(...)
  * bytes, 256-byte aligned, owned by the caller (two chunk slots: inputs,
  * outputs, plan workspace; and one status word per chunk).
- * Plans are built with BSA_PLAN_REMAP and without the GQA union table (the
- * forward does not read it).
+ * Plans are built without the GQA union table (the forward does not read
+ * it) and without regrouping.
  * Synchronous: returns once O and LSE are in host memory (it synchronises
  * `stream`).  Errors: BSA_ERR_INVALID_ARG, BSA_ERR_UNSUPPORTED,
  * BSA_ERR_WORKSPACE (buffer too small), BSA_ERR_ARCH, BSA_ERR_CUDA, and the

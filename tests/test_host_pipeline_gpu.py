@@ -1,9 +1,8 @@
 """GPU tests of bsa_attention_host: plan + forward from host buffers with the
 copies overlapped with the computation, chunk by chunk of (batch, K/V head)
 units.  Every row must equal, bit for bit, the device-resident path
-(bsa_plan_create with BSA_PLAN_REMAP, as the host path plans, + bsa_forward),
-which the forward parity tests pin to the oracle; one case is also compared
-with the oracle directly."""
+(bsa_plan_create + bsa_forward), which the forward parity tests pin to the
+oracle; one case is also compared with the oracle directly."""
 import ctypes
 
 import pytest
@@ -17,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 
 def device_path(bsa, w):
-    p = bsa.plan(w.mask.cuda(), w.bq, w.bk, w.gqa_group, flags=bsa.PLAN_REMAP)
+    p = bsa.plan(w.mask.cuda(), w.bq, w.bk, w.gqa_group)
     o, lse = bsa.forward(p, w.q.cuda(), w.k.cuda(), w.v.cuda())
     assert bsa.sync_status(p)[0] == 0
     return o.cpu(), lse.cpu()
