@@ -364,12 +364,15 @@ bsa_status bsa_forward_stage(const bsa_plan* plan, const void* Q, const void* K,
   // The key-norm stage resets its own status words, the row-bound stage the
   // pass counters and the forward status (the two may run on different
   // streams, the first beside the plan kernels).
-  if ((stages & (BSA_STAGE_PREPARE | BSA_STAGE_KNORM)) &&
-      cudaMemsetAsync(pd.control + kCtlKnormStatus, 0, 8, s) != cudaSuccess)
-    return BSA_ERR_CUDA;
-  if ((stages & (BSA_STAGE_PREPARE | BSA_STAGE_ROWBOUND)) &&
-      cudaMemsetAsync(pd.control, 0, 4 * (kCtlFallbackWork + 1), s) != cudaSuccess)
-    return BSA_ERR_CUDA;
+  const bool knorm = stages & (BSA_STAGE_PREPARE | BSA_STAGE_KNORM);
+  const bool rowbound = stages & (BSA_STAGE_PREPARE | BSA_STAGE_ROWBOUND);
+  if (knorm && rowbound) {  // one reset of both sets of words
+    if (cudaMemsetAsync(pd.control, 0, 4 * (kCtlKnormDetail + 1), s) != cudaSuccess) return BSA_ERR_CUDA;
+  } else if (knorm) {
+    if (cudaMemsetAsync(pd.control + kCtlKnormStatus, 0, 8, s) != cudaSuccess) return BSA_ERR_CUDA;
+  } else if (rowbound) {
+    if (cudaMemsetAsync(pd.control, 0, 4 * (kCtlFallbackWork + 1), s) != cudaSuccess) return BSA_ERR_CUDA;
+  }
   if (launch_forward(fp, d, (int)grid, s, stages) != cudaSuccess) return BSA_ERR_CUDA;
   return BSA_OK;
 }

@@ -70,7 +70,7 @@ bsa_status geometry(int B, int H, int NQB, int NKB, int bq, int bk, int g, int d
   s.bytes = off;
   const int nslots = G->chunks > 1 ? 2 : 1;
   G->status_off = s.bytes * nslots;
-  G->total = G->status_off + align256(8ull * G->chunks);  // two status words per chunk
+  G->total = G->status_off + align256(24ull * G->chunks);  // control words 1..6 of each chunk
   return BSA_OK;
 }
 
@@ -135,7 +135,7 @@ extern "C" bsa_status bsa_attention_host(const uint8_t* mask, int B, int H, int 
   if (cudaEventRecord(P.start, user) != cudaSuccess ||
       cudaStreamWaitEvent(P.in, P.start, 0) != cudaSuccess ||
       cudaStreamWaitEvent(P.out, P.start, 0) != cudaSuccess ||
-      cudaMemsetAsync(status_d, 0, 8ull * G.chunks, user) != cudaSuccess)
+      cudaMemsetAsync(status_d, 0, 24ull * G.chunks, user) != cudaSuccess)
     return BSA_ERR_CUDA;
 
   for (int i = 0; i < G.chunks; ++i) {
@@ -169,11 +169,9 @@ extern "C" bsa_status bsa_attention_host(const uint8_t* mask, int B, int H, int 
                      reinterpret_cast<float*>(sb + G.slot.lse), d, scale, user);
     bsa_plan_destroy(plan);
     if (st != BSA_OK) return st;
-    // Keep the chunk's device status words -- the forward's and the key-norm
-    // pass's (the next chunk in this slot resets them).
-    if (cudaMemcpyAsync(status_d + 2 * i, sb + G.slot.ws + L.off_control + 4 * kCtlStatus, 4,
-                        cudaMemcpyDeviceToDevice, user) != cudaSuccess ||
-        cudaMemcpyAsync(status_d + 2 * i + 1, sb + G.slot.ws + L.off_control + 4 * kCtlKnormStatus, 4,
+    // Keep the chunk's control words 1..6 -- among them the forward's and the
+    // key-norm pass's status (the next chunk in this slot resets them).
+    if (cudaMemcpyAsync(status_d + 6 * i, sb + G.slot.ws + L.off_control + 4 * kCtlStatus, 24,
                         cudaMemcpyDeviceToDevice, user) != cudaSuccess ||
         cudaEventRecord(P.comp[s], user) != cudaSuccess)
       return BSA_ERR_CUDA;
@@ -190,14 +188,17 @@ extern "C" bsa_status bsa_attention_host(const uint8_t* mask, int B, int H, int 
     return BSA_ERR_CUDA;
   // Host outputs are complete once the caller's stream is; report the first
   // chunk whose forward recorded a failure.
-  int32_t status_h[64];
+  int32_t status_h[6 * 16];
   if (cudaStreamSynchronize(user) != cudaSuccess) return BSA_ERR_CUDA;
-  for (int c0 = 0; c0 < 2 * G.chunks; c0 += 64) {
-    const int n = (2 * G.chunks - c0) < 64 ? (2 * G.chunks - c0) : 64;
-    if (cudaMemcpy(status_h, status_d + c0, 4ull * n, cudaMemcpyDeviceToHost) != cudaSuccess)
+  for (int c0 = 0; c0 < G.chunks; c0 += 16) {
+    const int n = (G.chunks - c0) < 16 ? (G.chunks - c0) : 16;
+    if (cudaMemcpy(status_h, status_d + 6 * c0, 24ull * n, cudaMemcpyDeviceToHost) != cudaSuccess)
       return BSA_ERR_CUDA;
-    for (int c = 0; c < n; ++c)
-      if (status_h[c] != 0) return static_cast<bsa_status>(status_h[c]);
+    for (int c = 0; c < n; ++c) {
+      const int32_t fwd = status_h[6 * c], knorm = status_h[6 * c + (kCtlKnormStatus - kCtlStatus)];
+      if (fwd != 0) return static_cast<bsa_status>(fwd);
+      if (knorm != 0) return static_cast<bsa_status>(knorm);
+    }
   }
   return BSA_OK;
 }
