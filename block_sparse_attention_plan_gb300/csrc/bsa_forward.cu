@@ -4,13 +4,22 @@
 // Source of the method: "Decoupling Logical Masks from GPU Execution for
 // Dynamic Block-Sparse Attention" (Tessera), abstract -- compute only the
 // blocks a logical mask selects, with tiles grouped per GPU task so that data
-// movement overlaps computation.  Online softmax over tiles (running max and
-// sum, rescaling the partial output) is the FlashAttention fusion the pages
-// refer to ("Sol-Attn" summary: inline sparsification inside the online
-// softmax).
+// movement overlaps computation.  The softmax over tiles is the
+// FlashAttention fusion the pages refer to ("Sol-Attn" summary: online
+// softmax), with a reading of its reference maximum described below.
+//
+// Passes of one forward (bsa_forward_stage can enqueue them separately):
+//   key-norm pass   the largest |k| of every K unit (reads K once);
+//   row-bound pass  per plan row, the largest of those over its units (and,
+//                   for paged K/V, each slot position's pool row);
+//   bounded pass    this kernel over every plan row with the row's reference
+//                   maximum m = |q| max|k| scale log2(e): no score exceeds
+//                   it, so no running maximum, exchange or rescale is needed;
+//                   a row whose weights would underflow is queued;
+//   exact pass      this kernel over the queued rows with a running maximum.
 //
 // One CTA (384 threads) per SM, looping over plan rows (one 128-row q-tile of
-// one head each) in longest-row-first order:
+// one head each, possibly of regrouped q-units) in schedule order:
 //   warp 0   (one thread) takes the work items, publishes them to the other
 //            roles, loads each row's Q tile and the K tiles of its slots into
 //            the K ring (shared-memory stages guarded by full/empty mbarriers);
@@ -26,8 +35,8 @@
 //            its scheduler;
 //   warps 4-11 the softmax: each row of a slot is shared by two threads, one
 //            in warps 4-7 (keys 0-63 of the slot) and one in warps 8-11 (keys
-//            64-127), which exchange their half-row maxima through shared
-//            memory so both use one running max and one O accumulator.
+//            64-127); they combine their row sums at the row's end (and, in
+//            the exact pass, their maxima while it runs).
 //
 // Tensor memory (512 x 32-bit columns x 128 lanes; lane = q-tile row):
 //   [0,128) S buffer 0   [128,256) S buffer 1   [256,256+d) O
@@ -71,9 +80,10 @@ constexpr float kRescaleSumBound = 65536.0f;  // 2^kRescaleThreshold
 // total weight (fp32 precision); a row below that (while it has selected
 // keys) is recomputed by the exact pass.
 constexpr float kFallbackPerKey = 0x1p-102f;
-// Work items (positions in the longest-row-first order) are taken from a
-// global atomic counter by the K producer and handed to the other roles
-// through a small ring in shared memory.
+// Work items (positions in the plan's schedule: K/V-head groups heaviest
+// first, rows longest first inside a group) are taken from a global atomic
+// counter by the K producer and handed to the other roles through a small
+// ring in shared memory.
 constexpr int kSchedSlots = 4;
 constexpr int kSchedConsumers = 1 + 2 + 8;  // V producer, two MMA threads, one lane per softmax warp
 
@@ -1007,7 +1017,8 @@ cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t stream) {
 // the rows it owns (16-byte reads rotated across the row so the threads of a
 // warp hit different banks).  Units wholly past the sequence's key length
 // (or, paged, without a valid page) get 0 and are not read: their keys are
-// masked.
+// masked.  A wait that runs out is recorded in the pass's own status words
+// (its stage may run on another stream beside the plan kernels).
 constexpr int kKmaxThreads = 128;
 constexpr int kKmaxStages = 3;
 constexpr uint32_t kKmaxGroupBytes = 32768;
