@@ -131,3 +131,41 @@ def test_host_pipeline_buffer_sizes(bsa):
             L.host_buffer_bytes(1, 24, 128, 128, 128, 128, 1, 128, *bad)
     with pytest.raises(bsa.BsaError):
         L.host_buffer_bytes(1, 24, 128, 128, 128, 128, 1, 96, 8)  # d not 64 / 128
+
+
+def test_affine_stage_and_host_argument_errors_without_device(bsa_lib, bsa):
+    # Every check below returns before the library touches a device: the
+    # pointers are host addresses that are never dereferenced.
+    L = bsa.plan_layout(1, 2, 4, 4, 128, 128)
+    out = ctypes.c_void_p()
+    buf = (ctypes.c_uint8 * 4096)()
+    aligned = (ctypes.addressof(buf) + 255) & ~255
+    VP = ctypes.c_void_p
+    geo = (1, 2, 4, 4, 128, 128, 1)
+    ws = (VP(aligned), L.workspace_bytes)
+    # affine plans: no seg_ptr; segments missing or misaligned; bad workspace
+    assert bsa_lib.bsa_plan_create_affine(None, VP(aligned), None, 1, *geo, *ws, 0, None,
+                                          ctypes.byref(out)) == -1
+    assert bsa_lib.bsa_plan_create_affine(None, None, VP(aligned), 1, *geo, *ws, 0, None,
+                                          ctypes.byref(out)) == -1
+    assert bsa_lib.bsa_plan_create_affine(None, VP(aligned + 4), VP(aligned), 1, *geo, *ws, 0,
+                                          None, ctypes.byref(out)) == -1
+    assert bsa_lib.bsa_plan_create_affine(None, VP(aligned), VP(aligned), -1, *geo, *ws, 0, None,
+                                          ctypes.byref(out)) == -1
+    assert bsa_lib.bsa_plan_create_affine(None, VP(aligned), VP(aligned), 1, *geo, VP(aligned),
+                                          L.workspace_bytes - 1, 0, None, ctypes.byref(out)) == -5
+    # staged forward: empty or unknown stage sets are rejected first
+    p = VP(aligned)
+    for bad in (0, -1, 0x20, 0x40):
+        assert bsa_lib.bsa_forward_stage(None, p, p, p, None, None, 0, p, p, 128, 0.0, bad,
+                                         None) == -1
+    assert bsa_lib.bsa_forward_stage(None, p, p, p, None, None, 0, p, p, 128, 0.0,
+                                     bsa.STAGE_ALL, None) == -1       # NULL plan
+    # host pipeline: NULL buffers, misaligned device buffer, too small, bad chunks
+    n = ctypes.c_size_t(0)
+    assert bsa_lib.bsa_attention_host_buffer_bytes(1, 2, 4, 4, 128, 128, 1, 64, 2, ctypes.byref(n)) == 0
+    args = (p, 1, 2, 4, 4, 128, 128, 1, p, p, p, p, p, 64, 0.0)
+    assert bsa_lib.bsa_attention_host(None, *args[1:], 2, p, n.value, None) == -1
+    assert bsa_lib.bsa_attention_host(*args, 2, VP(aligned + 16), n.value, None) == -1
+    assert bsa_lib.bsa_attention_host(*args, 2, p, n.value - 1, None) == -5
+    assert bsa_lib.bsa_attention_host(*args, 0, p, n.value, None) == -1
