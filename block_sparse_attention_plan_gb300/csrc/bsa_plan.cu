@@ -350,33 +350,52 @@ __device__ T block_exclusive_scan(T v, T* excl_out, T* warp_sums) {
 
 // Exclusive prefix sum of in[0..n) into out[0..n] (out[n] = total) by one
 // block: each thread sums a contiguous run (loads issued kRun at a time), the
-// run sums are scanned once, then each thread writes its run's prefixes.
+// run sums are scanned once, then each thread writes its run's prefixes --
+// from the values still in registers when its run fits in one batch.  With
+// in2, the sum of in2[0..n) is taken in the same load pass (*sum2).
 constexpr int kRun = 16;
 template <typename TIn>
-__device__ long long block_scan_array(const TIn* in, int32_t* out, int n, long long* wsum) {
+__device__ long long block_scan_array(const TIn* in, int32_t* out, int n, long long* wsum,
+                                      const TIn* in2 = nullptr, long long* sum2 = nullptr) {
   const int per = (n + blockDim.x - 1) / blockDim.x;
   const int i0 = threadIdx.x * per;
   const int i1 = min(i0 + per, n);
-  long long local = 0;
+  long long local = 0, local2 = 0;
+  TIn t[kRun] = {};
   for (int b = i0; b < i1; b += kRun) {
-    TIn t[kRun];
 #pragma unroll
     for (int k = 0; k < kRun; ++k) t[k] = (b + k < i1) ? in[b + k] : TIn(0);
+    if (in2 != nullptr) {
+#pragma unroll
+      for (int k = 0; k < kRun; ++k) local2 += (b + k < i1) ? (long long)in2[b + k] : 0ll;
+    }
 #pragma unroll
     for (int k = 0; k < kRun; ++k) local += (long long)t[k];
   }
   long long ex;
   const long long total = block_exclusive_scan<long long>(local, &ex, wsum);
+  if (in2 != nullptr) {
+    long long ex2;
+    const long long total2 = block_exclusive_scan<long long>(local2, &ex2, wsum);
+    if (sum2) *sum2 = total2;
+  }
   if (out) {
     long long run = ex;
-    for (int b = i0; b < i1; b += kRun) {
-      TIn t[kRun];
-#pragma unroll
-      for (int k = 0; k < kRun; ++k) t[k] = (b + k < i1) ? in[b + k] : TIn(0);
+    if (per <= kRun) {  // the run is still in t[]
 #pragma unroll
       for (int k = 0; k < kRun; ++k) {
-        if (b + k < i1) out[b + k] = (int32_t)run;
+        if (i0 + k < i1) out[i0 + k] = (int32_t)run;
         run += (long long)t[k];
+      }
+    } else {
+      for (int b = i0; b < i1; b += kRun) {
+#pragma unroll
+        for (int k = 0; k < kRun; ++k) t[k] = (b + k < i1) ? in[b + k] : TIn(0);
+#pragma unroll
+        for (int k = 0; k < kRun; ++k) {
+          if (b + k < i1) out[b + k] = (int32_t)run;
+          run += (long long)t[k];
+        }
       }
     }
     if (threadIdx.x == 0) out[n] = (int32_t)total;
@@ -387,9 +406,14 @@ __device__ long long block_scan_array(const TIn* in, int32_t* out, int n, long l
 __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(const PlanDev p) {
   __shared__ long long wsum[32];
   extern __shared__ int work_s[];  // [groups] total slots per K/V-head group
-  const long long S = block_scan_array<int32_t>(p.slots, p.row_ptr, p.rows, wsum);
-  const long long A = block_scan_array<int32_t>(p.lcnt, nullptr, p.rows, wsum);
-  const long long U = block_scan_array<int32_t>(p.ucnt, p.urow_ptr, p.urows, wsum);
+  long long A = 0;  // selected logical blocks: summed in the row-pointer scan's load pass
+  const long long S = block_scan_array<int32_t>(p.slots, p.row_ptr, p.rows, wsum, p.lcnt, &A);
+  long long U = 0;
+  if (p.urows > 0) {
+    U = block_scan_array<int32_t>(p.ucnt, p.urow_ptr, p.urows, wsum);
+  } else if (threadIdx.x == 0) {
+    p.urow_ptr[0] = 0;
+  }
   if (threadIdx.x == 0) {
     p.totals[0] = S;
     p.totals[1] = A;
