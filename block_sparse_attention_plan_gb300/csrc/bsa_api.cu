@@ -145,6 +145,82 @@ const PlanImpl* as_impl(const bsa_plan* p) {
 
 }  // namespace
 
+namespace bsa {
+// Forward parameters of one plan (layout L, device views pd, workspace ws)
+// for the given tensors: the TMA views of Q (128-row and q-unit boxes), K and
+// V (contiguous or paged pools), the plan and scratch pointers, the element
+// mask and the grid (one CTA per SM, at most one per plan row; grid_override
+// > 0 replaces the SM count).  Validates the pages and the view sizes.
+bsa_status make_fwd_params(const bsa_plan_layout& L, const PlanDev& pd, uint8_t* ws, bool remapped,
+                           const void* Q, const void* K, const void* V, const bsa_kv_pages* pages,
+                           const int32_t* kv_lens, int flags, void* O, float* LSE, int d,
+                           float scale, int dev, long long watchdog_ns, long long grid_override,
+                           FwdParams* out, int* grid_out) {
+  const long long Nq = (long long)L.NQB * L.bq, Nk = (long long)L.NKB * L.bk;
+  const long long qrows = (long long)L.B * L.H * Nq;
+  long long kvrows = (long long)L.B * L.Hkv * Nk;
+  if (pages) {
+    if (!pages->block_table || pages->max_pages < 1 || pages->page_size < 1 || pages->num_pages < 1)
+      return BSA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(pages->block_table) & 3u) return BSA_ERR_INVALID_ARG;
+    if (pages->page_size % L.ku) return BSA_ERR_UNSUPPORTED;
+    if ((long long)pages->max_pages * pages->page_size < Nk) return BSA_ERR_INVALID_ARG;
+    kvrows = (long long)pages->num_pages * L.Hkv * pages->page_size;
+  }
+  if (qrows >= (1ll << 31) || kvrows >= (1ll << 31)) return BSA_ERR_UNSUPPORTED;
+
+  FwdParams& fp = *out;
+  std::memset(&fp, 0, sizeof(fp));
+  if (!encode_map(&fp.tmQ, Q, (uint64_t)qrows, d, kTile) ||
+      !encode_map(&fp.tmQu, Q, (uint64_t)qrows, d, L.qu) ||
+      !encode_map(&fp.tmK, K, (uint64_t)kvrows, d, L.ku) ||
+      !encode_map(&fp.tmV, V, (uint64_t)kvrows, d, L.ku))
+    return BSA_ERR_CUDA;
+  fp.row_ptr = pd.row_ptr;
+  fp.slot_ku = pd.slot_ku;
+  fp.slot_mask = pd.slot_mask;
+  fp.order = pd.order;
+  fp.control = pd.control;
+  fp.O = static_cast<uint16_t*>(O);
+  fp.LSE = LSE;
+  fp.K = static_cast<const uint16_t*>(K);
+  const FwdScratch fs = fwd_scratch(L);
+  fp.kmax = reinterpret_cast<float*>(ws + fs.off_kmax);
+  fp.rowk = reinterpret_cast<float*>(ws + fs.off_rowk);
+  fp.fb_flag = reinterpret_cast<int32_t*>(ws + fs.off_fb_flag);
+  fp.fb_list = reinterpret_cast<int32_t*>(ws + fs.off_fb_list);
+  fp.sigma = remapped ? reinterpret_cast<const int32_t*>(ws + L.off_sigma) : nullptr;
+  fp.slot_capacity = L.slot_capacity;
+  fp.watchdog_ns = watchdog_ns;
+  if (pages) {
+    fp.block_table = pages->block_table;
+    fp.max_pages = pages->max_pages;
+    fp.page_size = pages->page_size;
+    fp.num_pages = pages->num_pages;
+    fp.prow = reinterpret_cast<int32_t*>(ws + fs.off_prow);
+  }
+  fp.kv_lens = kv_lens;
+  fp.causal = (flags & BSA_FWD_CAUSAL) ? 1 : 0;
+  fp.causal_off = (int)(Nk - Nq);
+  fp.elem_mask = (fp.causal || kv_lens) ? 1 : 0;
+  fp.B = L.B; fp.H = L.H; fp.Hkv = L.Hkv; fp.g = L.gqa_group; fp.NQT = L.NQT; fp.NKU = L.NKU;
+  fp.Nq = (int)Nq; fp.Nk = (int)Nk; fp.rq = L.rq; fp.rk = L.rk; fp.qu = L.qu; fp.ku = L.ku;
+  fp.rows = L.rows;
+  const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)d);
+  fp.scale_log2 = (float)(sc * 1.4426950408889634);
+
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  fp.sms = sms;
+  long long grid = grid_override > 0 ? grid_override : sms;
+  if (grid > L.rows) grid = L.rows;
+  if (grid < 1) grid = 1;
+  *grid_out = (int)grid;
+  return BSA_OK;
+}
+}  // namespace bsa
+
 extern "C" {
 
 int bsa_version(void) { return BSA_VERSION; }
@@ -298,68 +374,13 @@ bsa_status bsa_forward_stage(const bsa_plan* plan, const void* Q, const void* K,
   bsa_status st = check_arch(&dev);
   if (st != BSA_OK) return st;
   if (dev != p->device) return BSA_ERR_PLAN_MISMATCH;
-  const bsa_plan_layout& L = p->L;
-  const long long Nq = (long long)L.NQB * L.bq, Nk = (long long)L.NKB * L.bk;
-  const long long qrows = (long long)L.B * L.H * Nq;
-  long long kvrows = (long long)L.B * L.Hkv * Nk;
-  if (pages) {
-    if (!pages->block_table || pages->max_pages < 1 || pages->page_size < 1 || pages->num_pages < 1)
-      return BSA_ERR_INVALID_ARG;
-    if (reinterpret_cast<uintptr_t>(pages->block_table) & 3u) return BSA_ERR_INVALID_ARG;
-    if (pages->page_size % L.ku) return BSA_ERR_UNSUPPORTED;
-    if ((long long)pages->max_pages * pages->page_size < Nk) return BSA_ERR_INVALID_ARG;
-    kvrows = (long long)pages->num_pages * L.Hkv * pages->page_size;
-  }
-  if (qrows >= (1ll << 31) || kvrows >= (1ll << 31)) return BSA_ERR_UNSUPPORTED;
-
-  FwdParams fp;
-  std::memset(&fp, 0, sizeof(fp));
-  if (!encode_map(&fp.tmQ, Q, (uint64_t)qrows, d, kTile) ||
-      !encode_map(&fp.tmQu, Q, (uint64_t)qrows, d, L.qu) ||
-      !encode_map(&fp.tmK, K, (uint64_t)kvrows, d, L.ku) ||
-      !encode_map(&fp.tmV, V, (uint64_t)kvrows, d, L.ku))
-    return BSA_ERR_CUDA;
   const PlanDev& pd = p->dev;
-  fp.row_ptr = pd.row_ptr;
-  fp.slot_ku = pd.slot_ku;
-  fp.slot_mask = pd.slot_mask;
-  fp.order = pd.order;
-  fp.control = pd.control;
-  fp.O = static_cast<uint16_t*>(O);
-  fp.LSE = LSE;
-  fp.K = static_cast<const uint16_t*>(K);
-  const FwdScratch fs = fwd_scratch(L);
-  fp.kmax = reinterpret_cast<float*>(p->ws + fs.off_kmax);
-  fp.rowk = reinterpret_cast<float*>(p->ws + fs.off_rowk);
-  fp.fb_flag = reinterpret_cast<int32_t*>(p->ws + fs.off_fb_flag);
-  fp.fb_list = reinterpret_cast<int32_t*>(p->ws + fs.off_fb_list);
-  fp.sigma = p->dev.remap ? reinterpret_cast<const int32_t*>(p->ws + L.off_sigma) : nullptr;
-  fp.slot_capacity = L.slot_capacity;
-  fp.watchdog_ns = env_ll("BSA_WATCHDOG_MS", 1000) * 1000000ll;
-  if (pages) {
-    fp.block_table = pages->block_table;
-    fp.max_pages = pages->max_pages;
-    fp.page_size = pages->page_size;
-    fp.num_pages = pages->num_pages;
-    fp.prow = reinterpret_cast<int32_t*>(p->ws + fs.off_prow);
-  }
-  fp.kv_lens = kv_lens;
-  fp.causal = (flags & BSA_FWD_CAUSAL) ? 1 : 0;
-  fp.causal_off = (int)(Nk - Nq);
-  fp.elem_mask = (fp.causal || kv_lens) ? 1 : 0;
-  fp.B = L.B; fp.H = L.H; fp.Hkv = L.Hkv; fp.g = L.gqa_group; fp.NQT = L.NQT; fp.NKU = L.NKU;
-  fp.Nq = (int)Nq; fp.Nk = (int)Nk; fp.rq = L.rq; fp.rk = L.rk; fp.qu = L.qu; fp.ku = L.ku;
-  fp.rows = L.rows;
-  const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)d);
-  fp.scale_log2 = (float)(sc * 1.4426950408889634);
-
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return BSA_ERR_CUDA;
-  fp.sms = sms;
-  long long grid = env_ll("BSA_GRID", sms);
-  if (grid > L.rows) grid = L.rows;
-  if (grid < 1) grid = 1;
+  FwdParams fp;
+  int grid = 1;
+  st = make_fwd_params(p->L, pd, p->ws, p->dev.remap != 0, Q, K, V, pages, kv_lens, flags, O, LSE,
+                       d, scale, dev, env_ll("BSA_WATCHDOG_MS", 1000) * 1000000ll,
+                       env_ll("BSA_GRID", 0), &fp, &grid);
+  if (st != BSA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The key-norm stage resets its own status words, the row-bound stage the
   // pass counters and the forward status (the two may run on different

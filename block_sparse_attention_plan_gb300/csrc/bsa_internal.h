@@ -166,6 +166,12 @@ cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream);
 cudaError_t launch_forward(const FwdParams& p, int d, int grid, cudaStream_t stream,
                            int stages = BSA_STAGE_ALL);
 int forward_smem_bytes(int d);
+// Forward parameters and grid of one plan for the given tensors (bsa_api.cu).
+bsa_status make_fwd_params(const bsa_plan_layout& L, const PlanDev& pd, uint8_t* ws, bool remapped,
+                           const void* Q, const void* K, const void* V, const bsa_kv_pages* pages,
+                           const int32_t* kv_lens, int flags, void* O, float* LSE, int d,
+                           float scale, int dev, long long watchdog_ns, long long grid_override,
+                           FwdParams* out, int* grid_out);
 cudaError_t launch_watchdog_selftest(int32_t* status, long long limit_ns, cudaStream_t stream);
 
 }  // namespace bsa

@@ -19,7 +19,6 @@
 #include <cstring>
 #include <mutex>
 
-#include <cudaTypedefs.h>
 
 #include "bsa_internal.h"
 
@@ -49,32 +48,6 @@ bsa_status static_workspace(int dev, uint8_t** out) {
   return BSA_OK;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn_static() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
-bool encode_2d(CUtensorMap* m, const void* base, uint64_t rows, int d, int box_rows) {
-  auto fn = encode_fn_static();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1u, 1u};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -97,11 +70,10 @@ extern "C" bsa_status bsa_attention_static(const uint8_t* mask, int B, int H, in
   const long long qrows = (long long)B * H * Nq, kvrows = (long long)B * L.Hkv * Nk;
   if (qrows >= (1ll << 31) || kvrows >= (1ll << 31)) return BSA_ERR_UNSUPPORTED;
 
-  int dev = 0, maj = 0, min = 0, sms = 0;
+  int dev = 0, maj = 0, min = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return BSA_ERR_CUDA;
   if (maj != 10 || min != 3) return BSA_ERR_ARCH;
   uint8_t* ws = nullptr;
@@ -120,35 +92,10 @@ extern "C" bsa_status bsa_attention_static(const uint8_t* mask, int B, int H, in
   pd.nkeys = L.max_row_slots + 1; pd.groups = L.groups;
 
   FwdParams fp;
-  std::memset(&fp, 0, sizeof(fp));
-  if (!encode_2d(&fp.tmQ, Q, (uint64_t)qrows, d, kTile) ||
-      !encode_2d(&fp.tmQu, Q, (uint64_t)qrows, d, L.qu) ||
-      !encode_2d(&fp.tmK, K, (uint64_t)kvrows, d, L.ku) ||
-      !encode_2d(&fp.tmV, V, (uint64_t)kvrows, d, L.ku))
-    return BSA_ERR_CUDA;
-  fp.row_ptr = pd.row_ptr;
-  fp.slot_ku = pd.slot_ku;
-  fp.slot_mask = pd.slot_mask;
-  fp.order = pd.order;
-  fp.control = pd.control;
-  fp.O = static_cast<uint16_t*>(O);
-  fp.LSE = LSE;
-  fp.K = static_cast<const uint16_t*>(K);
-  const FwdScratch fs = fwd_scratch(L);
-  fp.kmax = reinterpret_cast<float*>(ws + fs.off_kmax);
-  fp.rowk = reinterpret_cast<float*>(ws + fs.off_rowk);
-  fp.fb_flag = reinterpret_cast<int32_t*>(ws + fs.off_fb_flag);
-  fp.fb_list = reinterpret_cast<int32_t*>(ws + fs.off_fb_list);
-  fp.slot_capacity = L.slot_capacity;
-  fp.watchdog_ns = 1000ll * 1000000ll;
-  fp.B = B;
-  fp.H = H; fp.Hkv = L.Hkv; fp.g = gqa_group; fp.NQT = L.NQT; fp.NKU = L.NKU;
-  fp.Nq = (int)Nq; fp.Nk = (int)Nk; fp.rq = L.rq; fp.rk = L.rk; fp.qu = L.qu; fp.ku = L.ku;
-  fp.rows = L.rows;
-  const double sc = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)d);
-  fp.scale_log2 = (float)(sc * 1.4426950408889634);
-  fp.sms = sms;
-  const int grid = sms < L.rows ? sms : L.rows;
+  int grid = 1;
+  st = make_fwd_params(L, pd, ws, false, Q, K, V, nullptr, nullptr, 0, O, LSE, d, scale, dev,
+                       1000ll * 1000000ll, 0, &fp, &grid);
+  if (st != BSA_OK) return st;
 
   // The control words (work counter, status) must start at zero on every call.
   cudaStream_t s = static_cast<cudaStream_t>(stream);
