@@ -24,11 +24,19 @@
  *                       ("CompactAttention", summary: Q-block union plus
  *                       intra-group union).
  *   bsa_forward      -- runs attention over exactly the tiles of a plan.
+ * Variants: bsa_plan_create_affine (rows given by affine descriptors instead
+ * of mask bytes), BSA_PLAN_REMAP (per-plane q-unit regrouping),
+ * bsa_forward_ex (paged K/V, key lengths, intra-block causality),
+ * bsa_forward_stage (the forward's passes one by one), bsa_attention_host
+ * (from host buffers with overlapped copies), bsa_attention_static (no
+ * allocation at all).
  *
  * Conventions
  *   - Every pointer argument named "device" is a CUDA device pointer owned by
  *     the caller; the library never allocates, frees or retains device
- *     memory.  The only host allocation is the small bsa_plan handle.
+ *     memory.  The only host allocation is the small bsa_plan handle
+ *     (bsa_attention_host also creates two streams and a few events for the
+ *     duration of the call).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls enqueue work on it and return without synchronising,
  *     except bsa_sync_status and bsa_plan_check, which synchronise it.
