@@ -48,3 +48,18 @@ def test_max_over_ranks_and_whole_job_value_two_ranks():
 def test_single_process_is_identity():
     assert bench.max_over_ranks([3.5, 1.25]) == [3.5, 1.25]
     assert bench.whole_job_tflops(1e12, 1.0, 1) == pytest.approx(1000.0)
+
+
+def test_cpu_baseline_sampler_and_config_on_cpu():
+    # The oracle leg of bench.py on the tiny workload: a positive rate over
+    # whole (b, h, q-block) samples, in a seeded order that resumes where it
+    # stopped; the config names the workload and its geometry.
+    from block_sparse_attention_plan_gb300 import workloads as W
+    w = W.make_workload("tiny")
+    rate, dt, done, nxt = bench.oracle_sample_rate(w, 0.2)
+    assert rate > 0 and dt > 0 and done > 0 and done % 8 == 0 and nxt == done
+    _, _, done2, nxt2 = bench.oracle_sample_rate(w, 0.05, start=nxt)
+    assert nxt2 == nxt + done2
+    cfg = bench._config(w, gpu=False)
+    assert cfg["workload"] == "tiny" and cfg["active_blocks"] == w.active_blocks
+    assert cfg["active_flop_per_step"] == w.active_flop
