@@ -12,7 +12,7 @@ import torch
 
 from oracle import attention as OA
 from block_sparse_attention_plan_gb300 import workloads as W
-from compare import assert_attention_close, channel_scale
+from compare import assert_attention_close
 
 pytestmark = pytest.mark.gpu
 
@@ -125,7 +125,7 @@ def test_forward_ex_argument_errors(bsa):
     VP = ctypes.c_void_p
     args = (VP(q.data_ptr()), VP(k.data_ptr()), VP(v.data_ptr()))
     outs = (VP(o.data_ptr()), VP(lse.data_ptr()), 128, 0.0, None)
-    assert lib.bsa_forward_ex(p.handle, *args, None, None, 0x2, *outs) == -1  # unknown flag
+    assert lib.bsa_forward_ex(p.handle, *args, None, None, 0x4, *outs) == -1  # unknown flag
     table = torch.zeros(w.q.shape[0], 64, dtype=torch.int32, device="cuda")
     bad = L.KVPagesC(table.data_ptr(), 64, 96, 8)  # 96 is not a multiple of the K unit 64
     assert lib.bsa_forward_ex(p.handle, *args, ctypes.byref(bad), None, 0, *outs) == -2
