@@ -255,6 +255,187 @@ def _config(w, gpu: bool = True):
     return c
 
 
+class _Case:
+    """One workload resident on the device, with the buffers and the step of
+    the hot path (plan, then forward) for it."""
+
+    def __init__(self, bsa, W, w, dev, stream, remap=False, page_size=0, causal=False,
+                 affine=False):
+        self.bsa, self.w, self.dev, self.stream = bsa, w, dev, stream
+        self.mask_d = w.mask.to(dev)
+        q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
+        self.fwd_extra = {"causal": bool(causal)}
+        if page_size:
+            # paged K/V: the sequence's pages scattered over the pools in a
+            # seeded random order, read through the block table (bsa_forward_ex)
+            ps = page_size
+            B_, Hkv_, Nk_, d_ = k.shape
+            if Nk_ % ps:
+                raise SystemExit(f"--page-size {ps} does not divide Nk = {Nk_}")
+            npg = Nk_ // ps
+            perm = torch.randperm(B_ * npg, generator=torch.Generator().manual_seed(5)).to(dev)
+
+            def to_pool(t):
+                pages = t.view(B_, Hkv_, npg, ps, d_).permute(0, 2, 1, 3, 4).reshape(B_ * npg, Hkv_, ps, d_)
+                pool = torch.empty(pages.shape, dtype=pages.dtype, device=dev)
+                pool[perm] = pages
+                return pool
+            k, v = to_pool(k), to_pool(v)
+            self.fwd_extra["block_table"] = perm.view(B_, npg).to(torch.int32).contiguous()
+        self.q, self.k, self.v = q, k, v
+        self.o = torch.empty_like(q)
+        self.lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        L = bsa.plan_layout(*w.mask.shape, w.bq, w.bk, w.gqa_group)
+        self.wsbuf = torch.empty(int(L.workspace_bytes), dtype=torch.uint8, device=dev)
+        self.plan_flags = bsa.PLAN_REMAP if remap else 0
+        self.remap_active = bool(remap and w.bq < 128 and w.gqa_group == 1 and w.Nq // 128 <= 8192)
+        self.affine = None
+        if affine:
+            # sliding, strided and dilated heads as affine row segments, the
+            # BigBird-style heads as mask rows (bsa_plan_create_affine)
+            if w.name != "regular":
+                raise SystemExit("--affine describes the regular workload's patterns")
+            segs, _ = W.regular_segments(w.Hq, w.mask.shape[3])
+            self.affine = (bsa._lib.affine_segments(segs, dev), self.mask_d)
+        self.side = torch.cuda.Stream(device=dev)
+        self.fork = torch.cuda.Event()
+        self.flush = (torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+                      if _needs_flush(w) else None)
+        self.p = None
+
+    # per step: 3 plan kernels (+1 when regrouping is active) + key norms,
+    # row bounds, bounded pass, exact pass
+    @property
+    def launches_per_step(self) -> int:
+        return 7 + int(self.remap_active)
+
+    def step(self, ev=None):
+        """A step: the plan kernels on the launching stream and, beside them on
+        a side stream, the key-norm pass (it reads only K and V); then the
+        row-bound, bounded and exact passes once both are done
+        (bsa_forward_stage).  Events: step start, plan + key norms done,
+        bounded pass start, bounded pass end, step end."""
+        bsa, w, stream = self.bsa, self.w, self.stream
+        if ev is not None:
+            ev[0].record(stream)
+        self.fork.record(stream)
+        if self.affine is not None:
+            p = bsa.plan_affine(self.affine[0], w.B, w.mask.shape[2], w.mask.shape[3], w.bq, w.bk,
+                                w.gqa_group, mask=self.affine[1], workspace=self.wsbuf,
+                                flags=self.plan_flags)
+        else:
+            p = bsa.plan(self.mask_d, w.bq, w.bk, w.gqa_group, workspace=self.wsbuf,
+                         flags=self.plan_flags)
+        self.side.wait_event(self.fork)  # starts with the plan kernels, not after them
+        args = (p, self.q, self.k, self.v)
+        kw = dict(out=self.o, lse=self.lse, **self.fwd_extra)
+        bsa.forward(*args, stages=bsa.STAGE_KNORM, stream=self.side, **kw)
+        stream.wait_stream(self.side)
+        if ev is not None:
+            ev[1].record(stream)
+        bsa.forward(*args, stages=bsa.STAGE_ROWBOUND, **kw)
+        if ev is not None:
+            ev[2].record(stream)
+        bsa.forward(*args, stages=bsa.STAGE_BOUNDED, **kw)
+        if ev is not None:
+            ev[3].record(stream)
+        bsa.forward(*args, stages=bsa.STAGE_EXACT, **kw)
+        if ev is not None:
+            ev[4].record(stream)
+        self.p = p
+        return p
+
+    def check(self, when):
+        st, det = self.bsa.sync_status(self.p)
+        if st != 0:
+            raise RuntimeError(f"{self.w.name}: device status {st} detail {det:#x} {when}")
+
+    def warm(self, n):
+        for _ in range(n):
+            self.step()
+        torch.cuda.synchronize()
+        self.check("during warm-up")
+
+    def timed(self, steps, barrier=lambda: None):
+        """Time `steps` steps; returns (per-step events, wall t0, wall t1)."""
+        fev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(5)) for _ in range(steps)]
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        for i in range(steps):
+            if self.flush is not None:
+                self.flush.fill_(i & 0xff)
+            self.step(fev[i])
+        torch.cuda.synchronize()
+        t1 = time.time()
+        barrier()
+        self.check("in the timed region")
+        return fev, t0, t1
+
+    def plan_stats(self):
+        """Plan totals: algorithmic plan bytes, computed FLOP (every slot
+        computes 128 query rows x 128 keys) and computed / selected."""
+        w = self.w
+        tot = self.p.arrays()["totals"]
+        S_, U_ = int(tot[0]), int(tot[2])
+        Lp = self.p.layout
+        plan_bytes = (w.mask.numel() + 4 * (Lp.rows + 1) + 4 * S_ * Lp.rk + 4 * S_ + 4 * Lp.rows
+                      + 4 * (Lp.urows + 1) + 4 * U_)
+        computed = 4.0 * 128 * 128 * w.d * S_
+        return plan_bytes, computed, computed / w.active_flop
+
+    def free(self):
+        for n in ("q", "k", "v", "o", "lse", "wsbuf", "mask_d", "flush", "p", "affine"):
+            setattr(self, n, None)
+
+
+def _times(fev):
+    ms = float(np.mean([e[0].elapsed_time(e[4]) for e in fev]))
+    fwd_ms = float(np.mean([e[1].elapsed_time(e[4]) for e in fev]))
+    plan_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in fev]))
+    bounded_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in fev]))
+    return ms, fwd_ms, plan_ms, bounded_ms
+
+
+# GB300 nominal dense bf16 tensor throughput per GPU (datasheet figure without
+# 2:4 sparsity), reported beside the measured peak.
+NOMINAL_BF16_TFLOPS = 2250.0
+PER_CONFIG = ("long_video_dit", "chunked_prefill", "regular", "tiny")
+
+
+def per_config_entry(bsa, W, name, dev, stream, clocks, peak, target_s=0.5):
+    """Measure one more workload in this process: the same step, timed over
+    enough steps for about `target_s` seconds (20 .. 2000 steps)."""
+    w = W.make_workload(name)
+    remap = w.bq < 128 and w.gqa_group == 1
+    c = _Case(bsa, W, w, dev, stream, remap=remap)
+    c.warm(3)
+    t0 = time.perf_counter()
+    for _ in range(3):
+        c.step()
+    torch.cuda.synchronize()
+    est = (time.perf_counter() - t0) / 3
+    steps = int(min(2000, max(20, math.ceil(target_s / max(est, 1e-6)))))
+    fev, w0, w1 = c.timed(steps)
+    ms, fwd_ms, plan_ms, bounded_ms = _times(fev)
+    _, computed, ratio = c.plan_stats()
+    flop = w.active_flop
+    kern = flop / (bounded_ms * 1e-3) / 1e12
+    e = {"workload": name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+         "bq": w.bq, "bk": w.bk, "density": round(w.density, 4), "active_flop": flop,
+         "computed_over_selected": ratio, "plan_flags": "BSA_PLAN_REMAP" if c.remap_active else 0,
+         "steps": steps, "step_ms": ms, "value": flop / (ms * 1e-3) / 1e12,
+         "kernel": "bsa_fwd_kernel<%d, bounded>" % w.d, "kernel_ms": bounded_ms,
+         "roofline": {"achieved": kern, "peak": peak, "frac": kern / peak,
+                      "frac_of_nominal": kern / NOMINAL_BF16_TFLOPS},
+         "forward_ms": fwd_ms, "plan_ms": plan_ms,
+         "clocks": clocks.summary(w0, w1)}
+    c.free()
+    del c, w
+    torch.cuda.empty_cache()
+    return e
+
+
 def run_gb300(args):
     ws, rank, local = _dist()
     import block_sparse_attention_plan_gb300 as bsa
@@ -284,75 +465,9 @@ def run_gb300(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
 
-    mask_d = w.mask.to(dev)
-    q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
-    fwd_extra = {"causal": bool(args.causal)}
-    if args.page_size:
-        # paged K/V: the sequence's pages scattered over the pools in a seeded
-        # random order, read through the block table (bsa_forward_ex)
-        ps = args.page_size
-        B_, Hkv_, Nk_, d_ = k.shape
-        if Nk_ % ps:
-            raise SystemExit(f"--page-size {ps} does not divide Nk = {Nk_}")
-        npg = Nk_ // ps
-        perm = torch.randperm(B_ * npg, generator=torch.Generator().manual_seed(5)).to(dev)
-
-        def to_pool(t):
-            pages = t.view(B_, Hkv_, npg, ps, d_).permute(0, 2, 1, 3, 4).reshape(B_ * npg, Hkv_, ps, d_)
-            pool = torch.empty(pages.shape, dtype=pages.dtype, device=dev)
-            pool[perm] = pages
-            return pool
-        k, v = to_pool(k), to_pool(v)
-        fwd_extra["block_table"] = perm.view(B_, npg).to(torch.int32).contiguous()
-    o = torch.empty_like(q)
-    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
-    L = bsa.plan_layout(*w.mask.shape, w.bq, w.bk, w.gqa_group)
-    wsbuf = torch.empty(int(L.workspace_bytes), dtype=torch.uint8, device=dev)
+    c = _Case(bsa, W, w, dev, stream, remap=args.remap, page_size=args.page_size,
+              causal=args.causal, affine=args.affine)
     flop = w.active_flop
-
-    plan_flags = bsa.PLAN_REMAP if args.remap else 0
-    remap_active = bool(args.remap and w.bq < 128 and w.gqa_group == 1 and w.Nq // 128 <= 8192)
-    affine = None
-    if args.affine:
-        # sliding, strided and dilated heads as affine row segments, the
-        # BigBird-style heads as mask rows (bsa_plan_create_affine)
-        if w.name != "regular":
-            raise SystemExit("--affine describes the regular workload's patterns")
-        segs, _ = W.regular_segments(w.Hq, w.mask.shape[3])
-        affine = (bsa._lib.affine_segments(segs, dev), mask_d)  # only BigBird heads' rows are read
-
-    # A step: the plan kernels on the launching stream and, beside them on a
-    # side stream, the key-norm pass (it reads only K); then the row-bound,
-    # bounded and exact passes once both are done (bsa_forward_stage).
-    # Events of a timed step: step start, plan + key norms done, bounded pass
-    # start, bounded pass end, step end.
-    side = torch.cuda.Stream(device=dev)
-    fork = torch.cuda.Event()
-
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        fork.record(stream)
-        if affine is not None:
-            p = bsa.plan_affine(affine[0], w.B, w.mask.shape[2], w.mask.shape[3], w.bq, w.bk,
-                                w.gqa_group, mask=affine[1], workspace=wsbuf, flags=plan_flags)
-        else:
-            p = bsa.plan(mask_d, w.bq, w.bk, w.gqa_group, workspace=wsbuf, flags=plan_flags)
-        side.wait_event(fork)  # starts with the plan kernels, not after them
-        bsa.forward(p, q, k, v, out=o, lse=lse, stages=bsa.STAGE_KNORM, stream=side, **fwd_extra)
-        stream.wait_stream(side)
-        if ev is not None:
-            ev[1].record(stream)
-        bsa.forward(p, q, k, v, out=o, lse=lse, stages=bsa.STAGE_ROWBOUND, **fwd_extra)
-        if ev is not None:
-            ev[2].record(stream)
-        bsa.forward(p, q, k, v, out=o, lse=lse, stages=bsa.STAGE_BOUNDED, **fwd_extra)
-        if ev is not None:
-            ev[3].record(stream)
-        bsa.forward(p, q, k, v, out=o, lse=lse, stages=bsa.STAGE_EXACT, **fwd_extra)
-        if ev is not None:
-            ev[4].record(stream)
-        return p
 
     def barrier():
         if dist:
@@ -365,44 +480,15 @@ def run_gb300(args):
         uuid = str(local)
     clocks = ClockSampler(uuid)
 
-    p = None
-    for _ in range(args.warmup):
-        p = step()
-    torch.cuda.synchronize()
-    if p is not None:
-        st, det = bsa.sync_status(p)
-        if st != 0:
-            raise RuntimeError(f"device status {st} detail {det:#x} during warm-up")
-
-    fev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(5)) for _ in range(args.steps)]
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if _needs_flush(w) else None
-    barrier()
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
-    for i in range(args.steps):
-        if flush is not None:
-            flush.fill_(i & 0xff)
-        p = step(fev[i])
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    barrier()
-    st, det = bsa.sync_status(p)
-    if st != 0:
-        raise RuntimeError(f"device status {st} detail {det:#x} in the timed region")
-    # plan bytes (algorithmic): the mask read once (none for affine heads'
-    # rows, counted anyway), the plan arrays written once
-    tot = p.arrays()["totals"]
-    S_, U_ = int(tot[0]), int(tot[2])
-    R_ = p.layout.rows
-    plan_bytes = (w.mask.numel() + 4 * (R_ + 1) + 4 * S_ * p.layout.rk + 4 * S_ + 4 * R_
-                  + 4 * (p.layout.urows + 1) + 4 * U_)
+    c.warm(args.warmup)
+    fev, t_wall0, t_wall1 = c.timed(args.steps, barrier)
+    plan_bytes, computed, ratio = c.plan_stats()
     # a step = plan start -> forward end, timed with events on the launching stream
-    ms = float(np.mean([e[0].elapsed_time(e[4]) for e in fev]))
-    fwd_ms = float(np.mean([e[1].elapsed_time(e[4]) for e in fev]))
-    plan_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in fev]))
-    bounded_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in fev]))
+    ms, fwd_ms, plan_ms, bounded_ms = _times(fev)
     ms, fwd_ms, bounded_ms = max_over_ranks([ms, fwd_ms, bounded_ms], dev)
     clk = clocks.summary(t_wall0, t_wall1)
+    launches = c.launches_per_step * args.steps
+    c.free()
 
     # end to end through the public API, host (pinned) buffers, copies timed
     mask_h = w.mask.pin_memory()
@@ -419,14 +505,23 @@ def run_gb300(args):
     torch.cuda.synchronize()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
     (e2e_ms,) = max_over_ranks([e2e_ms], dev)
-    clocks.stop()
     h2d = mask_h.numel() + (q_h.numel() + k_h.numel() + v_h.numel()) * 2
     d2h = oh.numel() * 2 + lh.numel() * 4
+    del mask_h, q_h, k_h, v_h, o_pin, l_pin, oh, lh
+    bsa._lib._host_buffers.clear()
+    torch.cuda.empty_cache()
+
+    per_config = None
+    if rank == 0 and ws == 1 and not args.no_per_config:
+        per_config = [per_config_entry(bsa, W, name, dev, stream, clocks, peak)
+                      for name in PER_CONFIG if name != w.name]
+    clocks.stop()
 
     value = whole_job_tflops(flop, ms, ws)
     achieved = flop / (bounded_ms * 1e-3) / 1e12      # the dominant kernel's launch
     achieved_fwd = flop / (fwd_ms * 1e-3) / 1e12      # the whole bsa_forward
     cfg = _config(w)
+    cfg["computed_over_selected"] = ratio
     if args.page_size:
         cfg["kv_pages"] = (f"page_size {args.page_size}, pages shuffled across the pool, read "
                            "through a block table (e2e stays on contiguous host buffers)")
@@ -443,6 +538,7 @@ def run_gb300(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
         "pct_of_peak": 100.0 * value / ws / peak,
+        "pct_of_nominal_peak": 100.0 * value / ws / NOMINAL_BF16_TFLOPS,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
                      "traffic": (args.traffic if args.traffic is not None else
@@ -455,7 +551,9 @@ def run_gb300(args):
                      "kernel": "bsa_fwd_kernel<%d, bounded>" % w.d, "kernel_ms": bounded_ms,
                      "forward_ms": fwd_ms, "forward_achieved": achieved_fwd,
                      "forward_frac": achieved_fwd / peak, "peak_source": f"{peak_src} bf16 burst",
-                     "frac_of_sustained": achieved / peak_sus},
+                     "frac_of_sustained": achieved / peak_sus,
+                     "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS,
+                     "nominal_peak": NOMINAL_BF16_TFLOPS},
         "e2e": {"value": whole_job_tflops(flop, e2e_ms, ws), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
         "plan_ms": plan_ms,
@@ -464,13 +562,13 @@ def run_gb300(args):
                  "frac_of_hbm": plan_bytes / (plan_ms * 1e-3) / 1e9 / _hbm_gbs(),
                  "note": "ms: step start until the plan kernels and the key-norm pass, run side by "
                          "side, are both done; the plan kernels are latency-bound at these sizes"},
-        # per step: 3 plan kernels (+1 when regrouping is active) + key norms,
-        # row bounds, bounded pass, exact pass
-        "gpu_launches": (7 + int(remap_active)) * args.steps,
+        "gpu_launches": launches,
         "clocks": clk,
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    if per_config is not None:
+        line["per_config"] = per_config
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -496,6 +594,8 @@ def main():
                     help="regular workload: plan from affine row segments (+ residual mask bytes)")
     ap.add_argument("--causal", action="store_true",
                     help="intra-block causal masking (queries are the last Nq positions)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config record of the other workloads")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per forward launch from an ncu capture of this kernel")
     args = ap.parse_args()

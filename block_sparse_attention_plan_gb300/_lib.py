@@ -4,7 +4,6 @@ supplies device memory and streams."""
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 from typing import Optional, Tuple
 
@@ -23,6 +22,7 @@ PLAN_REMAP = 0x2
 STAGE_PREPARE, STAGE_BOUNDED, STAGE_EXACT, STAGE_ALL = 0x1, 0x2, 0x4, 0x7
 STAGE_KNORM, STAGE_ROWBOUND = 0x8, 0x10
 FWD_CAUSAL = 0x1
+FWD_SPLIT_P = 0x2
 
 
 class KVPagesC(ctypes.Structure):
@@ -94,6 +94,8 @@ def library() -> ctypes.CDLL:
     lib.bsa_watchdog_selftest.argtypes = [VP, I, VP]
     lib.bsa_attention_static.restype = I
     lib.bsa_attention_static.argtypes = [U8P, I, I, I, I, I, I, I, VP, VP, VP, VP, VP, I, F, VP]
+    lib.bsa_attention_static_status.restype = I
+    lib.bsa_attention_static_status.argtypes = [VP, ctypes.POINTER(ctypes.c_int32)]
     lib.bsa_plan_create_affine.restype = I
     lib.bsa_plan_create_affine.argtypes = [U8P, VP, VP, I, I, I, I, I, I, I, I, VP, ctypes.c_size_t,
                                            I, VP, ctypes.POINTER(P)]
@@ -245,13 +247,15 @@ def forward(p: Plan, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
             stream: Optional[torch.cuda.Stream] = None,
             block_table: Optional[torch.Tensor] = None,
             kv_lens: Optional[torch.Tensor] = None,
-            causal: bool = False, stages: Optional[int] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+            causal: bool = False, stages: Optional[int] = None,
+            split: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
     """Block-sparse attention over plan ``p``.  Returns (O, LSE).
 
     Contiguous K/V: k, v [B, Hkv, Nk, d].  Paged K/V (``block_table`` given,
     int32 CUDA [B, max_pages]): k, v are pools [num_pages, Hkv, page_size, d].
     ``kv_lens`` (int32 CUDA [B]) and ``causal`` mask keys inside the selected
-    blocks (bsa_forward_ex).  ``stages`` (STAGE_* bits) enqueues only those
+    blocks (bsa_forward_ex); ``split`` applies every row's weights as two bf16
+    terms (BSA_FWD_SPLIT_P).  ``stages`` (STAGE_* bits) enqueues only those
     stages of the forward (bsa_forward_stage); O and LSE are complete once
     all three have run, in order."""
     L = p.layout
@@ -282,14 +286,15 @@ def forward(p: Plan, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     if lse is None:
         lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device)
     sc = 0.0 if scale is None else float(scale)
+    flags = (FWD_CAUSAL if causal else 0) | (FWD_SPLIT_P if split else 0)
     if stages is not None:
         _check(library().bsa_forward_stage(
             p.handle, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
             ctypes.c_void_p(v.data_ptr()), ctypes.byref(pages) if pages is not None else None,
             ctypes.c_void_p(kv_lens.data_ptr()) if kv_lens is not None else None,
-            FWD_CAUSAL if causal else 0, ctypes.c_void_p(out.data_ptr()),
+            flags, ctypes.c_void_p(out.data_ptr()),
             ctypes.c_void_p(lse.data_ptr()), d, sc, int(stages), _stream_ptr(stream)), "bsa_forward_stage")
-    elif pages is None and kv_lens is None and not causal:
+    elif pages is None and kv_lens is None and flags == 0:
         _check(library().bsa_forward(
             p.handle, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
             ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
@@ -299,7 +304,7 @@ def forward(p: Plan, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
             p.handle, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
             ctypes.c_void_p(v.data_ptr()), ctypes.byref(pages) if pages is not None else None,
             ctypes.c_void_p(kv_lens.data_ptr()) if kv_lens is not None else None,
-            FWD_CAUSAL if causal else 0, ctypes.c_void_p(out.data_ptr()),
+            flags, ctypes.c_void_p(out.data_ptr()),
             ctypes.c_void_p(lse.data_ptr()), d, sc, _stream_ptr(stream)), "bsa_forward_ex")
     return out, lse
 
@@ -394,5 +399,10 @@ def attention_static(mask: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: to
     return out, lse
 
 
-def default_scale(d: int) -> float:
-    return 1.0 / math.sqrt(d)
+def attention_static_status(stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, int]:
+    """(status, detail) the kernels of the last attention_static call on the
+    current device recorded (bsa_attention_static_status; synchronises)."""
+    det = ctypes.c_int32(0)
+    st = library().bsa_attention_static_status(_stream_ptr(stream), ctypes.byref(det))
+    return st, det.value
+

@@ -184,9 +184,13 @@ bsa_status make_fwd_params(const bsa_plan_layout& L, const PlanDev& pd, uint8_t*
   fp.O = static_cast<uint16_t*>(O);
   fp.LSE = LSE;
   fp.K = static_cast<const uint16_t*>(K);
+  fp.V = static_cast<const uint16_t*>(V);
   const FwdScratch fs = fwd_scratch(L);
   fp.kmax = reinterpret_cast<float*>(ws + fs.off_kmax);
   fp.rowk = reinterpret_cast<float*>(ws + fs.off_rowk);
+  fp.vmax = reinterpret_cast<float*>(ws + fs.off_vmax);
+  fp.rowv = reinterpret_cast<float*>(ws + fs.off_rowv);
+  fp.split_all = (flags & BSA_FWD_SPLIT_P) ? 1 : 0;
   fp.fb_flag = reinterpret_cast<int32_t*>(ws + fs.off_fb_flag);
   fp.fb_list = reinterpret_cast<int32_t*>(ws + fs.off_fb_list);
   fp.sigma = remapped ? reinterpret_cast<const int32_t*>(ws + L.off_sigma) : nullptr;
@@ -364,7 +368,7 @@ bsa_status bsa_forward_stage(const bsa_plan* plan, const void* Q, const void* K,
   if (!plan) return BSA_ERR_INVALID_ARG;
   if (!p) return BSA_ERR_PLAN_MISMATCH;
   if (!Q || !K || !V || !O || !LSE) return BSA_ERR_INVALID_ARG;
-  if (flags & ~BSA_FWD_CAUSAL) return BSA_ERR_INVALID_ARG;
+  if (flags & ~(BSA_FWD_CAUSAL | BSA_FWD_SPLIT_P)) return BSA_ERR_INVALID_ARG;
   if (kv_lens && (reinterpret_cast<uintptr_t>(kv_lens) & 3u)) return BSA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
     return BSA_ERR_INVALID_ARG;

@@ -9,8 +9,9 @@
 // softmax), with a reading of its reference maximum described below.
 //
 // Passes of one forward (bsa_forward_stage can enqueue them separately):
-//   key-norm pass   the largest |k| of every K unit (reads K once);
-//   row-bound pass  per plan row, the largest of those over its units (and,
+//   key-norm pass   the largest |k| and the largest |v| element of every K/V
+//                   unit (reads K and V once);
+//   row-bound pass  per plan row, the largest of each over its units (and,
 //                   for paged K/V, each slot position's pool row);
 //   bounded pass    this kernel over every plan row with the row's reference
 //                   maximum m = |q| max|k| scale log2(e): no score exceeds
@@ -29,19 +30,34 @@
 //            memory, result in tensor memory) for every slot, up to two slots
 //            ahead of the softmax (S is double-buffered);
 //   warp 2   owns the tensor-memory allocation (512 columns); one thread
-//            issues O += P V with P read from tensor memory.  Two issuing
-//            threads in different warps keep the tensor pipe fed while either
-//            one waits on a barrier or is slowed by the softmax warps sharing
-//            its scheduler;
+//            issues O += P V with P read from tensor memory, then hands the
+//            slot's buffer back to the S issuer.  Two issuing threads in
+//            different warps keep the tensor pipe fed while either one waits
+//            on a barrier or is slowed by the softmax warps sharing its
+//            scheduler;
 //   warps 4-11 the softmax: each row of a slot is shared by two threads, one
 //            in warps 4-7 (keys 0-63 of the slot) and one in warps 8-11 (keys
 //            64-127); they combine their row sums at the row's end (and, in
 //            the exact pass, their maxima while it runs).
 //
 // Tensor memory (512 x 32-bit columns x 128 lanes; lane = q-tile row):
-//   [0,128) S buffer 0   [128,256) S buffer 1   [256,256+d) O
-//   [384,448) P buffer 0 [448,512) P buffer 1   (P: bf16 pairs, keys 2c, 2c+1
-//   in column c).  Slot g of the CTA uses S and P buffer g mod 2.
+//   [0,128) [128,256) [256,384) slot buffers 0-2, [384,384+d) O.  Slot g of
+//   the CTA uses buffer g mod 3: the S issuer writes S there (fp32, key c in
+//   column c); the softmax thread of key half h loads columns [64h, 64h+64),
+//   then writes P over the first half of what it loaded: bf16 pairs (keys
+//   64h+2c, 64h+2c+1 in column 64h+c, c < 32) and, for rows computed with
+//   split weights, the low-order bf16 terms in columns [64h+32, 64h+64).
+//   Each thread only rewrites columns it has itself loaded, so no thread
+//   overwrites a score another one has yet to read.  The buffer is free again
+//   once that slot's P V has completed.
+//
+// Split weights.  P V on the tensor cores applies P rounded to bf16, i.e.
+// each weight with a relative error of up to 2^-8, which moves O by up to
+// 2^-8 times the spread of the V values the row attends.  For rows whose K/V
+// units hold a value with |v| > kSplitV (and for every row with
+// BSA_FWD_SPLIT_P) each weight p is applied as hi + lo, hi = bf16(p) and
+// lo = bf16(p - hi), with a second P V product for lo: the weights are then
+// exact to about 2^-16, and O is normalised by the fp32 sum of the weights.
 //
 // Every wait is bounded (watchdog): on expiry the CTA records
 // BSA_ERR_TIMEOUT in the plan's status word, lets its in-flight copies and
@@ -65,9 +81,14 @@ constexpr int kTmemCols = 512;
 constexpr int kRegsControl = 72;
 constexpr int kRegsSoftmax = 208;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split");
-constexpr uint32_t kColS = 0;    // S buffer b at kColS + 128 b
-constexpr uint32_t kColO = 256;  // O accumulator, d columns
-constexpr uint32_t kColP = 384;  // P buffer b at kColP + 64 b
+constexpr int kSlotBufs = 3;     // slot buffers (S, then P) in tensor memory
+constexpr uint32_t kColS = 0;    // slot buffer b at kColS + 128 b
+constexpr uint32_t kColO = 384;  // O accumulator, d columns
+// Rows whose K/V units hold a value of magnitude above this apply split
+// weights (hi + lo).  Values of N(0,1) inputs stay below it (their largest
+// magnitude over millions of draws is about 5.5), where the error of bf16
+// weights stays a few thousandths of the output scale.
+constexpr float kSplitV = 8.0f;
 // Lazy rescale: O and the row sums keep the reference maximum m of the row
 // until some score exceeds it by more than kRescaleThreshold (log2 units),
 // so weights stay <= 2^16 (bf16 and fp32 hold them exactly as well as 1).
@@ -105,11 +126,10 @@ struct Cfg {
   static constexpr int kBarKEmpty = kBarKFull + kStagesK;
   static constexpr int kBarVFull = kBarKEmpty + kStagesK;
   static constexpr int kBarVEmpty = kBarVFull + kStagesV;
-  static constexpr int kBarSFull = kBarVEmpty + kStagesV;   // [2]
-  static constexpr int kBarSFree = kBarSFull + 2;           // [2]
-  static constexpr int kBarPFull = kBarSFree + 2;           // [2]
-  static constexpr int kBarPFree = kBarPFull + 2;           // [2]
-  static constexpr int kBarOFull = kBarPFree + 2;
+  static constexpr int kBarSFull = kBarVEmpty + kStagesV;   // [3] S of the slot in buffer b
+  static constexpr int kBarSFree = kBarSFull + kSlotBufs;   // [3] P V of the slot done: buffer b free
+  static constexpr int kBarPFull = kBarSFree + kSlotBufs;   // [3] P of the slot in buffer b
+  static constexpr int kBarOFull = kBarPFull + kSlotBufs;
   static constexpr int kBarOFree = kBarOFull + 1;
   static constexpr int kBarXchg = kBarOFree + 1;            // [4 lane quadrants][2 parities]
   static constexpr int kBarDrain = kBarXchg + 8;
@@ -140,6 +160,20 @@ struct Item {
   int row;     // plan row
   int it;      // schedule position; < 0: no more work (-2: a wait gave up)
   float kb;    // largest key norm over the row's K units
+  bool split;  // apply the row's weights as hi + lo bf16 terms
+};
+
+// Slot-buffer cursor: buffer b = g mod 3 of the CTA's g-th slot and its use
+// count u = g / 3 (the phase of that buffer's barriers).  Every role advances
+// its own cursor once per slot, in the same order.
+struct SlotBuf {
+  uint32_t b = 0, u = 0;
+  __device__ __forceinline__ void next() {
+    if (++b == (uint32_t)kSlotBufs) {
+      b = 0;
+      ++u;
+    }
+  }
 };
 
 __device__ __forceinline__ void record_status(int32_t* ctl, int code, int site) {
@@ -150,7 +184,7 @@ __device__ __forceinline__ void record_status(int32_t* ctl, int code, int site) 
 // Decode one schedule entry, rejecting out-of-range plan data (the row is then
 // treated as empty and BSA_ERR_PLAN_MISMATCH is recorded).
 __device__ __forceinline__ Item load_item(const FwdParams& p, int it, bool report) {
-  Item m{0, 0, 0, 0, 1, 0, false, 0, it, 0.f};
+  Item m{0, 0, 0, 0, 1, 0, false, 0, it, 0.f, false};
   const int row = __ldg(p.order + it);
   if (row < 0 || row >= p.rows) {
     if (report) record_status(p.control, -7, kSitePlanRange);
@@ -204,7 +238,7 @@ __device__ __forceinline__ void sched_publish(uint8_t* smem, int slot, const Ite
   e[1] = m.n;
   e[2] = m.s0;
   e[3] = m.bh;
-  e[4] = (m.qx << 5) | m.qs;
+  e[4] = (m.qx << 6) | (m.split ? 32 : 0) | m.qs;
   e[5] = m.kvrow0;
   e[6] = m.valid ? m.row : -1;
   e[7] = __float_as_int(m.kb);
@@ -216,7 +250,7 @@ template <int D>
 __device__ __forceinline__ Item sched_take(const Smem<D>& sm, const uint8_t* smem, uint32_t t,
                                            bool lane_arrives, bool warp_sync, const Watchdog& wd) {
   using C = Cfg<D>;
-  Item m{0, 0, 0, 0, 1, 0, false, 0, -2, 0.f};
+  Item m{0, 0, 0, 0, 1, 0, false, 0, -2, 0.f, false};
   const int slot = (int)(t % kSchedSlots);
   bool ok = mbar_wait(sm.bar(C::kBarSchedFull + slot), (t / kSchedSlots) & 1u, wd, kSiteSched);
   if (warp_sync) ok = __all_sync(0xffffffffu, ok);
@@ -226,7 +260,8 @@ __device__ __forceinline__ Item sched_take(const Smem<D>& sm, const uint8_t* sme
   m.n = e[1];
   m.s0 = e[2];
   m.bh = e[3];
-  m.qx = e[4] >> 5;
+  m.qx = e[4] >> 6;
+  m.split = (e[4] & 32) != 0;
   m.qs = e[4] & 31;
   m.kvrow0 = e[5];
   const int row = e[6];
@@ -342,9 +377,12 @@ __device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, co
       if (it >= nwork) it = -1;
       if (it >= 0) {
         m = load_item(p, it, true);
-        if (m.n > 0) m.kb = __ldg(p.rowk + m.row);
+        if (m.n > 0) {
+          m.kb = __ldg(p.rowk + m.row);
+          m.split = p.split_all || __ldg(p.rowv + m.row) > kSplitV;
+        }
       } else {
-        m = Item{0, 0, 0, 0, 1, 0, false, 0, -1, 0.f};
+        m = Item{0, 0, 0, 0, 1, 0, false, 0, -1, 0.f, false};
       }
       sched_publish<D>(smem, slot, m);
       mbar_arrive(sm.bar(C::kBarSchedFull + slot));
@@ -410,20 +448,19 @@ struct MmaState {
   uint64_t vdesc0;    // MN-major SW128 descriptor of V stage 0 (LBO = next 64 columns)
   uint32_t kc = 0;    // K tiles consumed
   uint32_t vc = 0;    // V tiles consumed
-  uint32_t sg = 0;    // S tiles issued (slot g of the CTA uses S/P buffer g mod 2)
-  uint32_t pg = 0;    // P V products issued
+  SlotBuf sb;         // slot buffer of the next S tile (S issuer) or P V product (P V issuer)
   static constexpr uint64_t kStageStep = (uint64_t)(C::kTileBytes >> 4);
 };
 
-// S = Q K^T into S buffer sg mod 2 (M=128, N=128, K=16 per instruction, d/16
-// instructions), once the softmax has read that buffer's previous tile.
+// S = Q K^T into the slot's buffer (M=128, N=128, K=16 per instruction, d/16
+// instructions), once the P V of that buffer's previous slot has completed.
 template <int D>
 __device__ __forceinline__ bool issue_s(const Smem<D>& sm, MmaState<D>& st, uint32_t tmem, int qb,
                                         const Watchdog& wd) {
   using C = Cfg<D>;
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
-  const int b = (int)(st.sg & 1u);
-  const uint32_t u = st.sg >> 1;
+  const int b = (int)st.sb.b;
+  const uint32_t u = st.sb.u;
   if (u > 0 && !mbar_wait(sm.bar(C::kBarSFree + b), (u - 1) & 1u, wd, kSiteSFull)) return false;
   const uint32_t stage = st.kc % (uint32_t)C::kStagesK;
   if (!mbar_wait(sm.bar(C::kBarKFull + (int)stage), (st.kc / C::kStagesK) & 1u, wd, kSiteKvFull))
@@ -439,27 +476,35 @@ __device__ __forceinline__ bool issue_s(const Smem<D>& sm, MmaState<D>& st, uint
   mma_commit(sm.bar(C::kBarKEmpty + (int)stage));
   mma_commit(sm.bar(C::kBarSFull + b));
   ++st.kc;
-  ++st.sg;
+  st.sb.next();
   return true;
 }
 
 // O (+)= P V: M=128, N=d, K=16 keys per instruction, 8 instructions; P from
-// tensor memory (columns [8kk, 8kk+8) hold keys [16kk, 16kk+16)), V rows
-// [16kk, 16kk+16) start 2048 bytes apart.
+// the slot's buffer in tensor memory (keys [16kk, 16kk+16) in columns
+// 64(kk/4) + 8(kk%4) .. +8), V rows [16kk, 16kk+16) start 2048 bytes apart.
+// Split weights: 8 more instructions with the low-order terms (32 columns
+// further on) against the same V rows.
 template <int D>
 __device__ __forceinline__ void issue_pv(MmaState<D>& st, uint32_t tmem, uint32_t stage,
-                                         bool accumulate) {
+                                         bool accumulate, bool split) {
   constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
-  const uint32_t pcol = tmem + kColP + 64u * (st.pg & 1u);
+  const uint32_t pcol = tmem + kColS + 128u * st.sb.b;
   const uint64_t vd = st.vdesc0 + (uint64_t)stage * MmaState<D>::kStageStep;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
-    mma_ts(tmem + kColO, pcol + 8u * (uint32_t)kk, vd + (uint64_t)(kk * (2048 >> 4)), kIdescPV,
-           (accumulate || kk > 0) ? 1u : 0u);
+    mma_ts(tmem + kColO, pcol + 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3),
+           vd + (uint64_t)(kk * (2048 >> 4)), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+  if (split) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      mma_ts(tmem + kColO, pcol + 32u + 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3),
+             vd + (uint64_t)(kk * (2048 >> 4)), kIdescPV, 1u);
+  }
 }
 
-// S issuer: S of every slot, in slot order, as soon as its S buffer has been
-// read out by the softmax (two slots back) and its K tile has landed.
+// S issuer: S of every slot, in slot order, as soon as its buffer is free (the
+// P V of the slot three back has completed) and its K tile has landed.
 template <int D>
 __device__ __noinline__ void s_issuer_role(const FwdParams& p, const uint8_t* smem, const Smem<D> sm,
                                            uint32_t tmem, const Watchdog wd) {
@@ -487,7 +532,7 @@ __device__ __noinline__ void s_issuer_role(const FwdParams& p, const uint8_t* sm
 
 // P V issuer: O (+)= P V of every slot once its P is in tensor memory and its
 // V tile has landed; the first of a row also waits until the previous row's
-// epilogue has read O out.  Runs in its own warp so that its waits and
+// epilogue has read O out.  Its completion frees the slot's buffer.  Runs in its own warp so that its waits and
 // commits never leave the tensor pipe without queued S work.
 template <int D>
 __device__ __noinline__ void pv_issuer_role(const FwdParams& p, const uint8_t* smem, const Smem<D> sm,
@@ -503,8 +548,8 @@ __device__ __noinline__ void pv_issuer_role(const FwdParams& p, const uint8_t* s
     const int n = m.n;
     if (n == 0) continue;
     for (int j = 0; j < n && ok; ++j) {
-      const int b = (int)(st.pg & 1u);
-      if (!mbar_wait(sm.bar(C::kBarPFull + b), (st.pg >> 1) & 1u, wd, kSitePFull)) {
+      const int b = (int)st.sb.b;
+      if (!mbar_wait(sm.bar(C::kBarPFull + b), st.sb.u & 1u, wd, kSitePFull)) {
         ok = false;
         break;
       }
@@ -520,12 +565,12 @@ __device__ __noinline__ void pv_issuer_role(const FwdParams& p, const uint8_t* s
         break;
       }
       tc_fence_after();
-      issue_pv<D>(st, tmem, stage, j > 0);
+      issue_pv<D>(st, tmem, stage, j > 0, m.split);
       mma_commit(sm.bar(C::kBarVEmpty + (int)stage));
-      mma_commit(sm.bar(C::kBarPFree + b));
+      mma_commit(sm.bar(C::kBarSFree + b));  // the slot's buffer may take the next S
       if (j == n - 1) mma_commit(sm.bar(C::kBarOFull));
       ++st.vc;
-      ++st.pg;
+      st.sb.next();
     }
     ++rows;
   }
@@ -559,7 +604,8 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   const float sl2 = p.scale_log2;
   const uint64_t sl2x2 = f2_make(sl2, sl2);
   float* xbuf = reinterpret_cast<float*>(smem + C::kOffX);
-  uint32_t sg = 0, rows = 0, xc = 0, q_it = 0;
+  SlotBuf sb;  // the buffer of this CTA's next slot
+  uint32_t rows = 0, xc = 0, q_it = 0;
   uint32_t bits = 0xffffffffu;  // this row's sub-mask bits for the current slot
   // Element mask (causal / key lengths): key position of the first key of each
   // of this thread's two 32-key chunks of the current slot (-1: padding), the
@@ -675,6 +721,65 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     f2_split(acc2[1], s2, s3);
     return (s0 + s1) + (s2 + s3);
   };
+  // Split weights: pk gets hi = bf16(p), lo gets bf16(p - hi) (p - hi is
+  // exact in fp32: hi is within a factor of two of p).  The weights applied,
+  // hi + lo, are within 2^-16 of p, so the fp32 sum of p normalises them.
+  auto exp_pack_split = [&](const uint32_t (&v)[64], uint32_t (&pk)[32], uint32_t (&lo)[32],
+                            float m) -> float {
+    const float mb = (m == -INFINITY) ? 0.f : m;
+    const uint64_t nmbx2 = f2_make(-mb, -mb);
+    const uint64_t neg1x2 = f2_make(-1.f, -1.f);
+    uint64_t acc2[2] = {0ull, 0ull};
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      if (chunks & (1u << c)) {
+#pragma unroll
+        for (int e = 16 * c; e < 16 * c + 16; ++e) {
+          float x0, x1;
+          f2_split(ffma2(f2_make(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sl2x2, nmbx2),
+                   x0, x1);
+          const uint64_t p2 = f2_make(ex2_approx(x0), ex2_approx(x1));
+          float p0, p1;
+          f2_split(p2, p0, p1);
+          const uint32_t hi = pack_bf16x2(p0, p1);
+          pk[e] = hi;
+          acc2[e & 1] = fadd2(acc2[e & 1], p2);
+          float r0, r1;
+          f2_split(ffma2(f2_make(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u)),
+                         neg1x2, p2),
+                   r0, r1);
+          lo[e] = pack_bf16x2(r0, r1);
+        }
+      } else {
+#pragma unroll
+        for (int e = 16 * c; e < 16 * c + 16; ++e) {
+          pk[e] = 0u;
+          lo[e] = 0u;
+        }
+      }
+    }
+    float s0, s1, s2, s3;
+    f2_split(acc2[0], s0, s1);
+    f2_split(acc2[1], s2, s3);
+    return (s0 + s1) + (s2 + s3);
+  };
+  // The slot's weights of this thread as bf16 pairs into its P columns (and,
+  // split, the low-order terms 32 columns on); sum_w as exp_pack.
+  auto make_p = [&](const uint32_t (&v)[64], float m, bool split, uint32_t pcol,
+                    float* sum_w) -> float {
+    uint32_t pk[32];
+    float sum;
+    if (split) {
+      uint32_t lo[32];
+      sum = exp_pack_split(v, pk, lo, m);
+      *sum_w = sum;
+      tmem_st32(pcol + 32u, lo);
+    } else {
+      sum = exp_pack(v, pk, m, sum_w);
+    }
+    tmem_st32(pcol, pk);
+    return sum;
+  };
 
   for (uint32_t t = 0;; ++t) {
     const Item m = sched_take<D>(sm, smem, t, lane == 0, true, wd);
@@ -728,12 +833,12 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       lim_warp = min(p.causal ? qmin + p.causal_off : 0x7fffffff, kvl - 1);
       lim_warp_hi = min(p.causal ? qmin + 31 + p.causal_off : 0x7fffffff, kvl - 1);
     }
-    float l_run = 0.f, lw_run = 0.f;  // exact and bf16-weight row sums
+    float l_run = 0.f, lw_run = 0.f;  // exact and applied-weight row sums
     bool has_keys = false;            // (bounded pass) some key of this thread's columns is kept
     bool ok = true;
     for (int j = 0; j < m.n; ++j) {
-      const int b = (int)(sg & 1u);
-      const uint32_t u = sg >> 1;
+      const int b = (int)sb.b;
+      const uint32_t u = sb.u;
       if (submask) bits = (__ldg(p.slot_mask + m.s0 + j) >> (qi * p.rk)) & my_bits_mask;
       if (kGeneral && p.elem_mask) {
 #pragma unroll
@@ -750,22 +855,13 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       tc_fence_after();
       uint32_t v[64];
       load_s(tmem + tl + kColS + 128u * (uint32_t)b, v);
-      // The scores are in registers: hand the S buffer back for the next S.
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.bar(C::kBarSFree + b));
-      uint32_t pk[32];
       float sum, sum_w, factor = 1.f;
-      const uint32_t pcol = tmem + tl + kColP + 64u * (uint32_t)b + 32u * (uint32_t)h;
+      // This thread's P columns: the first half of the 64 it has just loaded
+      // (the scores are in registers; no other thread reads these columns).
+      const uint32_t pcol = tmem + tl + kColS + 128u * (uint32_t)b + 64u * (uint32_t)h;
       if constexpr (!kExact) {
         has_keys |= live;  // (set by load_s)
-        sum = exp_pack(v, pk, m_ref, &sum_w);
-        // P buffer b was last read by the P V of slot g - 2.
-        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
-          ok = false;
-          break;
-        }
-        tmem_st32(pcol, pk);
+        sum = make_p(v, m_ref, m.split, pcol, &sum_w);
       } else if (m_ref == -INFINITY) {
         // No reference yet in this row: the whole-row maximum first (both
         // threads of a row get the same value and so the same reference).
@@ -785,22 +881,12 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
           break;
         }
         m_ref = fmaxf(mx, mo) * sl2;  // stays -inf while every key so far is masked
-        sum = exp_pack(v, pk, m_ref, &sum_w);
-        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
-          ok = false;
-          break;
-        }
-        tmem_st32(pcol, pk);
+        sum = make_p(v, m_ref, m.split, pcol, &sum_w);
       } else {
         // Exponentials against the current reference right away; whether a
         // rescale is due is settled while P is being written.
-        sum = exp_pack(v, pk, m_ref, &sum_w);
+        sum = make_p(v, m_ref, m.split, pcol, &sum_w);
         post(sum_w);
-        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
-          ok = false;
-          break;
-        }
-        tmem_st32(pcol, pk);
         float sw_other = 0.f;
         if (!collect(sw_other)) {
           ok = false;
@@ -830,18 +916,19 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
               factor = ex2_approx(m_ref - m_new);
               m_ref = m_new;
             }
-            sum = exp_pack(v, pk, m_ref, &sum_w);
-            // O changes scale: the P V of slot g - 1 must have finished with
-            // it (the one of slot g starts only after this slot's P is
-            // published).
-            const uint32_t g1 = sg - 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + (int)(g1 & 1u)), (g1 >> 1) & 1u, wd, kSitePFull))) {
+            // O changes scale: the P V of slot g - 1 (the row's previous
+            // slot) must have finished with it; its completion is the one
+            // that freed that slot's buffer.  The P V of slot g starts only
+            // after this slot's P is published.
+            const int pb = (b == 0) ? kSlotBufs - 1 : b - 1;
+            const uint32_t pu = (b == 0) ? u - 1u : u;
+            if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarSFree + pb), pu & 1u, wd, kSitePFull))) {
               ok = false;
               break;
             }
             tc_fence_after();
             tmem_wait_st();
-            tmem_st32(pcol, pk);
+            sum = make_p(v, m_ref, m.split, pcol, &sum_w);
             const uint32_t o_addr = tmem + tl + kColO + (uint32_t)(h * (D / 2));
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
@@ -861,7 +948,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.bar(C::kBarPFull + b));  // one arrival per warp
-      ++sg;
+      sb.next();
     }
     if (!ok) break;
     // ------------------------------------------------------------ epilogue
@@ -930,10 +1017,11 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
     for (int i = 0; i < 2; ++i) {
       mbar_init(sm.bar(C::kBarQFull + i), 1);
       mbar_init(sm.bar(C::kBarQEmpty + i), 1 + 8);  // S issuer commit + softmax warps
-      mbar_init(sm.bar(C::kBarSFull + i), 1);
-      mbar_init(sm.bar(C::kBarSFree + i), 8);  // one arrival per softmax warp
+    }
+    for (int i = 0; i < kSlotBufs; ++i) {
+      mbar_init(sm.bar(C::kBarSFull + i), 1);  // S issuer commit
+      mbar_init(sm.bar(C::kBarSFree + i), 1);  // P V issuer commit
       mbar_init(sm.bar(C::kBarPFull + i), 8);  // one arrival per softmax warp
-      mbar_init(sm.bar(C::kBarPFree + i), 1);
     }
     for (int s = 0; s < C::kStagesK; ++s) {
       mbar_init(sm.bar(C::kBarKFull + s), 1);
@@ -1009,16 +1097,19 @@ cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t stream) {
 }
 
 // Largest key norm of every K unit (ku rows) of every K/V head, i.e. a bound
-// on |k| for the Cauchy-Schwarz reference of the bounded pass; also clears
-// the fallback flags.  Each CTA streams groups of kKmaxGroupBytes / (ku*d*2)
-// consecutive units through a ring of shared-memory stages with bulk copies
-// (one thread issues them, completion on the stage's mbarrier), so many
-// bytes are in flight per SM with few registers; each thread then reduces
-// the rows it owns (16-byte reads rotated across the row so the threads of a
-// warp hit different banks).  Units wholly past the sequence's key length
-// (or, paged, without a valid page) get 0 and are not read: their keys are
-// masked.  A wait that runs out is recorded in the pass's own status words
-// (its stage may run on another stream beside the plan kernels).
+// on |k| for the Cauchy-Schwarz reference of the bounded pass, and largest
+// |v| element of every V unit (which decides whether a row applies split
+// weights); also clears the fallback flags.  The K units come first, then
+// the V units: each CTA streams groups of kKmaxGroupBytes / (ku*d*2)
+// consecutive units of one tensor through a ring of shared-memory stages
+// with bulk copies (one thread issues them, completion on the stage's
+// mbarrier), so many bytes are in flight per SM with few registers; each
+// thread then reduces the rows it owns (16-byte reads rotated across the row
+// so the threads of a warp hit different banks).  Units wholly past the
+// sequence's key length (or, paged, without a valid page) get 0 and are not
+// read: their keys are masked.  A wait that runs out is recorded in the
+// pass's own status words (its stage may run on another stream beside the
+// plan kernels).
 constexpr int kKmaxThreads = 128;
 constexpr int kKmaxStages = 3;
 constexpr uint32_t kKmaxGroupBytes = 32768;
@@ -1045,7 +1136,8 @@ __global__ void __launch_bounds__(kKmaxThreads) kmax_kernel(const FwdParams p) {
   const uint32_t ubytes = (uint32_t)p.ku * D * 2;
   const int G = (int)(kKmaxGroupBytes / ubytes);  // units per stage (1 .. 8)
   const long long units = (long long)p.B * p.Hkv * p.NKU;
-  const long long groups = (units + G - 1) / G;
+  const long long groups = (units + G - 1) / G;   // per tensor
+  const long long total = 2 * groups;             // K groups, then V groups
   if (tid == 0) {
     *abort_flag = 0;
     for (int s = 0; s < kKmaxStages; ++s) mbar_init(bars + 8u * s, 1);
@@ -1053,24 +1145,25 @@ __global__ void __launch_bounds__(kKmaxThreads) kmax_kernel(const FwdParams p) {
   }
   __syncthreads();
 
-  // Thread 0: start the copies of unit group gi into stage s.
+  // Thread 0: start the copies of group gi (of K below `groups`, else of V)
+  // into stage s.
   auto issue = [&](long long gi, int s) {
+    const bool isv = gi >= groups;
+    const long long g0 = (isv ? gi - groups : gi) * G;
+    const uint16_t* src = isv ? p.V : p.K;
     uint32_t bytes = 0;
     for (int k = 0; k < G; ++k) {
-      const long long unit = gi * G + k;
+      const long long unit = g0 + k;
       int skip = 1;
-      long long row0 = 0;
       if (unit < units) {
         const int head = (int)(unit / p.NKU), y = (int)(unit % p.NKU);  // head = b * Hkv + hkv
-        const int b = head / p.Hkv, hkv = head % p.Hkv;
+        const int b = head / p.Hkv;
         const int key = y * p.ku;
         skip = (p.kv_lens != nullptr && key >= __ldg(p.kv_lens + b)) ? 1 : 0;
-        row0 = unit * p.ku;  // contiguous: units in row order
         if (p.block_table != nullptr && !skip) {
           const int lp = key / p.page_size;
           const int phys = (lp < p.max_pages) ? __ldg(p.block_table + (size_t)b * p.max_pages + lp) : -1;
           if (phys < 0 || phys >= p.num_pages) skip = 1;
-          else row0 = ((long long)phys * p.Hkv + hkv) * p.page_size + (key - lp * p.page_size);
         }
       }
       skip_s[s * 32 + k] = skip;
@@ -1079,32 +1172,34 @@ __global__ void __launch_bounds__(kKmaxThreads) kmax_kernel(const FwdParams p) {
     mbar_arrive_expect_tx(bars + 8u * s, bytes);
     for (int k = 0; k < G; ++k) {
       if (skip_s[s * 32 + k]) continue;
-      const long long unit = gi * G + k;
+      const long long unit = g0 + k;
       const int head = (int)(unit / p.NKU), y = (int)(unit % p.NKU);
-      long long row0 = unit * p.ku;
+      long long row0 = unit * p.ku;  // contiguous: units in row order
       if (p.block_table != nullptr) {
         const int b = head / p.Hkv, hkv = head % p.Hkv, key = y * p.ku, lp = key / p.page_size;
         const int phys = __ldg(p.block_table + (size_t)b * p.max_pages + lp);
         row0 = ((long long)phys * p.Hkv + hkv) * p.page_size + (key - lp * p.page_size);
       }
-      bulk_load(base + s * kKmaxGroupBytes + k * ubytes, p.K + (size_t)row0 * D, ubytes, bars + 8u * s);
+      bulk_load(base + s * kKmaxGroupBytes + k * ubytes, src + (size_t)row0 * D, ubytes, bars + 8u * s);
     }
   };
 
   if (tid == 0) {
     for (int s = 0; s < kKmaxStages; ++s) {
       const long long gi = blockIdx.x + (long long)s * gridDim.x;
-      if (gi < groups) issue(gi, s);
+      if (gi < total) issue(gi, s);
     }
   }
   constexpr int kChunks = D / 8;  // 16-byte chunks per row
   const int rows = G * p.ku;      // rows per stage: 32768 / (2 D)
   uint32_t it = 0;
-  for (long long gi = blockIdx.x; gi < groups; gi += gridDim.x, ++it) {
+  for (long long gi = blockIdx.x; gi < total; gi += gridDim.x, ++it) {
+    const bool isv = gi >= groups;
     const int s = (int)(it % kKmaxStages);
     const bool waited = mbar_wait(bars + 8u * s, (it / kKmaxStages) & 1u, wd, kSiteKvFull);
     if (!__syncthreads_and(waited)) break;  // uniform: no thread left behind at a barrier
-    // Rows tid, tid + 128, ... of the stage; row r at byte r * 2D.
+    // Rows tid, tid + 128, ... of the stage; row r at byte r * 2D.  K: the
+    // row's squared norm; V: the row's largest |v|.
     for (int rb = 0; rb * kKmaxThreads < rows; ++rb) {
       const int r = rb * kKmaxThreads + tid;
       const uint32_t rowp = base + s * kKmaxGroupBytes + (uint32_t)r * (D * 2);
@@ -1116,44 +1211,51 @@ __global__ void __launch_bounds__(kKmaxThreads) kmax_kernel(const FwdParams p) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xffff0000u);
-          s2a = fmaf(lo, lo, s2a);
-          s2b = fmaf(hi, hi, s2b);
+          if (isv) {
+            s2a = fmaxf(s2a, fabsf(lo));
+            s2b = fmaxf(s2b, fabsf(hi));
+          } else {
+            s2a = fmaf(lo, lo, s2a);
+            s2b = fmaf(hi, hi, s2b);
+          }
         }
       }
-      float m = s2a + s2b;
+      float m = isv ? fmaxf(s2a, s2b) : s2a + s2b;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
       if (lane == 0) rmax_s[rb * (kKmaxThreads / 32) + warp] = m;  // rows 32*(rb*4+warp) ..
     }
     __syncthreads();
     if (tid < G) {
-      const long long unit = gi * G + tid;
+      const long long unit = (isv ? gi - groups : gi) * G + tid;
       if (unit < units) {
         float m = 0.f;
         if (!skip_s[s * 32 + tid]) {
           const int b0 = tid * p.ku / 32, b1 = (tid + 1) * p.ku / 32;  // 32-row blocks of the unit
           for (int q = b0; q < b1; ++q) m = fmaxf(m, rmax_s[q]);
         }
-        p.kmax[unit] = sqrtf(m);
+        if (isv) p.vmax[unit] = m;
+        else p.kmax[unit] = sqrtf(m);
       }
     }
     __syncthreads();  // stage s and rmax_s free again
     if (tid == 0) {
       const long long gn = gi + (long long)kKmaxStages * gridDim.x;
-      if (gn < groups) issue(gn, s);
+      if (gn < total) issue(gn, s);
     }
   }
   if (*abort_flag && tid == 0) {
     // Let copies already issued land before the CTA's shared memory goes away.
     for (int s = 0; s < kKmaxStages; ++s) {
       const long long gi = blockIdx.x + (long long)(it + s) * gridDim.x;
-      if (gi < groups) drain_wait(bars + 8u * ((it + s) % kKmaxStages), ((it + s) / kKmaxStages) & 1u, wd);
+      if (gi < total) drain_wait(bars + 8u * ((it + s) % kKmaxStages), ((it + s) / kKmaxStages) & 1u, wd);
     }
   }
 }
 
 // Largest key norm over the K units of each plan row's slots (one warp per
-// row), the |k| factor of the row's Cauchy-Schwarz reference.  Paged K/V: also
+// row), the |k| factor of the row's Cauchy-Schwarz reference, and the largest
+// |v| element over the same units.  Paged K/V: also
 // the pool row of each slot position's unit, (page*Hkv + hkv)*page_size +
 // key % page_size with the page from the block table, so the producers read
 // rows as they would plan entries.  A page outside the table is an error only
@@ -1163,15 +1265,19 @@ __global__ void __launch_bounds__(256) rowbound_kernel(const FwdParams p) {
   const int row = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
   if (row >= p.rows) return;
   const int s0 = __ldg(p.row_ptr + row), s1 = __ldg(p.row_ptr + row + 1);
-  float km = 0.f;
+  float km = 0.f, vm = 0.f;
   if (s0 >= 0 && s1 >= s0 && (long long)s1 <= p.slot_capacity) {  // else the forward reports it
     const int bh = row / p.NQT, b = bh / p.H, h = bh % p.H, hkv = h / p.g;
     const float* kh = p.kmax + (size_t)(b * p.Hkv + hkv) * p.NKU;
+    const float* vh = p.vmax + (size_t)(b * p.Hkv + hkv) * p.NKU;
     const int kvl = (p.prow && p.kv_lens) ? __ldg(p.kv_lens + b) : 0x7fffffff;
     for (long long i = (long long)s0 * p.rk + lane; i < (long long)s1 * p.rk; i += 32) {
       const int y = __ldg(p.slot_ku + i);
       const bool valid = y >= 0 && y < p.NKU;
-      if (valid) km = fmaxf(km, __ldg(kh + y));
+      if (valid) {
+        km = fmaxf(km, __ldg(kh + y));
+        vm = fmaxf(vm, __ldg(vh + y));
+      }
       if (p.prow) {
         int prow = -1;  // padding, or an entry out of range (reported here)
         if (valid) {
@@ -1191,8 +1297,14 @@ __global__ void __launch_bounds__(256) rowbound_kernel(const FwdParams p) {
     }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, o));
-  if (lane == 0) p.rowk[row] = km;
+  for (int o = 16; o > 0; o >>= 1) {
+    km = fmaxf(km, __shfl_xor_sync(0xffffffffu, km, o));
+    vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+  }
+  if (lane == 0) {
+    p.rowk[row] = km;
+    p.rowv[row] = vm;
+  }
 }
 
 template <int D>
@@ -1201,7 +1313,7 @@ cudaError_t launch_passes(const FwdParams& p, int grid, cudaStream_t stream, int
   const bool general = p.block_table != nullptr || p.elem_mask;
   if (stages & (BSA_STAGE_PREPARE | BSA_STAGE_KNORM)) {
   const long long units = (long long)p.B * p.Hkv * p.NKU;
-  const long long kgroups = (units + (kKmaxGroupBytes / (p.ku * D * 2)) - 1) / (kKmaxGroupBytes / (p.ku * D * 2));
+  const long long kgroups = 2 * ((units + (kKmaxGroupBytes / (p.ku * D * 2)) - 1) / (kKmaxGroupBytes / (p.ku * D * 2)));
   long long kgrid = 2ll * (p.sms > 0 ? p.sms : 1);
   if (kgrid > kgroups) kgrid = kgroups;
   if (kgrid < 1) kgrid = 1;

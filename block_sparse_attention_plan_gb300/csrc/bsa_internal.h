@@ -100,10 +100,12 @@ inline void set_plan_views(PlanDev& d, uint8_t* ws, const bsa_plan_layout& L) {
 // Forward-pass scratch inside a plan workspace, after the plan-construction
 // scratch: the largest key norm of every K unit (float[B*Hkv*NKU]), that of
 // every plan row's selected units (float[rows]), a fallback flag per plan row
-// and the list of rows queued for the exact pass (int32[rows] each), and for
-// paged K/V the pool row of every slot position (int32[slot_capacity*rk]).
+// and the list of rows queued for the exact pass (int32[rows] each), for
+// paged K/V the pool row of every slot position (int32[slot_capacity*rk]),
+// and the largest |v| element of every V unit and of every plan row's units
+// (float[B*Hkv*NKU], float[rows]).
 struct FwdScratch {
-  uint64_t off_kmax, off_rowk, off_fb_flag, off_fb_list, off_prow, end;
+  uint64_t off_kmax, off_rowk, off_fb_flag, off_fb_list, off_prow, off_vmax, off_rowv, end;
 };
 inline FwdScratch fwd_scratch(const bsa_plan_layout& L) {
   uint64_t off = plan_scratch(L).end;
@@ -113,6 +115,8 @@ inline FwdScratch fwd_scratch(const bsa_plan_layout& L) {
   f.off_fb_flag = off; off = align256(off + 4ull * (uint64_t)L.rows);
   f.off_fb_list = off; off = align256(off + 4ull * (uint64_t)L.rows);
   f.off_prow = off;    off = align256(off + 4ull * (uint64_t)L.slot_capacity * L.rk);
+  f.off_vmax = off;    off = align256(off + 4ull * (uint64_t)L.B * L.Hkv * L.NKU);
+  f.off_rowv = off;    off = align256(off + 4ull * (uint64_t)L.rows);
   f.end = off;
   return f;
 }
@@ -131,8 +135,12 @@ struct FwdParams {
   uint16_t* O;       // bf16 bits
   float* LSE;
   const uint16_t* K;     // bf16 bits, [B*Hkv*Nk, d] (read by the key-norm pass)
+  const uint16_t* V;     // bf16 bits, same view as K (read by the key-norm pass)
   float* kmax;           // largest key norm per K unit
   float* rowk;           // largest key norm over each plan row's K units
+  float* vmax;           // largest |v| element per V unit
+  float* rowv;           // largest |v| element over each plan row's V units
+  int split_all;         // every row applies split (hi + lo) weights
   int32_t* fb_flag;      // per plan row: queued for the exact pass
   int32_t* fb_list;      // plan rows queued for the exact pass
   // Paged K/V (block_table == nullptr: contiguous [B*Hkv*Nk, d]).

@@ -34,6 +34,11 @@ static __device__ __align__(256) uint8_t g_static_workspace[BSA_STATIC_WORKSPACE
 
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
+// Byte offset of the control words (status, detail) inside the scratch area
+// for the last call on each device (they move with the problem's layout);
+// 0 before the first call.
+uint64_t g_ctl_off[kMaxDevices] = {};
+bool g_called[kMaxDevices] = {};
 
 bsa_status static_workspace(int dev, uint8_t** out) {
   if (dev < 0 || dev >= kMaxDevices) return BSA_ERR_UNSUPPORTED;
@@ -97,10 +102,41 @@ extern "C" bsa_status bsa_attention_static(const uint8_t* mask, int B, int H, in
                        1000ll * 1000000ll, 0, &fp, &grid);
   if (st != BSA_OK) return st;
 
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_ctl_off[dev] = L.off_control;
+    g_called[dev] = true;
+  }
   // The control words (work counter, status) must start at zero on every call.
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(pd.control, 0, 64, s) != cudaSuccess) return BSA_ERR_CUDA;
   if (launch_plan(pd, s) != cudaSuccess) return BSA_ERR_CUDA;
   if (launch_forward(fp, d, grid, s) != cudaSuccess) return BSA_ERR_CUDA;
   return BSA_OK;
+}
+
+// Status the kernels of the last bsa_attention_static call on the current
+// device recorded in the scratch area (see include/bsa.h).
+extern "C" bsa_status bsa_attention_static_status(void* stream, int32_t* detail) {
+  if (detail) *detail = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return BSA_ERR_UNSUPPORTED;
+  uint64_t off = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_called[dev]) return BSA_OK;  // nothing has run on this device
+    off = g_ctl_off[dev];
+  }
+  uint8_t* ws = nullptr;
+  bsa_status st = static_workspace(dev, &ws);
+  if (st != BSA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t ctl[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (cudaMemcpyAsync(ctl, ws + off, sizeof(ctl), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return BSA_ERR_CUDA;
+  const bool knorm = ctl[kCtlStatus] == 0 && ctl[kCtlKnormStatus] != 0;
+  if (detail) *detail = knorm ? ctl[kCtlKnormDetail] : ctl[kCtlDetail];
+  return static_cast<bsa_status>(knorm ? ctl[kCtlKnormStatus] : ctl[kCtlStatus]);
 }

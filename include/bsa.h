@@ -225,6 +225,13 @@ typedef struct bsa_kv_pages {
 /* Intra-block causal masking: key position j is visible to query position i
  * only when j <= i + (Nk - Nq) (queries are the last Nq positions). */
 #define BSA_FWD_CAUSAL 0x1
+/* Apply every row's softmax weights as two bf16 terms, hi = bf16(p) and
+ * lo = bf16(p - hi), with a second P V product for lo (weights exact to about
+ * 2^-16 instead of 2^-8).  Without the flag this is done only for rows whose
+ * selected K/V units hold a V element of magnitude above 8, where bf16
+ * weights would move O by more than a few thousandths; the tensor work of
+ * such rows grows by half. */
+#define BSA_FWD_SPLIT_P 0x2
 
 /*
  * bsa_forward_ex -- bsa_forward with paged K/V, per-sequence key lengths and
@@ -235,7 +242,7 @@ typedef struct bsa_kv_pages {
  * pages: NULL for contiguous K, V [B][Hkv][Nk][d]; else K and V are the
  *   pools described above.
  * kv_lens: NULL, or device int32 [B] (each in [0, Nk]), caller-owned.
- * flags: 0 or BSA_FWD_CAUSAL.
+ * flags: 0 or an OR of BSA_FWD_CAUSAL and BSA_FWD_SPLIT_P.
  * Other arguments and errors as bsa_forward; additionally
  * BSA_ERR_UNSUPPORTED for a page size that is not a multiple of the K unit
  * and BSA_ERR_INVALID_ARG for a NULL block table, non-positive sizes or
@@ -322,21 +329,39 @@ bsa_status bsa_watchdog_selftest(int32_t* status, int limit_us, void* stream);
  *   - Calls no cudaMalloc/cudaFree or other allocating routine.  The first
  *     call on a device looks up the scratch array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  With lazy module loading (the CUDA default)
+ *     that first call is also where the driver loads the library's device
+ *     code and commits the scratch array on the device, so a caller that
+ *     must not allocate during execution makes one call (any small problem)
+ *     at set-up time.  The looked-up address is kept for the life of the
+ *     process: after cudaDeviceReset, or anything else that destroys the
+ *     device's primary context, this call is not supported.
  *   - Every call on a device shares the one scratch area and leaves its
  *     contents behind; the call clears what must start at zero (work counter
  *     and status words) itself.  Calls whose GPU work overlaps in time (for
  *     example on two streams) race on the scratch area and must be avoided.
- *   - Enqueues a memset, the three plan kernels and the forward kernel on
+ *   - Enqueues a memset, the three plan kernels and the forward passes on
  *     `stream` without synchronising.  Errors detected by the kernels
  *     (watchdog expiry, out-of-range plan data) are recorded in the scratch
- *     area and are not reported by this call; it returns host-detected
- *     argument errors and launch failures only.
+ *     area, not returned by this call (it returns host-detected argument
+ *     errors and launch failures only); bsa_attention_static_status reads
+ *     them back.
  */
 #define BSA_STATIC_WORKSPACE_BYTES (16u << 20)
 bsa_status bsa_attention_static(const uint8_t* mask, int B, int H, int NQB, int NKB, int bq,
                                 int bk, int gqa_group, const void* Q, const void* K, const void* V,
                                 void* O, float* LSE, int d, float scale, void* stream);
+
+/*
+ * bsa_attention_static_status -- synchronise `stream` and report the status
+ * the kernels of the last bsa_attention_static call on the current device
+ * left in the scratch area, with the same codes and *detail encoding as
+ * bsa_sync_status (BSA_OK when no call has run on the device yet).  The
+ * status words are read with one cudaMemcpyAsync on `stream` into a local
+ * host array.  Meaningful only while no other bsa_attention_static call on
+ * the device is in flight.
+ */
+bsa_status bsa_attention_static_status(void* stream, int32_t* detail);
 
 /*
  * bsa_attention_host -- plan + forward from HOST buffers, with the transfers
