@@ -30,26 +30,24 @@
 //            memory, result in tensor memory) for every slot, up to two slots
 //            ahead of the softmax (S is double-buffered);
 //   warp 2   owns the tensor-memory allocation (512 columns); one thread
-//            issues O += P V with P read from tensor memory, then hands the
-//            slot's buffer back to the S issuer.  Two issuing threads in
-//            different warps keep the tensor pipe fed while either one waits
-//            on a barrier or is slowed by the softmax warps sharing its
-//            scheduler;
+//            issues O += P V with P read from tensor memory.  Two issuing
+//            threads in different warps keep the tensor pipe fed while either
+//            one waits on a barrier or is slowed by the softmax warps sharing
+//            its scheduler;
 //   warps 4-11 the softmax: each row of a slot is shared by two threads, one
 //            in warps 4-7 (keys 0-63 of the slot) and one in warps 8-11 (keys
 //            64-127); they combine their row sums at the row's end (and, in
 //            the exact pass, their maxima while it runs).
 //
 // Tensor memory (512 x 32-bit columns x 128 lanes; lane = q-tile row):
-//   [0,128) [128,256) [256,384) slot buffers 0-2, [384,384+d) O.  Slot g of
-//   the CTA uses buffer g mod 3: the S issuer writes S there (fp32, key c in
-//   column c); the softmax thread of key half h loads columns [64h, 64h+64),
-//   then writes P over the first half of what it loaded: bf16 pairs (keys
-//   64h+2c, 64h+2c+1 in column 64h+c, c < 32) and, for rows computed with
-//   split weights, the low-order bf16 terms in columns [64h+32, 64h+64).
-//   Each thread only rewrites columns it has itself loaded, so no thread
-//   overwrites a score another one has yet to read.  The buffer is free again
-//   once that slot's P V has completed.
+//   [0,128) S buffer 0   [128,256) S buffer 1   [256,256+d) O
+//   [384,448) P buffer 0 [448,512) P buffer 1   (P: bf16 pairs, keys 2c, 2c+1
+//   in column c).  Slot g of the CTA uses S and P buffer g mod 2.  A row with
+//   split weights keeps the low-order terms of slot g in S buffer g mod 2:
+//   the softmax thread of key half h, which loaded that buffer's columns
+//   [64h, 64h+64), writes them over [64h, 64h+32) (pairs laid out as in P);
+//   no thread rewrites a column another one has yet to read, and that S
+//   buffer is released by the slot's P V instead of by the softmax.
 //
 // Split weights.  P V on the tensor cores applies P rounded to bf16, i.e.
 // each weight with a relative error of up to 2^-8, which moves O by up to
@@ -81,9 +79,9 @@ constexpr int kTmemCols = 512;
 constexpr int kRegsControl = 72;
 constexpr int kRegsSoftmax = 208;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split");
-constexpr int kSlotBufs = 3;     // slot buffers (S, then P) in tensor memory
-constexpr uint32_t kColS = 0;    // slot buffer b at kColS + 128 b
-constexpr uint32_t kColO = 384;  // O accumulator, d columns
+constexpr uint32_t kColS = 0;    // S buffer b at kColS + 128 b
+constexpr uint32_t kColO = 256;  // O accumulator, d columns
+constexpr uint32_t kColP = 384;  // P buffer b at kColP + 64 b
 // Rows whose K/V units hold a value of magnitude above this apply split
 // weights (hi + lo).  Values of N(0,1) inputs stay below it (their largest
 // magnitude over millions of draws is about 5.5), where the error of bf16
@@ -126,10 +124,11 @@ struct Cfg {
   static constexpr int kBarKEmpty = kBarKFull + kStagesK;
   static constexpr int kBarVFull = kBarKEmpty + kStagesK;
   static constexpr int kBarVEmpty = kBarVFull + kStagesV;
-  static constexpr int kBarSFull = kBarVEmpty + kStagesV;   // [3] S of the slot in buffer b
-  static constexpr int kBarSFree = kBarSFull + kSlotBufs;   // [3] P V of the slot done: buffer b free
-  static constexpr int kBarPFull = kBarSFree + kSlotBufs;   // [3] P of the slot in buffer b
-  static constexpr int kBarOFull = kBarPFull + kSlotBufs;
+  static constexpr int kBarSFull = kBarVEmpty + kStagesV;   // [2]
+  static constexpr int kBarSFree = kBarSFull + 2;           // [2]
+  static constexpr int kBarPFull = kBarSFree + 2;           // [2]
+  static constexpr int kBarPFree = kBarPFull + 2;           // [2]
+  static constexpr int kBarOFull = kBarPFree + 2;
   static constexpr int kBarOFree = kBarOFull + 1;
   static constexpr int kBarXchg = kBarOFree + 1;            // [4 lane quadrants][2 parities]
   static constexpr int kBarDrain = kBarXchg + 8;
@@ -163,18 +162,6 @@ struct Item {
   bool split;  // apply the row's weights as hi + lo bf16 terms
 };
 
-// Slot-buffer cursor: buffer b = g mod 3 of the CTA's g-th slot and its use
-// count u = g / 3 (the phase of that buffer's barriers).  Every role advances
-// its own cursor once per slot, in the same order.
-struct SlotBuf {
-  uint32_t b = 0, u = 0;
-  __device__ __forceinline__ void next() {
-    if (++b == (uint32_t)kSlotBufs) {
-      b = 0;
-      ++u;
-    }
-  }
-};
 
 __device__ __forceinline__ void record_status(int32_t* ctl, int code, int site) {
   if (atomicCAS(ctl + kCtlStatus, 0, code) == 0)
@@ -448,19 +435,21 @@ struct MmaState {
   uint64_t vdesc0;    // MN-major SW128 descriptor of V stage 0 (LBO = next 64 columns)
   uint32_t kc = 0;    // K tiles consumed
   uint32_t vc = 0;    // V tiles consumed
-  SlotBuf sb;         // slot buffer of the next S tile (S issuer) or P V product (P V issuer)
+  uint32_t sg = 0;    // S tiles issued (slot g of the CTA uses S/P buffer g mod 2)
+  uint32_t pg = 0;    // P V products issued
   static constexpr uint64_t kStageStep = (uint64_t)(C::kTileBytes >> 4);
 };
 
-// S = Q K^T into the slot's buffer (M=128, N=128, K=16 per instruction, d/16
-// instructions), once the P V of that buffer's previous slot has completed.
+// S = Q K^T into S buffer sg mod 2 (M=128, N=128, K=16 per instruction, d/16
+// instructions), once that buffer's previous tile has been read out (by the
+// softmax, or for split weights by that slot's P V).
 template <int D>
 __device__ __forceinline__ bool issue_s(const Smem<D>& sm, MmaState<D>& st, uint32_t tmem, int qb,
                                         const Watchdog& wd) {
   using C = Cfg<D>;
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
-  const int b = (int)st.sb.b;
-  const uint32_t u = st.sb.u;
+  const int b = (int)(st.sg & 1u);
+  const uint32_t u = st.sg >> 1;
   if (u > 0 && !mbar_wait(sm.bar(C::kBarSFree + b), (u - 1) & 1u, wd, kSiteSFull)) return false;
   const uint32_t stage = st.kc % (uint32_t)C::kStagesK;
   if (!mbar_wait(sm.bar(C::kBarKFull + (int)stage), (st.kc / C::kStagesK) & 1u, wd, kSiteKvFull))
@@ -476,35 +465,37 @@ __device__ __forceinline__ bool issue_s(const Smem<D>& sm, MmaState<D>& st, uint
   mma_commit(sm.bar(C::kBarKEmpty + (int)stage));
   mma_commit(sm.bar(C::kBarSFull + b));
   ++st.kc;
-  st.sb.next();
+  ++st.sg;
   return true;
 }
 
 // O (+)= P V: M=128, N=d, K=16 keys per instruction, 8 instructions; P from
-// the slot's buffer in tensor memory (keys [16kk, 16kk+16) in columns
-// 64(kk/4) + 8(kk%4) .. +8), V rows [16kk, 16kk+16) start 2048 bytes apart.
-// Split weights: 8 more instructions with the low-order terms (32 columns
-// further on) against the same V rows.
+// tensor memory (columns [8kk, 8kk+8) hold keys [16kk, 16kk+16)), V rows
+// [16kk, 16kk+16) start 2048 bytes apart.  Split weights: 8 more
+// instructions with the low-order terms, which sit in the slot's S buffer
+// (keys [16kk, 16kk+16) in columns 64(kk/4) + 8(kk%4) .. +8), against the
+// same V rows.
 template <int D>
 __device__ __forceinline__ void issue_pv(MmaState<D>& st, uint32_t tmem, uint32_t stage,
                                          bool accumulate, bool split) {
   constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, true);
-  const uint32_t pcol = tmem + kColS + 128u * st.sb.b;
+  const uint32_t pcol = tmem + kColP + 64u * (st.pg & 1u);
   const uint64_t vd = st.vdesc0 + (uint64_t)stage * MmaState<D>::kStageStep;
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
-    mma_ts(tmem + kColO, pcol + 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3),
-           vd + (uint64_t)(kk * (2048 >> 4)), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+    mma_ts(tmem + kColO, pcol + 8u * (uint32_t)kk, vd + (uint64_t)(kk * (2048 >> 4)), kIdescPV,
+           (accumulate || kk > 0) ? 1u : 0u);
   if (split) {
+    const uint32_t lcol = tmem + kColS + 128u * (st.pg & 1u);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-      mma_ts(tmem + kColO, pcol + 32u + 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3),
+      mma_ts(tmem + kColO, lcol + 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3),
              vd + (uint64_t)(kk * (2048 >> 4)), kIdescPV, 1u);
   }
 }
 
-// S issuer: S of every slot, in slot order, as soon as its buffer is free (the
-// P V of the slot three back has completed) and its K tile has landed.
+// S issuer: S of every slot, in slot order, as soon as its S buffer has been
+// read out (two slots back) and its K tile has landed.
 template <int D>
 __device__ __noinline__ void s_issuer_role(const FwdParams& p, const uint8_t* smem, const Smem<D> sm,
                                            uint32_t tmem, const Watchdog wd) {
@@ -532,7 +523,7 @@ __device__ __noinline__ void s_issuer_role(const FwdParams& p, const uint8_t* sm
 
 // P V issuer: O (+)= P V of every slot once its P is in tensor memory and its
 // V tile has landed; the first of a row also waits until the previous row's
-// epilogue has read O out.  Its completion frees the slot's buffer.  Runs in its own warp so that its waits and
+// epilogue has read O out.  Runs in its own warp so that its waits and
 // commits never leave the tensor pipe without queued S work.
 template <int D>
 __device__ __noinline__ void pv_issuer_role(const FwdParams& p, const uint8_t* smem, const Smem<D> sm,
@@ -548,8 +539,8 @@ __device__ __noinline__ void pv_issuer_role(const FwdParams& p, const uint8_t* s
     const int n = m.n;
     if (n == 0) continue;
     for (int j = 0; j < n && ok; ++j) {
-      const int b = (int)st.sb.b;
-      if (!mbar_wait(sm.bar(C::kBarPFull + b), st.sb.u & 1u, wd, kSitePFull)) {
+      const int b = (int)(st.pg & 1u);
+      if (!mbar_wait(sm.bar(C::kBarPFull + b), (st.pg >> 1) & 1u, wd, kSitePFull)) {
         ok = false;
         break;
       }
@@ -567,10 +558,17 @@ __device__ __noinline__ void pv_issuer_role(const FwdParams& p, const uint8_t* s
       tc_fence_after();
       issue_pv<D>(st, tmem, stage, j > 0, m.split);
       mma_commit(sm.bar(C::kBarVEmpty + (int)stage));
-      mma_commit(sm.bar(C::kBarSFree + b));  // the slot's buffer may take the next S
+      mma_commit(sm.bar(C::kBarPFree + b));
+      if (m.split) {
+        // The S buffer held this slot's low-order terms: release it for the
+        // next S once they are read, with as many arrivals as the softmax
+        // warps give it otherwise.
+#pragma unroll
+        for (int w8 = 0; w8 < 8; ++w8) mma_commit(sm.bar(C::kBarSFree + b));
+      }
       if (j == n - 1) mma_commit(sm.bar(C::kBarOFull));
       ++st.vc;
-      st.sb.next();
+      ++st.pg;
     }
     ++rows;
   }
@@ -604,8 +602,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   const float sl2 = p.scale_log2;
   const uint64_t sl2x2 = f2_make(sl2, sl2);
   float* xbuf = reinterpret_cast<float*>(smem + C::kOffX);
-  SlotBuf sb;  // the buffer of this CTA's next slot
-  uint32_t rows = 0, xc = 0, q_it = 0;
+  uint32_t sg = 0, rows = 0, xc = 0, q_it = 0;
   uint32_t bits = 0xffffffffu;  // this row's sub-mask bits for the current slot
   // Element mask (causal / key lengths): key position of the first key of each
   // of this thread's two 32-key chunks of the current slot (-1: padding), the
@@ -765,22 +762,6 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   };
   // The slot's weights of this thread as bf16 pairs into its P columns (and,
   // split, the low-order terms 32 columns on); sum_w as exp_pack.
-  auto make_p = [&](const uint32_t (&v)[64], float m, bool split, uint32_t pcol,
-                    float* sum_w) -> float {
-    uint32_t pk[32];
-    float sum;
-    if (split) {
-      uint32_t lo[32];
-      sum = exp_pack_split(v, pk, lo, m);
-      *sum_w = sum;
-      tmem_st32(pcol + 32u, lo);
-    } else {
-      sum = exp_pack(v, pk, m, sum_w);
-    }
-    tmem_st32(pcol, pk);
-    return sum;
-  };
-
   for (uint32_t t = 0;; ++t) {
     const Item m = sched_take<D>(sm, smem, t, lane == 0, true, wd);
     if (m.it < 0) break;
@@ -836,9 +817,13 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     float l_run = 0.f, lw_run = 0.f;  // exact and applied-weight row sums
     bool has_keys = false;            // (bounded pass) some key of this thread's columns is kept
     bool ok = true;
+    // The slot loop, instantiated per kind of row (split weights or not): a
+    // row runs one of them, so the hot loop holds one exponential path.
+    auto slot_loop = [&](auto split_c) {
+    constexpr bool kSplit = decltype(split_c)::value;
     for (int j = 0; j < m.n; ++j) {
-      const int b = (int)sb.b;
-      const uint32_t u = sb.u;
+      const int b = (int)(sg & 1u);
+      const uint32_t u = sg >> 1;
       if (submask) bits = (__ldg(p.slot_mask + m.s0 + j) >> (qi * p.rk)) & my_bits_mask;
       if (kGeneral && p.elem_mask) {
 #pragma unroll
@@ -855,13 +840,39 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       tc_fence_after();
       uint32_t v[64];
       load_s(tmem + tl + kColS + 128u * (uint32_t)b, v);
+      if constexpr (!kSplit) {
+        // The scores are in registers: hand the S buffer back for the next S.
+        // (Split weights keep their low-order terms there; the slot's P V
+        // hands it back.)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.bar(C::kBarSFree + b));
+      }
+      uint32_t pk[32];
       float sum, sum_w, factor = 1.f;
-      // This thread's P columns: the first half of the 64 it has just loaded
-      // (the scores are in registers; no other thread reads these columns).
-      const uint32_t pcol = tmem + tl + kColS + 128u * (uint32_t)b + 64u * (uint32_t)h;
+      const uint32_t pcol = tmem + tl + kColP + 64u * (uint32_t)b + 32u * (uint32_t)h;
+      // Weights against reference `mr` into pk (and, split, the low-order
+      // terms straight into this thread's own S columns).
+      auto exps = [&](float mr) -> float {
+        if constexpr (kSplit) {
+          uint32_t lo[32];
+          const float t = exp_pack_split(v, pk, lo, mr);
+          sum_w = t;
+          tmem_st32(tmem + tl + kColS + 128u * (uint32_t)b + 64u * (uint32_t)h, lo);
+          return t;
+        } else {
+          return exp_pack(v, pk, mr, &sum_w);
+        }
+      };
       if constexpr (!kExact) {
         has_keys |= live;  // (set by load_s)
-        sum = make_p(v, m_ref, m.split, pcol, &sum_w);
+        sum = exps(m_ref);
+        // P buffer b was last read by the P V of slot g - 2.
+        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
+          ok = false;
+          break;
+        }
+        tmem_st32(pcol, pk);
       } else if (m_ref == -INFINITY) {
         // No reference yet in this row: the whole-row maximum first (both
         // threads of a row get the same value and so the same reference).
@@ -881,12 +892,22 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
           break;
         }
         m_ref = fmaxf(mx, mo) * sl2;  // stays -inf while every key so far is masked
-        sum = make_p(v, m_ref, m.split, pcol, &sum_w);
+        sum = exps(m_ref);
+        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
+          ok = false;
+          break;
+        }
+        tmem_st32(pcol, pk);
       } else {
         // Exponentials against the current reference right away; whether a
         // rescale is due is settled while P is being written.
-        sum = make_p(v, m_ref, m.split, pcol, &sum_w);
+        sum = exps(m_ref);
         post(sum_w);
+        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
+          ok = false;
+          break;
+        }
+        tmem_st32(pcol, pk);
         float sw_other = 0.f;
         if (!collect(sw_other)) {
           ok = false;
@@ -916,19 +937,19 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
               factor = ex2_approx(m_ref - m_new);
               m_ref = m_new;
             }
-            // O changes scale: the P V of slot g - 1 (the row's previous
-            // slot) must have finished with it; its completion is the one
-            // that freed that slot's buffer.  The P V of slot g starts only
-            // after this slot's P is published.
-            const int pb = (b == 0) ? kSlotBufs - 1 : b - 1;
-            const uint32_t pu = (b == 0) ? u - 1u : u;
-            if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarSFree + pb), pu & 1u, wd, kSitePFull))) {
+            tmem_wait_st();  // the first stores of this slot's terms are done
+            sum = exps(m_ref);
+            // O changes scale: the P V of slot g - 1 must have finished with
+            // it (the one of slot g starts only after this slot's P is
+            // published).
+            const uint32_t g1 = sg - 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + (int)(g1 & 1u)), (g1 >> 1) & 1u, wd, kSitePFull))) {
               ok = false;
               break;
             }
             tc_fence_after();
             tmem_wait_st();
-            sum = make_p(v, m_ref, m.split, pcol, &sum_w);
+            tmem_st32(pcol, pk);
             const uint32_t o_addr = tmem + tl + kColO + (uint32_t)(h * (D / 2));
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
@@ -948,8 +969,11 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.bar(C::kBarPFull + b));  // one arrival per warp
-      sb.next();
+      ++sg;
     }
+    };
+    if (m.split) slot_loop(std::true_type{});
+    else slot_loop(std::false_type{});
     if (!ok) break;
     // ------------------------------------------------------------ epilogue
     if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarOFull), rows & 1u, wd, kSiteODone))) break;
@@ -1017,11 +1041,11 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
     for (int i = 0; i < 2; ++i) {
       mbar_init(sm.bar(C::kBarQFull + i), 1);
       mbar_init(sm.bar(C::kBarQEmpty + i), 1 + 8);  // S issuer commit + softmax warps
-    }
-    for (int i = 0; i < kSlotBufs; ++i) {
-      mbar_init(sm.bar(C::kBarSFull + i), 1);  // S issuer commit
-      mbar_init(sm.bar(C::kBarSFree + i), 1);  // P V issuer commit
+      mbar_init(sm.bar(C::kBarSFull + i), 1);
+      // one arrival per softmax warp, or (split weights) 8 P V commits
+      mbar_init(sm.bar(C::kBarSFree + i), 8);
       mbar_init(sm.bar(C::kBarPFull + i), 8);  // one arrival per softmax warp
+      mbar_init(sm.bar(C::kBarPFree + i), 1);
     }
     for (int s = 0; s < C::kStagesK; ++s) {
       mbar_init(sm.bar(C::kBarKFull + s), 1);
