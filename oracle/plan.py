@@ -9,14 +9,18 @@ summary: a Q-block union plus an intra-group union give a GQA-aware per-group
 KV block table.  The pages give no concrete rule; the plainest reading, used
 here and by the CUDA path (which implements it independently), is:
 
-Mapping (physical q-tile = 128 query rows, physical K/V slot = 128 key rows):
-  qu = min(bq,128) rows per q-unit, rq = 128/qu q-units per q-tile,
+Mapping (physical q-tile = T query rows, T = 128 or, for bq <= 64, 64;
+physical K/V slot = 128 key rows):
+  qu = min(bq,T) rows per q-unit, rq = T/qu q-units per q-tile,
   sq = bq/qu q-units per logical q-block (2 when bq = 256: subdivide);
   ku = min(bk,128) rows per k-unit, rk = 128/ku k-units per slot,
   sk = bk/ku k-units per logical k-block.
-  bq = 128 / bk = 128 retains; smaller blocks are combined rq (rk) to a tile
+  bq = T / bk = 128 retains; smaller blocks are combined rq (rk) to a tile
   (slot); bq = 256 / bk = 256 are subdivided into two 128-row units.
-  NQT = Nq/128 q-tiles, NKU = Nk/ku k-units.
+  NQT = Nq/T q-tiles, NKU = Nk/ku k-units.  The 64-row tile is a second
+  physical mapping of small query blocks: a 64-row q-block is a tile of its
+  own instead of sharing a 128-row tile (and the union of selections) with a
+  neighbour.
   Unit mask U[b,h,x,y] = mask[b,h,x // sq, y // sk] != 0.
 
 Per plan row r = (b*H + h)*NQT + qt:
@@ -51,6 +55,7 @@ import numpy as np
 
 SUPPORTED_BLOCKS = (32, 64, 128, 256)
 TILE = 128
+TILES = (64, 128)   # physical q-tile heights
 
 
 @dataclass
@@ -65,13 +70,16 @@ class Mapping:
     sk: int
 
 
-def mapping(bq: int, bk: int) -> Mapping:
-    """Retain / combine / subdivide rule for one (bq, bk) pair."""
+def mapping(bq: int, bk: int, tile: int = TILE) -> Mapping:
+    """Retain / combine / subdivide rule for one (bq, bk) pair and q-tile
+    height ``tile`` (128, or 64 for bq <= 64); K/V slots are always 128 keys."""
     if bq not in SUPPORTED_BLOCKS or bk not in SUPPORTED_BLOCKS:
         raise ValueError(f"unsupported block sizes bq={bq} bk={bk}")
-    qu = min(bq, TILE)
+    if tile not in TILES or (tile == 64 and bq > 64):
+        raise ValueError(f"unsupported q-tile height {tile} for bq={bq}")
+    qu = min(bq, tile)
     ku = min(bk, TILE)
-    return Mapping(bq, bk, qu, TILE // qu, bq // qu, ku, TILE // ku, bk // ku)
+    return Mapping(bq, bk, qu, tile // qu, bq // qu, ku, TILE // ku, bk // ku)
 
 
 def unit_mask(mask: np.ndarray, mp: Mapping) -> np.ndarray:
@@ -118,24 +126,26 @@ def choose_sigma(Up: np.ndarray, rq: int, rk: int) -> int:
     return best
 
 
-def build_plan(mask, bq: int, bk: int, gqa_group: int = 1, remap: bool = False) -> dict:
+def build_plan(mask, bq: int, bk: int, gqa_group: int = 1, remap: bool = False,
+               tile: int = TILE) -> dict:
     """Return every plan array as numpy (int32 / uint32 / int64).
 
     remap: choose each (b, h) plane's q-unit grouping stride (choose_sigma);
     only when tiles combine several q-units (rq > 1) and without GQA
     grouping (gqa_group = 1), otherwise every plane keeps stride 1.  The
-    strides are returned as plane_sigma [B*H]."""
+    strides are returned as plane_sigma [B*H].
+    tile: q-tile height (see the mapping rule above)."""
     if hasattr(mask, "detach"):
         mask = mask.detach().cpu().numpy()
     mask = np.asarray(mask)
-    mp = mapping(bq, bk)
+    mp = mapping(bq, bk, tile)
     B, H, NQB, NKB = mask.shape
     if H % gqa_group:
         raise ValueError("H must be a multiple of gqa_group")
     U = unit_mask(mask, mp)
     NQU, NKU = U.shape[2], U.shape[3]
     if NQU % mp.rq:
-        raise ValueError("Nq must be a multiple of 128")
+        raise ValueError(f"Nq must be a multiple of {tile}")
     NQT = NQU // mp.rq
     R = B * H * NQT
 

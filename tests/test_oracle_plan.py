@@ -32,13 +32,14 @@ def tile_rows(qt: int, sigma: int, rq: int):
     return [run * sigma * rq + r + i * sigma for i in range(rq)]
 
 
-def check_plan_invariants(mask: np.ndarray, bq: int, bk: int, g: int, p: dict):
-    """Structural checks written independently of the oracle's construction."""
+def check_plan_invariants(mask: np.ndarray, bq: int, bk: int, g: int, p: dict, tile: int = 128):
+    """Structural checks written independently of the oracle's construction
+    (``tile``: q-tile height; K/V slots hold 128 keys)."""
     B, H, NQB, NKB = mask.shape
     Nq, Nk = NQB * bq, NKB * bk
-    qu, ku = min(bq, 128), min(bk, 128)
-    rq, rk = 128 // qu, 128 // ku
-    NQT = Nq // 128
+    qu, ku = min(bq, tile), min(bk, 128)
+    rq, rk = tile // qu, 128 // ku
+    NQT = Nq // tile
     R = B * H * NQT
     rp, sk, sm = p["row_ptr"].astype(np.int64), p["slot_ku"].reshape(-1, rk), p["slot_mask"]
     assert rp[0] == 0 and rp.size == R + 1 and np.all(np.diff(rp) >= 0)
@@ -122,10 +123,11 @@ def test_hand_worked_examples():
     cases = json.load(open(GOLDEN))["cases"]
     for c in cases:
         mask = np.array(c["mask"], dtype=np.uint8)
-        p = OP.build_plan(mask, c["bq"], c["bk"], c["gqa_group"])
+        tile = c.get("tile", 128)
+        p = OP.build_plan(mask, c["bq"], c["bk"], c["gqa_group"], tile=tile)
         for k in KEYS:
             assert p[k].tolist() == c[k], (c["name"], k, p[k].tolist(), c[k])
-        check_plan_invariants(mask, c["bq"], c["bk"], c["gqa_group"], p)
+        check_plan_invariants(mask, c["bq"], c["bk"], c["gqa_group"], p, tile)
 
 
 GRIDS = {32: 4, 64: 2, 128: 3, 256: 3}  # NQB so that Nq is a multiple of 128
@@ -140,6 +142,19 @@ def test_exhaustive_small_grids(bq, bk):
         m = np.array([(bits >> t) & 1 for t in range(n)], dtype=np.uint8).reshape(1, 1, nqb, nkb)
         p = OP.build_plan(m, bq, bk, 1)
         check_plan_invariants(m, bq, bk, 1, p)
+
+
+@pytest.mark.parametrize("bq,bk", list(itertools.product((32, 64), (32, 64, 128, 256))))
+def test_exhaustive_small_grids_tile64(bq, bk):
+    # 64-row q-tiles: a 64-row q-block is a tile of its own, two 32-row
+    # q-blocks share one
+    nqb = 4 if bq == 32 else 3
+    nkb = 2 if bq == 32 else 3
+    n = nqb * nkb
+    for bits in range(1 << n):
+        m = np.array([(bits >> t) & 1 for t in range(n)], dtype=np.uint8).reshape(1, 1, nqb, nkb)
+        p = OP.build_plan(m, bq, bk, 1, tile=64)
+        check_plan_invariants(m, bq, bk, 1, p, tile=64)
 
 
 @pytest.mark.parametrize("bq,bk,g", [(64, 32, 2), (32, 64, 4), (128, 256, 2), (256, 64, 1)])
@@ -170,12 +185,44 @@ def test_chunked_prefill_closed_form_counts():
             assert sorted(s) == ks[ks >= 0].tolist()
 
 
+def test_chunked_prefill_closed_form_tile64():
+    # one 64-row q-block per tile: each row lists exactly its q-block's 65
+    # selected k-blocks, in ceil(65 / 2) = 33 slots
+    w = W.make_workload("chunked_prefill", data=False)
+    m = w.mask.numpy()
+    p = OP.build_plan(m, 64, 64, 4, tile=64)
+    rp = p["row_ptr"].astype(np.int64)
+    assert np.all(np.diff(rp) == 33) and p["totals"][0] == 32 * 64 * 33 == 67584
+    sk = p["slot_ku"].reshape(-1, 2)
+    for h in (0, 9, 31):
+        for qb in (0, 40, 63):
+            r = h * 64 + qb
+            ks = sk[rp[r]:rp[r + 1]].ravel()
+            assert ks[ks >= 0].tolist() == np.flatnonzero(m[0, h, qb]).tolist()
+            assert ks[-1] == -1   # 65 units: the last slot is half padding
+
+
+def test_random_masks_tile64_gqa_and_remap():
+    for bq, bk, g in ((64, 32, 2), (32, 64, 4), (32, 128, 1), (64, 256, 1)):
+        w = W.random_problem(17 + bq + bk, 2, 4, 4 // g, 512, 768, 16, bq, bk, 0.3, values=True)
+        m = w.mask.numpy()
+        check_plan_invariants(m, bq, bk, g, OP.build_plan(m, bq, bk, g, tile=64), tile=64)
+        if g == 1 and bq == 32:
+            check_plan_invariants(m, bq, bk, g, OP.build_plan(m, bq, bk, g, remap=True, tile=64), tile=64)
+
+
 def test_mapping_rule():
     assert (OP.mapping(128, 128).rq, OP.mapping(128, 128).rk) == (1, 1)
     mp = OP.mapping(32, 64)
     assert (mp.qu, mp.rq, mp.sq, mp.ku, mp.rk, mp.sk) == (32, 4, 1, 64, 2, 1)
     mp = OP.mapping(256, 256)
     assert (mp.qu, mp.rq, mp.sq, mp.ku, mp.rk, mp.sk) == (128, 1, 2, 128, 1, 2)
+    mp = OP.mapping(32, 64, tile=64)
+    assert (mp.qu, mp.rq, mp.sq, mp.ku, mp.rk, mp.sk) == (32, 2, 1, 64, 2, 1)
+    mp = OP.mapping(64, 256, tile=64)
+    assert (mp.qu, mp.rq, mp.sq, mp.ku, mp.rk, mp.sk) == (64, 1, 1, 128, 1, 2)
+    with pytest.raises(ValueError):
+        OP.mapping(128, 64, tile=64)   # the 64-row tile is for blocks of at most 64 rows
     with pytest.raises(ValueError):
         OP.mapping(48, 64)
     with pytest.raises(ValueError):
