@@ -19,6 +19,7 @@ STATUS_NAMES = {
 }
 PLAN_NO_UNION = 0x1
 PLAN_REMAP = 0x2
+PLAN_Q64 = 0x4
 STAGE_PREPARE, STAGE_BOUNDED, STAGE_EXACT, STAGE_ALL = 0x1, 0x2, 0x4, 0x7
 STAGE_KNORM, STAGE_ROWBOUND = 0x8, 0x10
 FWD_CAUSAL = 0x1

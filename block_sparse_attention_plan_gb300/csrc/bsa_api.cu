@@ -35,18 +35,21 @@ bsa_status compute_layout(int B, int H, int NQB, int NKB, int bq, int bk, int g,
   if (B < 1 || H < 1 || NQB < 1 || NKB < 1 || g < 1) return BSA_ERR_INVALID_ARG;
   if (!supported_block(bq) || !supported_block(bk)) return BSA_ERR_UNSUPPORTED;
   if (H % g) return BSA_ERR_INVALID_ARG;
-  if (flags & ~(BSA_PLAN_NO_UNION | BSA_PLAN_REMAP)) return BSA_ERR_INVALID_ARG;
+  if (flags & ~(BSA_PLAN_NO_UNION | BSA_PLAN_REMAP | BSA_PLAN_Q64)) return BSA_ERR_INVALID_ARG;
+  // Physical q-tile height: 128 rows, or 64 for blocks of at most 64 rows.
+  const int qtile = (flags & BSA_PLAN_Q64) ? 64 : kTile;
+  if (qtile < bq && qtile < kTile) return BSA_ERR_UNSUPPORTED;
   bsa_plan_layout l;
   std::memset(&l, 0, sizeof(l));
   l.B = B; l.H = H; l.Hkv = H / g; l.NQB = NQB; l.NKB = NKB; l.bq = bq; l.bk = bk; l.gqa_group = g;
-  l.qu = bq < kTile ? bq : kTile;
-  l.rq = kTile / l.qu;
+  l.qu = bq < qtile ? bq : qtile;
+  l.rq = qtile / l.qu;
   l.sq = bq / l.qu;
   l.ku = bk < kTile ? bk : kTile;
   l.rk = kTile / l.ku;
   l.sk = bk / l.ku;
   const long long NQU = (long long)NQB * l.sq;
-  if (NQU % l.rq) return BSA_ERR_INVALID_ARG;  // Nq must be a multiple of 128
+  if (NQU % l.rq) return BSA_ERR_INVALID_ARG;  // Nq must be a multiple of the q-tile height
   const long long NQT = NQU / l.rq;
   const long long NKU = (long long)NKB * l.sk;
   const long long rows = (long long)B * H * NQT;
@@ -171,7 +174,7 @@ bsa_status make_fwd_params(const bsa_plan_layout& L, const PlanDev& pd, uint8_t*
 
   FwdParams& fp = *out;
   std::memset(&fp, 0, sizeof(fp));
-  if (!encode_map(&fp.tmQ, Q, (uint64_t)qrows, d, kTile) ||
+  if (!encode_map(&fp.tmQ, Q, (uint64_t)qrows, d, L.qu * L.rq) ||
       !encode_map(&fp.tmQu, Q, (uint64_t)qrows, d, L.qu) ||
       !encode_map(&fp.tmK, K, (uint64_t)kvrows, d, L.ku) ||
       !encode_map(&fp.tmV, V, (uint64_t)kvrows, d, L.ku))
@@ -378,6 +381,9 @@ bsa_status bsa_forward_stage(const bsa_plan* plan, const void* Q, const void* K,
   bsa_status st = check_arch(&dev);
   if (st != BSA_OK) return st;
   if (dev != p->device) return BSA_ERR_PLAN_MISMATCH;
+  // 64-row q-tiles: contiguous K/V without an element mask only.
+  if (p->L.qu * p->L.rq == 64 && (pages || kv_lens || (flags & BSA_FWD_CAUSAL)))
+    return BSA_ERR_UNSUPPORTED;
   const PlanDev& pd = p->dev;
   FwdParams fp;
   int grid = 1;

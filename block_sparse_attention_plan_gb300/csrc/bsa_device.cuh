@@ -297,6 +297,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// Same with A read MN-major as well (bit 15): A stored with its M index
+// contiguous, as a [K][M] tile.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int M, int N, bool a_mn_major,
+                                                         bool b_mn_major) {
+  return idesc_bf16_f32(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
+}
 
 // 16-byte shared-memory load.
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {

@@ -64,13 +64,10 @@
 #include <type_traits>
 #include <cuda_bf16.h>
 
-#include "bsa_device.cuh"
-#include "bsa_internal.h"
+#include "bsa_fwd_common.cuh"
 
 namespace bsa {
 namespace {
-
-using namespace dev;
 
 constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;
@@ -82,11 +79,6 @@ static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "regist
 constexpr uint32_t kColS = 0;    // S buffer b at kColS + 128 b
 constexpr uint32_t kColO = 256;  // O accumulator, d columns
 constexpr uint32_t kColP = 384;  // P buffer b at kColP + 64 b
-// Rows whose K/V units hold a value of magnitude above this apply split
-// weights (hi + lo).  Values of N(0,1) inputs stay below it (their largest
-// magnitude over millions of draws is about 5.5), where the error of bf16
-// weights stays a few thousandths of the output scale.
-constexpr float kSplitV = 8.0f;
 // Lazy rescale: O and the row sums keep the reference maximum m of the row
 // until some score exceeds it by more than kRescaleThreshold (log2 units),
 // so weights stay <= 2^16 (bf16 and fp32 hold them exactly as well as 1).
@@ -94,23 +86,16 @@ constexpr float kSplitV = 8.0f;
 // is what is checked per slot; only then are the exact maxima compared.
 constexpr float kRescaleThreshold = 16.0f;
 constexpr float kRescaleSumBound = 65536.0f;  // 2^kRescaleThreshold
-// Bounded pass: weights below 2^-126 are flushed to zero, so a row of at most
-// n keys whose weights sum to at least n * 2^-102 loses under 2^-24 of its
-// total weight (fp32 precision); a row below that (while it has selected
-// keys) is recomputed by the exact pass.
-constexpr float kFallbackPerKey = 0x1p-102f;
-// Work items (positions in the plan's schedule: K/V-head groups heaviest
-// first, rows longest first inside a group) are taken from a global atomic
-// counter by the K producer and handed to the other roles through a small
-// ring in shared memory.
-constexpr int kSchedSlots = 4;
-constexpr int kSchedConsumers = 1 + 2 + 8;  // V producer, two MMA threads, one lane per softmax warp
-
-template <int D>
+template <int D_>
 struct Cfg {
+  static constexpr int D = D_;
   static constexpr int kTileBytes = 128 * D * 2;   // 128 rows x d bf16
   static constexpr int kChunks = D / 64;           // 64-column (128-byte) swizzle blocks
   static constexpr int kChunkBytes = 128 * 128;    // one block of 128 rows
+  static constexpr int kQBytes = kTileBytes;       // the Q tile is a 128-row tile too
+  static constexpr int kQChunkBytes = kChunkBytes;
+  static constexpr int kKSweeps = 1;
+  static constexpr bool kQueueSplit = false;
   static constexpr int kQBufs = (D == 128) ? 1 : 2;
   static constexpr int kStagesK = (D == 128) ? 3 : 6;
   static constexpr int kStagesV = (D == 128) ? 3 : 6;
@@ -142,287 +127,6 @@ struct Cfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// Q buffer index and phase parity of the q_it-th non-empty row of a CTA.
-template <int D>
-__device__ __forceinline__ int q_buf(uint32_t q_it) { return (int)(q_it % Cfg<D>::kQBufs); }
-template <int D>
-__device__ __forceinline__ uint32_t q_par(uint32_t q_it) { return (q_it / Cfg<D>::kQBufs) & 1u; }
-
-struct Item {
-  int n;       // slots of the row (0 = empty or rejected)
-  int s0;      // first slot index
-  int bh;      // b*H + h
-  int qx;      // first q-unit of the row's q-tile (its q-unit i is qx + i*qs)
-  int qs;      // q-unit stride of the plane (1 unless the plan regrouped it)
-  int kvrow0;  // first K/V row of the head's sequence in the [B*Hkv*Nk, d] view
-  bool valid;  // the schedule entry named a plan row
-  int row;     // plan row
-  int it;      // schedule position; < 0: no more work (-2: a wait gave up)
-  float kb;    // largest key norm over the row's K units
-  bool split;  // apply the row's weights as hi + lo bf16 terms
-};
-
-
-__device__ __forceinline__ void record_status(int32_t* ctl, int code, int site) {
-  if (atomicCAS(ctl + kCtlStatus, 0, code) == 0)
-    atomicExch(ctl + kCtlDetail, (int)((blockIdx.x << 8) | (site & 0xff)));
-}
-
-// Decode one schedule entry, rejecting out-of-range plan data (the row is then
-// treated as empty and BSA_ERR_PLAN_MISMATCH is recorded).
-__device__ __forceinline__ Item load_item(const FwdParams& p, int it, bool report) {
-  Item m{0, 0, 0, 0, 1, 0, false, 0, it, 0.f, false};
-  const int row = __ldg(p.order + it);
-  if (row < 0 || row >= p.rows) {
-    if (report) record_status(p.control, -7, kSitePlanRange);
-    return m;
-  }
-  m.valid = true;
-  m.row = row;
-  const int s0 = __ldg(p.row_ptr + row), s1 = __ldg(p.row_ptr + row + 1);
-  m.bh = row / p.NQT;
-  const int qt = row % p.NQT;
-  m.qs = 1;
-  m.qx = qt * p.rq;
-  if (p.sigma != nullptr) {  // a plan built with regrouping
-    int sig = __ldg(p.sigma + m.bh);
-    if (!(sig == 1 || sig == 2 || sig == 4 || sig == 8 || sig == 16) || p.NQT % sig) {
-      if (report) record_status(p.control, -7, kSitePlanRange + 5);
-      sig = 1;
-    }
-    m.qs = sig;
-    m.qx = (qt / sig) * sig * p.rq + qt % sig;
-  }
-  if (s0 < 0 || s1 < s0 || (long long)s1 > p.slot_capacity) {
-    if (report) record_status(p.control, -7, kSitePlanRange + 1);
-    return m;
-  }
-  const int b = m.bh / p.H, h = m.bh % p.H;
-  m.n = s1 - s0;
-  m.s0 = s0;
-  m.kvrow0 = (b * p.Hkv + h / p.g) * p.Nk;
-  return m;
-}
-
-// Shared-memory views common to all roles.
-template <int D>
-struct Smem {
-  using C = Cfg<D>;
-  uint32_t base;
-  __device__ __forceinline__ uint32_t bar(int i) const { return base + C::kOffBar + 8u * (uint32_t)i; }
-  __device__ __forceinline__ uint32_t q(int qb) const { return base + C::kOffQ + qb * C::kTileBytes; }
-  __device__ __forceinline__ uint32_t kst(int s) const { return base + C::kOffK + s * C::kTileBytes; }
-  __device__ __forceinline__ uint32_t vst(int s) const { return base + C::kOffV + s * C::kTileBytes; }
-};
-
-// The work-item ring: the K producer decodes each schedule entry once (its
-// global loads run ahead of everyone else) and publishes the whole item, 8
-// words, so that no other role touches global memory at a row start.
-template <int D>
-__device__ __forceinline__ void sched_publish(uint8_t* smem, int slot, const Item& m) {
-  volatile int* e = reinterpret_cast<volatile int*>(smem + Cfg<D>::kOffSched) + slot * 8;
-  e[0] = m.it;
-  e[1] = m.n;
-  e[2] = m.s0;
-  e[3] = m.bh;
-  e[4] = (m.qx << 6) | (m.split ? 32 : 0) | m.qs;
-  e[5] = m.kvrow0;
-  e[6] = m.valid ? m.row : -1;
-  e[7] = __float_as_int(m.kb);
-}
-
-// Consumer side: wait for entry t, read it, release it (`lane_arrives`: this
-// thread releases the entry).  it = -2 when the wait gave up.
-template <int D>
-__device__ __forceinline__ Item sched_take(const Smem<D>& sm, const uint8_t* smem, uint32_t t,
-                                           bool lane_arrives, bool warp_sync, const Watchdog& wd) {
-  using C = Cfg<D>;
-  Item m{0, 0, 0, 0, 1, 0, false, 0, -2, 0.f, false};
-  const int slot = (int)(t % kSchedSlots);
-  bool ok = mbar_wait(sm.bar(C::kBarSchedFull + slot), (t / kSchedSlots) & 1u, wd, kSiteSched);
-  if (warp_sync) ok = __all_sync(0xffffffffu, ok);
-  if (!ok) return m;
-  const volatile int* e = reinterpret_cast<const volatile int*>(smem + C::kOffSched) + slot * 8;
-  m.it = e[0];
-  m.n = e[1];
-  m.s0 = e[2];
-  m.bh = e[3];
-  m.qx = e[4] >> 6;
-  m.split = (e[4] & 32) != 0;
-  m.qs = e[4] & 31;
-  m.kvrow0 = e[5];
-  const int row = e[6];
-  m.valid = row >= 0;
-  m.row = m.valid ? row : 0;
-  m.kb = __int_as_float(e[7]);
-  if (warp_sync) __syncwarp();
-  if (lane_arrives) mbar_arrive(sm.bar(C::kBarSchedEmpty + slot));
-  return m;
-}
-
-// Bounded wait used during teardown: ignores the abort flag, short limit.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const Watchdog& wd) {
-  volatile int no_abort = 0;
-  Watchdog quick{&no_abort, wd.status, wd.detail, 100000000ll};
-  mbar_wait(bar, parity, quick, kSiteDrain);
-}
-
-// ------------------------------------------------------------------ producers
-// K/V units of one slot as the plan lists them (rk <= 4 entries, -1 = padding)
-// or, for paged K/V, their pool rows as the row-bound pass resolved them.  A
-// producer reads them two slots ahead, so the global-load latency overlaps
-// its stage waits instead of sitting between a stage freeing and its copy
-// (a block-table lookup there, dependent on the plan entry, cost the paged
-// path about 40 %).
-struct SlotKeys {
-  int y[4];
-};
-template <bool kGeneral>
-__device__ __forceinline__ SlotKeys fetch_keys(const FwdParams& p, const Item& m, int j) {
-  SlotKeys k;
-  const int32_t* ent = ((kGeneral && p.prow) ? p.prow : p.slot_ku) + (size_t)(m.s0 + j) * p.rk;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) k.y[u] = (u < p.rk) ? __ldg(ent + u) : -1;
-  return k;
-}
-
-// One ring of tile stages with a single producer and a single consumer.
-struct Ring {
-  uint32_t data;   // shared address of stage 0
-  uint32_t full;   // barrier of stage 0 (stage s at +8 s)
-  uint32_t empty;
-  int stages;
-};
-
-// Gather the 128 keys of one slot into the next stage of `r`.
-template <int D, bool kGeneral>
-__device__ __forceinline__ bool load_tile(const FwdParams& p, const CUtensorMap* map, const Ring& r,
-                                          const Item& m, const SlotKeys& keys, uint32_t& it,
-                                          uint64_t pol, const Watchdog& wd) {
-  using C = Cfg<D>;
-  const uint32_t stage = it % (uint32_t)r.stages;
-  const uint32_t ph = (it / (uint32_t)r.stages) & 1u;
-  if (!mbar_wait(r.empty + 8u * stage, ph ^ 1u, wd, kSiteKvEmpty)) return false;
-  const uint32_t full = r.full + 8u * stage;
-  mbar_arrive_expect_tx(full, C::kTileBytes);
-  const bool paged = kGeneral && p.prow != nullptr;  // keys are pool rows
-  int first = keys.y[0];
-  if (first < 0 || (!paged && first >= p.NKU)) {
-    record_status(p.control, -7, kSitePlanRange + 2);
-    first = 0;
-  }
-  const uint32_t dst0 = r.data + stage * (uint32_t)C::kTileBytes;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    if (u >= p.rk) break;
-    int y = keys.y[u];
-    if (y < 0) {
-      y = first;  // padding position: load real rows, the sub-mask hides them
-    } else if (!paged && y >= p.NKU) {
-      record_status(p.control, -7, kSitePlanRange + 3);
-      y = first;
-    }
-    const int row = paged ? y : m.kvrow0 + y * p.ku;
-#pragma unroll
-    for (int c = 0; c < C::kChunks; ++c)
-      tma_load_2d(dst0 + c * C::kChunkBytes + u * p.ku * 128, map, c * 64, row, full, pol);
-  }
-  ++it;
-  return true;
-}
-
-// K producer (kside): takes work items from the global counter, publishes
-// them, loads each row's Q tile and the K tile of every slot.  V producer:
-// reads the published items and loads the V tile of every slot.  Both load in
-// slot order, which is the order the MMA thread consumes each ring in.
-template <int D, bool kGeneral>
-__device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, const Smem<D> sm,
-                                           const Watchdog wd, bool kside) {
-  using C = Cfg<D>;
-  const CUtensorMap* map = kside ? &p.tmK : &p.tmV;
-  if (kside) {
-    tma_prefetch_desc(&p.tmQ);
-    tma_prefetch_desc(&p.tmQu);
-  }
-  tma_prefetch_desc(map);
-  const uint64_t pol_q = policy_evict_first();
-  const uint64_t pol_kv = policy_evict_last();
-  const Ring r = kside ? Ring{sm.kst(0), sm.bar(C::kBarKFull), sm.bar(C::kBarKEmpty), C::kStagesK}
-                       : Ring{sm.vst(0), sm.bar(C::kBarVFull), sm.bar(C::kBarVEmpty), C::kStagesV};
-  uint32_t q_it = 0, kv_it = 0;
-  bool ok = true;
-  const int nwork =
-      p.work_count ? *reinterpret_cast<const volatile int32_t*>(p.work_count) : p.rows;
-  for (uint32_t t = 0; ok; ++t) {
-    Item m;
-    if (kside) {
-      const int slot = (int)(t % kSchedSlots);
-      if (!mbar_wait(sm.bar(C::kBarSchedEmpty + slot), ((t / kSchedSlots) & 1u) ^ 1u, wd,
-                     kSiteSched))
-        break;
-      int it = atomicAdd(p.work_counter, 1);
-      if (it >= nwork) it = -1;
-      if (it >= 0) {
-        m = load_item(p, it, true);
-        if (m.n > 0) {
-          m.kb = __ldg(p.rowk + m.row);
-          m.split = p.split_all || __ldg(p.rowv + m.row) > kSplitV;
-        }
-      } else {
-        m = Item{0, 0, 0, 0, 1, 0, false, 0, -1, 0.f, false};
-      }
-      sched_publish<D>(smem, slot, m);
-      mbar_arrive(sm.bar(C::kBarSchedFull + slot));
-    } else {
-      m = sched_take<D>(sm, smem, t, true, false, wd);
-    }
-    if (m.it < 0) break;
-    if (m.n == 0) continue;
-    if (kside) {
-      const int qb = q_buf<D>(q_it);
-      if (!mbar_wait(sm.bar(C::kBarQEmpty + qb), q_par<D>(q_it) ^ 1u, wd, kSiteQEmpty)) break;
-      mbar_arrive_expect_tx(sm.bar(C::kBarQFull + qb), C::kTileBytes);
-      if (m.qs == 1) {  // the tile's q-units are contiguous: one 128-row box
-        const int qrow = m.bh * p.Nq + m.qx * p.qu;
-#pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_2d(sm.q(qb) + c * C::kChunkBytes, &p.tmQ, c * 64, qrow,
-                      sm.bar(C::kBarQFull + qb), pol_q);
-      } else {  // q-unit i (qu rows) into tile rows [i*qu, (i+1)*qu)
-        for (int i = 0; i < p.rq; ++i) {
-          const int qrow = m.bh * p.Nq + (m.qx + i * m.qs) * p.qu;
-#pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_2d(sm.q(qb) + c * C::kChunkBytes + i * p.qu * 128, &p.tmQu, c * 64, qrow,
-                        sm.bar(C::kBarQFull + qb), pol_q);
-        }
-      }
-      ++q_it;
-    }
-    SlotKeys k0 = fetch_keys<kGeneral>(p, m, 0), k1 = k0;
-    if (m.n > 1) k1 = fetch_keys<kGeneral>(p, m, 1);
-    for (int j = 0; j < m.n && ok; ++j) {
-      SlotKeys k2 = k1;
-      if (j + 2 < m.n) k2 = fetch_keys<kGeneral>(p, m, j + 2);
-      ok = load_tile<D, kGeneral>(p, map, r, m, k0, kv_it, pol_kv, wd);
-      k0 = k1;
-      k1 = k2;
-    }
-  }
-  if (*wd.abort_flag) {
-    // Let copies already issued land before the CTA's shared memory goes away.
-    const uint32_t nst = (uint32_t)r.stages;
-    const uint32_t nk = kv_it < nst ? kv_it : nst;
-    for (uint32_t t = kv_it - nk; t < kv_it; ++t)
-      drain_wait(r.full + 8u * (t % nst), (t / nst) & 1u, wd);
-    if (kside) {
-      const uint32_t nq = q_it < (uint32_t)C::kQBufs ? q_it : (uint32_t)C::kQBufs;
-      for (uint32_t t = q_it - nq; t < q_it; ++t)
-        drain_wait(sm.bar(C::kBarQFull + q_buf<D>(t)), q_par<D>(t), wd);
-    }
-  }
-}
-
 // ------------------------------------------------------------------ MMA issuer
 // Descriptors are built once; per instruction only a compile-time offset is
 // added (the start-address field is the low 14 bits of the descriptor and
@@ -444,7 +148,7 @@ struct MmaState {
 // instructions), once that buffer's previous tile has been read out (by the
 // softmax, or for split weights by that slot's P V).
 template <int D>
-__device__ __forceinline__ bool issue_s(const Smem<D>& sm, MmaState<D>& st, uint32_t tmem, int qb,
+__device__ __forceinline__ bool issue_s(const Smem<Cfg<D>>& sm, MmaState<D>& st, uint32_t tmem, int qb,
                                         const Watchdog& wd) {
   using C = Cfg<D>;
   constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
@@ -497,7 +201,7 @@ __device__ __forceinline__ void issue_pv(MmaState<D>& st, uint32_t tmem, uint32_
 // S issuer: S of every slot, in slot order, as soon as its S buffer has been
 // read out (two slots back) and its K tile has landed.
 template <int D>
-__device__ __noinline__ void s_issuer_role(const FwdParams& p, const uint8_t* smem, const Smem<D> sm,
+__device__ __noinline__ void s_issuer_role(const FwdParams& p, const uint8_t* smem, const Smem<Cfg<D>> sm,
                                            uint32_t tmem, const Watchdog wd) {
   using C = Cfg<D>;
   MmaState<D> st;
@@ -507,11 +211,11 @@ __device__ __noinline__ void s_issuer_role(const FwdParams& p, const uint8_t* sm
   uint32_t q_it = 0;
   bool ok = true;
   for (uint32_t t = 0; ok; ++t) {
-    const Item m = sched_take<D>(sm, smem, t, true, false, wd);
+    const Item m = sched_take<Cfg<D>>(sm, smem, t, true, false, wd);
     if (m.it < 0) break;
     if (m.n == 0) continue;
-    const int qb = q_buf<D>(q_it);
-    if (!mbar_wait(sm.bar(C::kBarQFull + qb), q_par<D>(q_it), wd, kSiteQFull)) break;
+    const int qb = q_buf<Cfg<D>>(q_it);
+    if (!mbar_wait(sm.bar(C::kBarQFull + qb), q_par<Cfg<D>>(q_it), wd, kSiteQFull)) break;
     tc_fence_after();
     for (int j = 0; j < m.n && ok; ++j) ok = issue_s<D>(sm, st, tmem, qb, wd);
     if (ok) mma_commit(sm.bar(C::kBarQEmpty + qb));  // Q is free once the row's S MMAs are done
@@ -526,7 +230,7 @@ __device__ __noinline__ void s_issuer_role(const FwdParams& p, const uint8_t* sm
 // epilogue has read O out.  Runs in its own warp so that its waits and
 // commits never leave the tensor pipe without queued S work.
 template <int D>
-__device__ __noinline__ void pv_issuer_role(const FwdParams& p, const uint8_t* smem, const Smem<D> sm,
+__device__ __noinline__ void pv_issuer_role(const FwdParams& p, const uint8_t* smem, const Smem<Cfg<D>> sm,
                                             uint32_t tmem, const Watchdog wd) {
   using C = Cfg<D>;
   MmaState<D> st;
@@ -534,7 +238,7 @@ __device__ __noinline__ void pv_issuer_role(const FwdParams& p, const uint8_t* s
   uint32_t rows = 0;
   bool ok = true;
   for (uint32_t t = 0; ok; ++t) {
-    const Item m = sched_take<D>(sm, smem, t, true, false, wd);
+    const Item m = sched_take<Cfg<D>>(sm, smem, t, true, false, wd);
     if (m.it < 0) break;
     const int n = m.n;
     if (n == 0) continue;
@@ -586,7 +290,7 @@ __device__ __noinline__ void pv_issuer_role(const FwdParams& p, const uint8_t* s
 // Exact pass (kExact = true): the running row maximum, agreed between the
 // two threads of a row, with a lazy rescale of O.
 template <int D, bool kExact, bool kGeneral>
-__device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, const Smem<D>& sm,
+__device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, const Smem<Cfg<D>>& sm,
                                              uint32_t tmem, const Watchdog& wd) {
   using C = Cfg<D>;
   const int warp = threadIdx.x / 32;
@@ -763,7 +467,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   // The slot's weights of this thread as bf16 pairs into its P columns (and,
   // split, the low-order terms 32 columns on); sum_w as exp_pack.
   for (uint32_t t = 0;; ++t) {
-    const Item m = sched_take<D>(sm, smem, t, lane == 0, true, wd);
+    const Item m = sched_take<Cfg<D>>(sm, smem, t, lane == 0, true, wd);
     if (m.it < 0) break;
     if (!m.valid) continue;
     // Query position of this thread's row: q-unit qi of the tile is q-unit
@@ -779,8 +483,8 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     }
     // The row's Q tile: (bounded pass) this row's query norm; then release
     // it (with the S issuer's commit, the buffer can be refilled).
-    const int qb = q_buf<D>(q_it);
-    if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarQFull + qb), q_par<D>(q_it), wd, kSiteQFull)))
+    const int qb = q_buf<Cfg<D>>(q_it);
+    if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarQFull + qb), q_par<Cfg<D>>(q_it), wd, kSiteQFull)))
       break;
     float m_ref = -INFINITY;
     if constexpr (!kExact) {
@@ -1027,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const Smem<D> sm{smem_u32(smem)};
+  const Smem<Cfg<D>> sm{smem_u32(smem)};
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   const Watchdog wd{abort_flag, p.control + kCtlStatus, p.control + kCtlDetail, p.watchdog_ns};
@@ -1081,10 +785,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
   } else {
     regs_dec<kRegsControl>();
     if (lane == 0 && !*abort_flag) {
-      if (warp == 0) producer_role<D, kGeneral>(p, smem, sm, wd, true);
+      if (warp == 0) producer_role<Cfg<D>, kGeneral>(p, smem, sm, wd, true);
       else if (warp == 1) s_issuer_role<D>(p, smem, sm, tmem, wd);
       else if (warp == 2) pv_issuer_role<D>(p, smem, sm, tmem, wd);
-      else if (warp == 3) producer_role<D, kGeneral>(p, smem, sm, wd, false);
+      else if (warp == 3) producer_role<Cfg<D>, kGeneral>(p, smem, sm, wd, false);
     }
   }
 
@@ -1352,11 +1056,15 @@ cudaError_t launch_passes(const FwdParams& p, int grid, cudaStream_t stream, int
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  // Plans with 64-row q-tiles run the kernels of bsa_forward_q64.cu (plain
+  // path only; the host rejects pages and element masks for them).
+  const bool q64 = p.qu * p.rq == 64;
   if (stages & BSA_STAGE_BOUNDED) {
     FwdParams a = p;
     a.work_counter = p.control + kCtlWorkCounter;
     a.work_count = nullptr;
-    e = general ? launch_d<D, false, true>(a, grid, stream) : launch_d<D, false, false>(a, grid, stream);
+    e = q64 ? launch_forward_q64(a, D, grid, stream, false)
+            : general ? launch_d<D, false, true>(a, grid, stream) : launch_d<D, false, false>(a, grid, stream);
     if (e != cudaSuccess) return e;
   }
   if (stages & BSA_STAGE_EXACT) {
@@ -1365,7 +1073,8 @@ cudaError_t launch_passes(const FwdParams& p, int grid, cudaStream_t stream, int
     x.order = p.fb_list;
     x.work_counter = p.control + kCtlFallbackWork;
     x.work_count = p.control + kCtlFallbackCount;
-    e = general ? launch_d<D, true, true>(x, grid, stream) : launch_d<D, true, false>(x, grid, stream);
+    e = q64 ? launch_forward_q64(x, D, grid, stream, true)
+            : general ? launch_d<D, true, true>(x, grid, stream) : launch_d<D, true, false>(x, grid, stream);
   }
   return e;
 }

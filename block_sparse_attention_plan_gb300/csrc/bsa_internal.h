@@ -174,6 +174,9 @@ cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream);
 cudaError_t launch_forward(const FwdParams& p, int d, int grid, cudaStream_t stream,
                            int stages = BSA_STAGE_ALL);
 int forward_smem_bytes(int d);
+// Bounded (exact = false) or exact pass of a plan with 64-row q-tiles
+// (bsa_forward_q64.cu); launched by launch_forward for such plans.
+cudaError_t launch_forward_q64(const FwdParams& p, int d, int grid, cudaStream_t stream, bool exact);
 // Forward parameters and grid of one plan for the given tensors (bsa_api.cu).
 bsa_status make_fwd_params(const bsa_plan_layout& L, const PlanDev& pd, uint8_t* ws, bool remapped,
                            const void* Q, const void* K, const void* V, const bsa_kv_pages* pages,

@@ -84,7 +84,7 @@ typedef struct bsa_plan_layout {
   /* mapping: qu = rows per q-unit, rq = q-units per 128-row q-tile,
    * sq = q-units per logical q-block; ku, rk, sk likewise for keys */
   int32_t qu, rq, sq, ku, rk, sk;
-  int32_t NQT;          /* q-tiles per head  = Nq / 128 */
+  int32_t NQT;          /* q-tiles per head  = Nq / (qu * rq): 128-row tiles, or 64 with BSA_PLAN_Q64 */
   int32_t NKU;          /* k-units per head  = Nk / ku */
   int32_t rows;         /* plan rows R = B*H*NQT */
   int32_t urows;        /* union rows = B*Hkv*NQT when gqa_group > 1, else 0 */
@@ -118,6 +118,18 @@ typedef struct bsa_plan_layout {
  * gqa_group == 1 and the plane has at most 8192 q-tiles; otherwise (and
  * without the flag) every stride is 1.  One extra kernel launch. */
 #define BSA_PLAN_REMAP 0x2
+/* 64-row q-tiles, for query blocks of at most 64 rows (bq in {32, 64};
+ * BSA_ERR_UNSUPPORTED otherwise): a 64-row query block is a q-tile of its own
+ * and two 32-row blocks share one, instead of two (four) blocks sharing a
+ * 128-row tile and the union of their selections -- a second physical mapping
+ * of small blocks ("Decoupling Logical Masks from GPU Execution for Dynamic
+ * Block-Sparse Attention" (Tessera), abstract: logical blocks are combined
+ * into physical tiles).  Nq must then be a multiple of 64.  bsa_forward runs
+ * such plans with a kernel that puts the 128 keys of a slot on the MMA's M
+ * dimension and the tile's 64 queries on N (contiguous K/V, no element mask:
+ * bsa_forward_ex returns BSA_ERR_UNSUPPORTED for pages, key lengths or
+ * causality on these plans). */
+#define BSA_PLAN_Q64 0x4
 
 /*
  * bsa_plan_layout_query -- sizes and workspace layout for a plan.

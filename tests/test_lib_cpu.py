@@ -109,8 +109,14 @@ def test_plan_flags_and_layout_independent_of_remap(bsa):
     L1 = bsa.plan_layout(2, 16, 256, 256, 32, 32, 1, bsa.PLAN_REMAP)
     assert L0.as_dict() == L1.as_dict()  # regrouping needs no extra workspace
     with pytest.raises(bsa.BsaError) as e:
-        bsa.plan_layout(2, 16, 256, 256, 32, 32, 1, 0x4)  # unknown flag
+        bsa.plan_layout(2, 16, 256, 256, 32, 32, 1, 0x8)  # unknown flag
     assert e.value.status == -1
+    # 64-row q-tiles: twice the q-tiles (plan rows); two 32-row blocks per tile
+    L2 = bsa.plan_layout(2, 16, 256, 256, 32, 32, 1, bsa.PLAN_Q64)
+    assert (L2.NQT, L2.rq, L2.qu, L2.rows) == (2 * L0.NQT, 2, 32, 2 * L0.rows)
+    with pytest.raises(bsa.BsaError) as e:
+        bsa.plan_layout(2, 16, 64, 64, 128, 32, 1, bsa.PLAN_Q64)  # blocks of more than 64 rows
+    assert e.value.status == -2
 
 
 def test_host_pipeline_buffer_sizes(bsa):
