@@ -133,6 +133,24 @@ bool encode_map(CUtensorMap* m, const void* base, uint64_t rows, int d, int box_
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// d = 128 bf16 rows viewed as (64 columns, rows, 2 halves): strides 2 bytes,
+// 256 bytes (next row), 128 bytes (second half of the row); box
+// {64, box_rows, 2}.  A box lands in shared memory as box_rows rows of the
+// first half, then box_rows rows of the second, each 128-byte-swizzled: the
+// layout two {64, box_rows} boxes of the 2D view give.  Returns false if the
+// driver does not take the view (the caller then uses the 2D one).
+bool encode_map_halves(CUtensorMap* m, const void* base, uint64_t rows, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64u, (cuuint64_t)rows, 2u};
+  cuuint64_t strides[2] = {256u, 128u};
+  cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 2u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 long long env_ll(const char* name, long long dflt) {
   const char* s = std::getenv(name);
   if (!s || !*s) return dflt;
@@ -179,6 +197,11 @@ bsa_status make_fwd_params(const bsa_plan_layout& L, const PlanDev& pd, uint8_t*
       !encode_map(&fp.tmK, K, (uint64_t)kvrows, d, L.ku) ||
       !encode_map(&fp.tmV, V, (uint64_t)kvrows, d, L.ku))
     return BSA_ERR_CUDA;
+  if (d == 128) {
+    fp.q_box3 = encode_map_halves(&fp.tmQ3, Q, (uint64_t)qrows, L.qu * L.rq) ? 1 : 0;
+    fp.kv_box3 = (L.rk == 1 && encode_map_halves(&fp.tmK3, K, (uint64_t)kvrows, kTile) &&
+                  encode_map_halves(&fp.tmV3, V, (uint64_t)kvrows, kTile)) ? 1 : 0;
+  }
   fp.row_ptr = pd.row_ptr;
   fp.slot_ku = pd.slot_ku;
   fp.slot_mask = pd.slot_mask;

@@ -206,6 +206,14 @@ __device__ __forceinline__ bool load_tile(const FwdParams& p, const CUtensorMap*
     first = 0;
   }
   const uint32_t dst0 = r.data + stage * (uint32_t)C::kTileBytes;
+  if (C::kChunks == 2 && p.kv_box3) {  // one 128-key unit: both halves in one box
+    int y = keys.y[0];
+    if (y < 0 || (!paged && y >= p.NKU)) y = first;
+    const int row = paged ? y : m.kvrow0 + y * p.ku;
+    tma_load_3d(dst0, map, 0, row, 0, full, pol);
+    ++it;
+    return true;
+  }
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
     if (u >= p.rk) break;
@@ -233,9 +241,10 @@ __device__ __forceinline__ bool load_tile(const FwdParams& p, const CUtensorMap*
 template <class C, bool kGeneral>
 __device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, const Smem<C> sm,
                                            const Watchdog wd, bool kside) {
-  const CUtensorMap* map = kside ? &p.tmK : &p.tmV;
+  const CUtensorMap* map = (C::kChunks == 2 && p.kv_box3) ? (kside ? &p.tmK3 : &p.tmV3)
+                                                          : (kside ? &p.tmK : &p.tmV);
   if (kside) {
-    tma_prefetch_desc(&p.tmQ);
+    tma_prefetch_desc((C::kChunks == 2 && p.q_box3) ? &p.tmQ3 : &p.tmQ);
     tma_prefetch_desc(&p.tmQu);
   }
   tma_prefetch_desc(map);
@@ -286,10 +295,14 @@ __device__ __noinline__ void producer_role(const FwdParams& p, uint8_t* smem, co
       mbar_arrive_expect_tx(sm.bar(C::kBarQFull + qb), C::kQBytes);
       if (m.qs == 1) {  // the tile's q-units are contiguous: one box of the tile's rows
         const int qrow = m.bh * p.Nq + m.qx * p.qu;
+        if (C::kChunks == 2 && p.q_box3) {
+          tma_load_3d(sm.q(qb), &p.tmQ3, 0, qrow, 0, sm.bar(C::kBarQFull + qb), pol_q);
+        } else {
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_2d(sm.q(qb) + c * C::kQChunkBytes, &p.tmQ, c * 64, qrow,
-                      sm.bar(C::kBarQFull + qb), pol_q);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_2d(sm.q(qb) + c * C::kQChunkBytes, &p.tmQ, c * 64, qrow,
+                        sm.bar(C::kBarQFull + qb), pol_q);
+        }
       } else {  // q-unit i (qu rows) into tile rows [i*qu, (i+1)*qu)
         for (int i = 0; i < p.rq; ++i) {
           const int qrow = m.bh * p.Nq + (m.qx + i * m.qs) * p.qu;

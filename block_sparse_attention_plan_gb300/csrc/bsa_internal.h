@@ -127,6 +127,15 @@ struct FwdParams {
   CUtensorMap tmK;   // K viewed as [B*Hkv*Nk, d], box {64, ku}
   CUtensorMap tmV;   // V likewise
   CUtensorMap tmQu;  // Q viewed as [B*Hq*Nq, d], box {64, qu}: one q-unit (regrouped tiles)
+  // d = 128: the same tensors viewed in 3D as (64 columns, rows, 2 halves of
+  // a row), so that one box brings both 64-column halves of a tile, laid out
+  // in shared memory half after half as the MMA reads them (two 2D boxes
+  // otherwise).  Used when kv_box3 / q_box3 are set.
+  CUtensorMap tmQ3;  // box {64, q-tile rows, 2}
+  CUtensorMap tmK3;  // box {64, 128, 2} (slots of one 128-key unit)
+  CUtensorMap tmV3;
+  int q_box3;        // the contiguous Q tile is loaded through tmQ3
+  int kv_box3;       // K/V slots (one unit each) are loaded through tmK3 / tmV3
   const int32_t* row_ptr;
   const int32_t* slot_ku;
   const uint32_t* slot_mask;
