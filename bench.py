@@ -260,7 +260,7 @@ class _Case:
     the hot path (plan, then forward) for it."""
 
     def __init__(self, bsa, W, w, dev, stream, remap=False, page_size=0, causal=False,
-                 affine=False):
+                 affine=False, flags=None):
         self.bsa, self.w, self.dev, self.stream = bsa, w, dev, stream
         self.mask_d = w.mask.to(dev)
         q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
@@ -285,10 +285,12 @@ class _Case:
         self.q, self.k, self.v = q, k, v
         self.o = torch.empty_like(q)
         self.lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
-        L = bsa.plan_layout(*w.mask.shape, w.bq, w.bk, w.gqa_group)
+        self.plan_flags = (bsa.PLAN_REMAP if remap else 0) if flags is None else int(flags)
+        L = bsa.plan_layout(*w.mask.shape, w.bq, w.bk, w.gqa_group, self.plan_flags)
         self.wsbuf = torch.empty(int(L.workspace_bytes), dtype=torch.uint8, device=dev)
-        self.plan_flags = bsa.PLAN_REMAP if remap else 0
-        self.remap_active = bool(remap and w.bq < 128 and w.gqa_group == 1 and w.Nq // 128 <= 8192)
+        self.tile_rows = L.qu * L.rq
+        self.remap_active = bool((self.plan_flags & bsa.PLAN_REMAP) and L.rq > 1 and w.gqa_group == 1
+                                 and L.NQT <= 8192)
         self.affine = None
         if affine:
             # sliding, strided and dilated heads as affine row segments, the
@@ -381,7 +383,7 @@ class _Case:
         Lp = self.p.layout
         plan_bytes = (w.mask.numel() + 4 * (Lp.rows + 1) + 4 * S_ * Lp.rk + 4 * S_ + 4 * Lp.rows
                       + 4 * (Lp.urows + 1) + 4 * U_)
-        computed = 4.0 * 128 * 128 * w.d * S_
+        computed = 4.0 * self.tile_rows * 128 * w.d * S_
         return plan_bytes, computed, computed / w.active_flop
 
     def free(self):
@@ -436,6 +438,32 @@ def per_config_entry(bsa, W, name, dev, stream, clocks, peak, target_s=0.5):
     return e
 
 
+def _e2e(bsa, w, args, ws, dev, barrier):
+    """End to end through the public API: host (pinned) buffers, the copies
+    in the timed region (bsa.attention -> bsa_attention_host)."""
+    mask_h = w.mask.pin_memory()
+    q_h, k_h, v_h = w.q.pin_memory(), w.k.pin_memory(), w.v.pin_memory()
+    n_e2e = max(2, min(args.steps, args.e2e_steps))
+    o_pin = torch.empty(w.q.shape, dtype=w.q.dtype, pin_memory=True)
+    l_pin = torch.empty(w.q.shape[:3], dtype=torch.float32, pin_memory=True)
+    bsa.attention(mask_h, q_h, k_h, v_h, w.bq, w.bk, out=o_pin, lse_out=l_pin)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        oh, lh = bsa.attention(mask_h, q_h, k_h, v_h, w.bq, w.bk, out=o_pin, lse_out=l_pin)
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+    (e2e_ms,) = max_over_ranks([e2e_ms], dev)
+    h2d = mask_h.numel() + (q_h.numel() + k_h.numel() + v_h.numel()) * 2
+    d2h = oh.numel() * 2 + lh.numel() * 4
+    del mask_h, q_h, k_h, v_h, o_pin, l_pin, oh, lh
+    bsa._lib._host_buffers.clear()
+    torch.cuda.empty_cache()
+    return {"value": whole_job_tflops(w.active_flop, e2e_ms, ws), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
+
+
 def run_gb300(args):
     ws, rank, local = _dist()
     import block_sparse_attention_plan_gb300 as bsa
@@ -466,7 +494,7 @@ def run_gb300(args):
     stream = torch.cuda.current_stream()
 
     c = _Case(bsa, W, w, dev, stream, remap=args.remap, page_size=args.page_size,
-              causal=args.causal, affine=args.affine)
+              causal=args.causal, affine=args.affine, flags=args.plan_flags)
     flop = w.active_flop
 
     def barrier():
@@ -489,27 +517,9 @@ def run_gb300(args):
     clk = clocks.summary(t_wall0, t_wall1)
     launches = c.launches_per_step * args.steps
     c.free()
-
-    # end to end through the public API, host (pinned) buffers, copies timed
-    mask_h = w.mask.pin_memory()
-    q_h, k_h, v_h = w.q.pin_memory(), w.k.pin_memory(), w.v.pin_memory()
-    n_e2e = max(2, min(args.steps, args.e2e_steps))
-    o_pin = torch.empty(w.q.shape, dtype=w.q.dtype, pin_memory=True)
-    l_pin = torch.empty(w.q.shape[:3], dtype=torch.float32, pin_memory=True)
-    bsa.attention(mask_h, q_h, k_h, v_h, w.bq, w.bk, out=o_pin, lse_out=l_pin)
-    barrier()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(n_e2e):
-        oh, lh = bsa.attention(mask_h, q_h, k_h, v_h, w.bq, w.bk, out=o_pin, lse_out=l_pin)
-    torch.cuda.synchronize()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
-    (e2e_ms,) = max_over_ranks([e2e_ms], dev)
-    h2d = mask_h.numel() + (q_h.numel() + k_h.numel() + v_h.numel()) * 2
-    d2h = oh.numel() * 2 + lh.numel() * 4
-    del mask_h, q_h, k_h, v_h, o_pin, l_pin, oh, lh
-    bsa._lib._host_buffers.clear()
-    torch.cuda.empty_cache()
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e(bsa, w, args, ws, dev, barrier)
 
     per_config = None
     if rank == 0 and ws == 1 and not args.no_per_config:
@@ -554,8 +564,7 @@ def run_gb300(args):
                      "frac_of_sustained": achieved / peak_sus,
                      "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS,
                      "nominal_peak": NOMINAL_BF16_TFLOPS},
-        "e2e": {"value": whole_job_tflops(flop, e2e_ms, ws), "unit": UNIT,
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+        "e2e": e2e,
         "plan_ms": plan_ms,
         "plan": {"ms": plan_ms, "bytes": int(plan_bytes),
                  "gbs": plan_bytes / (plan_ms * 1e-3) / 1e9,
@@ -594,6 +603,10 @@ def main():
                     help="regular workload: plan from affine row segments (+ residual mask bytes)")
     ap.add_argument("--causal", action="store_true",
                     help="intra-block causal masking (queries are the last Nq positions)")
+    ap.add_argument("--plan-flags", type=int, default=None,
+                    help="plan flags (BSA_PLAN_*) for the timed step; overrides --remap")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end leg (sweeps of the device path only)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per_config record of the other workloads")
     ap.add_argument("--traffic", type=float, default=None,

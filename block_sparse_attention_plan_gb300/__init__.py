@@ -10,9 +10,10 @@ generators.
 from ._lib import (  # noqa: F401
     BsaError, Layout, Plan, PLAN_NO_UNION, PLAN_Q64, PLAN_REMAP, STAGE_ALL, STAGE_BOUNDED, STAGE_EXACT, STAGE_KNORM, STAGE_PREPARE,
     STAGE_ROWBOUND, attention, attention_static, attention_static_status, forward, library, plan, plan_affine,
-    plan_check, plan_layout, sync_status, watchdog_selftest,
+    plan_check, plan_layout, plan_workspace_bytes, select_flags, sync_status, watchdog_selftest,
 )
 
 __all__ = ["BsaError", "Layout", "Plan", "PLAN_NO_UNION", "PLAN_Q64", "PLAN_REMAP", "STAGE_ALL", "STAGE_BOUNDED",
            "STAGE_EXACT", "STAGE_KNORM", "STAGE_PREPARE", "STAGE_ROWBOUND", "attention", "attention_static", "attention_static_status", "forward", "library",
-           "plan", "plan_affine", "plan_check", "plan_layout", "sync_status", "watchdog_selftest"]
+           "plan", "plan_affine", "plan_check", "plan_layout", "plan_workspace_bytes", "select_flags", "sync_status",
+           "watchdog_selftest"]

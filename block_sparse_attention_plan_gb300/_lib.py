@@ -53,6 +53,17 @@ class Layout(ctypes.Structure):
         return {n: getattr(self, n) for n, _ in self._fields_}
 
 
+class PlanArraysC(ctypes.Structure):
+    """Mirror of ``bsa_plan_arrays`` (host buffers for bsa_plan_export)."""
+    _fields_ = []
+    for _n, _t in (("row_ptr", ctypes.c_void_p), ("slot_ku", ctypes.c_void_p),
+                   ("slot_mask", ctypes.c_void_p), ("urow_ptr", ctypes.c_void_p),
+                   ("ukb", ctypes.c_void_p), ("order", ctypes.c_void_p),
+                   ("plane_sigma", ctypes.c_void_p)):
+        _fields_ += [(_n, _t), (_n + "_cap", ctypes.c_size_t)]
+    _fields_ += [("totals", ctypes.c_int64 * 4)]
+
+
 _lib = None
 
 
@@ -75,6 +86,12 @@ def library() -> ctypes.CDLL:
     lib.bsa_plan_create.restype = I
     lib.bsa_plan_create.argtypes = [U8P, I, I, I, I, I, I, I, VP, ctypes.c_size_t, I, VP,
                                     ctypes.POINTER(P)]
+    lib.bsa_plan_select_flags.restype = I
+    lib.bsa_plan_select_flags.argtypes = [I, I, I, I, I, I, I, I]
+    lib.bsa_plan_workspace_bytes.restype = ctypes.c_size_t
+    lib.bsa_plan_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
+    lib.bsa_plan_export.restype = I
+    lib.bsa_plan_export.argtypes = [P, VP, ctypes.POINTER(PlanArraysC)]
     lib.bsa_plan_get_layout.restype = I
     lib.bsa_plan_get_layout.argtypes = [P, ctypes.POINTER(Layout)]
     lib.bsa_plan_workspace.restype = VP
@@ -118,6 +135,19 @@ def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
 def _check(status: int, what: str):
     if status != BSA_OK:
         raise BsaError(status, what)
+
+
+def select_flags(B: int, H: int, NQB: int, NKB: int, bq: int, bk: int, gqa_group: int, d: int) -> int:
+    """Plan flags chosen from the library's measured table (bsa_plan_select_flags)."""
+    f = int(library().bsa_plan_select_flags(B, H, NQB, NKB, bq, bk, gqa_group, d))
+    _check(min(f, 0), "bsa_plan_select_flags")
+    return f
+
+
+def plan_workspace_bytes(B: int, H: int, NQB: int, NKB: int, bq: int, bk: int,
+                         gqa_group: int = 1) -> int:
+    """Workspace bytes of a plan (bsa_plan_workspace_bytes; 0 for bad arguments)."""
+    return int(library().bsa_plan_workspace_bytes(B, H, NQB, NKB, bq, bk, gqa_group))
 
 
 def plan_layout(B: int, H: int, NQB: int, NKB: int, bq: int, bk: int, gqa_group: int = 1,
@@ -166,6 +196,28 @@ class Plan:
             "totals": totals,
             "plane_sigma": self._view(L.off_sigma, L.B * L.H, torch.int32),
         }
+
+    def export(self, stream: Optional[torch.cuda.Stream] = None) -> dict:
+        """Host copies of the plan arrays through bsa_plan_export (synchronises):
+        int32 numpy arrays (slot_mask as uint32) and the int64 totals."""
+        import numpy as np
+        L = self.layout
+        c = PlanArraysC()
+        _check(library().bsa_plan_export(self.handle, _stream_ptr(stream), ctypes.byref(c)),
+               "bsa_plan_export")
+        tot = np.array(list(c.totals), dtype=np.int64)
+        S, U = int(tot[0]), int(tot[2])
+        out = {"row_ptr": np.empty(L.rows + 1, np.int32), "slot_ku": np.empty(S * L.rk, np.int32),
+               "slot_mask": np.empty(S, np.uint32), "urow_ptr": np.empty(L.urows + 1, np.int32),
+               "ukb": np.empty(U, np.int32), "order": np.empty(L.rows, np.int32),
+               "plane_sigma": np.empty(L.B * L.H, np.int32)}
+        for k, a in out.items():
+            setattr(c, k, ctypes.c_void_p(a.ctypes.data))
+            setattr(c, k + "_cap", a.size)
+        _check(library().bsa_plan_export(self.handle, _stream_ptr(stream), ctypes.byref(c)),
+               "bsa_plan_export")
+        out["totals"] = tot
+        return out
 
     def control(self) -> torch.Tensor:
         return self._view(self.layout.off_control, 16, torch.int32)
@@ -347,12 +399,14 @@ def attention(mask: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Ten
     overlapping streams; pinned memory keeps the copies asynchronous), with a
     device scratch buffer cached per shape; O and LSE come back in pinned host
     tensors (or ``out`` / ``lse_out``).  Device tensors: plan + forward.
-    Plans regroup q-units where that saves tiles (PLAN_REMAP).
+    Device plans take the flags of the library's measured table
+    (bsa_plan_select_flags: q-tile height, regrouping).
     Returns (O, LSE) on the inputs' device."""
     host = not q.is_cuda
     g = q.shape[1] // k.shape[1]
     if not host:
-        pl = plan(mask, bq, bk, g, flags=PLAN_REMAP, stream=stream)
+        flags = select_flags(*mask.shape, bq, bk, g, q.shape[3])
+        pl = plan(mask, bq, bk, g, flags=flags, stream=stream)
         return forward(pl, q, k, v, scale=scale, stream=stream)
     B, H, NQB, NKB = mask.shape
     d = q.shape[3]

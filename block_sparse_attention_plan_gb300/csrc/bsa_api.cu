@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 
 #include "bsa_internal.h"
+#include "bsa_regime_table.h"
 
 using namespace bsa;
 
@@ -274,6 +275,31 @@ bsa_status bsa_plan_layout_query(int B, int H, int NQB, int NKB, int bq, int bk,
   return compute_layout(B, H, NQB, NKB, bq, bk, gqa_group, flags, out, nullptr);
 }
 
+int bsa_plan_select_flags(int B, int H, int NQB, int NKB, int bq, int bk, int gqa_group, int d) {
+  bsa_plan_layout L;
+  bsa_status st = compute_layout(B, H, NQB, NKB, bq, bk, gqa_group, 0, &L, nullptr);
+  if (st != BSA_OK) return st;
+  if (d != 64 && d != 128) return BSA_ERR_UNSUPPORTED;
+  int tile = kTile;
+  for (const RegimeEntry& e : kRegimeTable)
+    if (e.bq == bq && e.bk == bk && e.d == d) tile = e.tile;
+  int flags = 0;
+  bsa_plan_layout L64;
+  if (tile == 64 && compute_layout(B, H, NQB, NKB, bq, bk, gqa_group, BSA_PLAN_Q64, &L64, nullptr) == BSA_OK) {
+    flags |= BSA_PLAN_Q64;
+    if (L64.rq > 1 && gqa_group == 1) flags |= BSA_PLAN_REMAP;
+  } else if (L.rq > 1 && gqa_group == 1) {
+    flags |= BSA_PLAN_REMAP;
+  }
+  return flags;
+}
+
+size_t bsa_plan_workspace_bytes(int B, int H, int NQB, int NKB, int bq, int bk, int gqa_group) {
+  bsa_plan_layout L;
+  if (compute_layout(B, H, NQB, NKB, bq, bk, gqa_group, 0, &L, nullptr) != BSA_OK) return 0;
+  return (size_t)L.workspace_bytes;
+}
+
 namespace {
 
 // Plan of a logical mask given as mask bytes, affine row segments, or both
@@ -485,6 +511,41 @@ bsa_status bsa_plan_check(const bsa_plan* plan, void* stream) {
     const int r = order[i];
     if (r < 0 || r >= L.rows || seen[r]) return BSA_ERR_PLAN_MISMATCH;
     seen[r] = 1;
+  }
+  return BSA_OK;
+}
+
+bsa_status bsa_plan_export(const bsa_plan* plan, void* stream, bsa_plan_arrays* out) {
+  const PlanImpl* p = as_impl(plan);
+  if (!p || !out) return BSA_ERR_INVALID_ARG;
+  const bsa_plan_layout& L = p->L;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BSA_ERR_CUDA;
+  if (cudaMemcpy(out->totals, p->dev.totals, sizeof(out->totals), cudaMemcpyDeviceToHost) !=
+      cudaSuccess)
+    return BSA_ERR_CUDA;
+  const long long S = out->totals[0], U = out->totals[2];
+  if (S < 0 || S > L.slot_capacity || U < 0 || U > L.union_capacity) return BSA_ERR_PLAN_MISMATCH;
+  struct Copy {
+    void* dst;
+    size_t cap;
+    const void* src;
+    size_t n;  // elements (4 bytes each)
+  };
+  const Copy copies[] = {
+      {out->row_ptr, out->row_ptr_cap, p->dev.row_ptr, (size_t)L.rows + 1},
+      {out->slot_ku, out->slot_ku_cap, p->dev.slot_ku, (size_t)S * L.rk},
+      {out->slot_mask, out->slot_mask_cap, p->dev.slot_mask, (size_t)S},
+      {out->urow_ptr, out->urow_ptr_cap, p->dev.urow_ptr, (size_t)L.urows + 1},
+      {out->ukb, out->ukb_cap, p->dev.ukb, (size_t)U},
+      {out->order, out->order_cap, p->dev.order, (size_t)L.rows},
+      {out->plane_sigma, out->plane_sigma_cap, p->dev.sigma, (size_t)L.B * L.H},
+  };
+  for (const Copy& c : copies)
+    if (c.dst && c.cap < c.n) return BSA_ERR_WORKSPACE;
+  for (const Copy& c : copies) {
+    if (!c.dst || c.n == 0) continue;
+    if (cudaMemcpy(c.dst, c.src, 4 * c.n, cudaMemcpyDeviceToHost) != cudaSuccess) return BSA_ERR_CUDA;
   }
   return BSA_OK;
 }

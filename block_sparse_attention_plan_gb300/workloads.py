@@ -355,8 +355,39 @@ SMALL_CONFIGS = {
 }
 
 
+def sweep_mask(gen: torch.Generator, B: int, H: int, NQB: int, NKB: int, bq: int, bk: int,
+               density: float, skew: float) -> torch.Tensor:
+    """Mask family of the mapping sweep: every (b, h, q-block) row gets its
+    own density rho * (1 + skew * u), u ~ U(-1, 1) (clipped to [0.01, 1]),
+    and selects each key block independently with it (no correlation between
+    neighbouring q-blocks: the case where combining them costs most), plus
+    the key blocks covering the q-block's own token range, so that no row is
+    empty."""
+    u = torch.rand(B, H, NQB, 1, generator=gen) * 2.0 - 1.0
+    rho = (density * (1.0 + skew * u)).clamp(0.01, 1.0)
+    m = (torch.rand(B, H, NQB, NKB, generator=gen) < rho).to(torch.uint8)
+    for qb in range(NQB):
+        lo, hi = qb * bq // bk, ((qb + 1) * bq - 1) // bk
+        m[:, :, qb, lo:hi + 1] = 1
+    return m
+
+
+def _sweep(spec: str, data: bool, seed: int) -> Workload:
+    """``sweep:bq=64,bk=128,d=128,density=0.2,skew=0.5`` (defaults: B=1, H=16,
+    N=16384, density 0.2, skew 0)."""
+    kv = dict(x.split("=") for x in spec.split(":", 1)[1].split(",") if x)
+    bq, bk, d = int(kv.get("bq", 64)), int(kv.get("bk", 64)), int(kv.get("d", 128))
+    B, H, N = int(kv.get("B", 1)), int(kv.get("H", 16)), int(kv.get("N", 16384))
+    density, skew = float(kv.get("density", 0.2)), float(kv.get("skew", 0.0))
+    return _wl(spec, B, H, H, N, N, d, bq, bk,
+               lambda g: sweep_mask(g, B, H, N // bq, N // bk, bq, bk, density, skew), data, seed)
+
+
 def make_workload(name: str, seed: int = 0, data: bool = True) -> Workload:
-    """Build a named workload (``CONFIGS`` or ``SMALL_CONFIGS``)."""
+    """Build a named workload (``CONFIGS`` or ``SMALL_CONFIGS``), or one of the
+    mapping sweep (``sweep:...``, see ``_sweep``)."""
+    if name.startswith("sweep:"):
+        return _sweep(name, data, seed)
     fn = CONFIGS.get(name) or SMALL_CONFIGS.get(name)
     if fn is None:
         raise KeyError(f"unknown workload {name!r}")

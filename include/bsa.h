@@ -132,6 +132,21 @@ typedef struct bsa_plan_layout {
 #define BSA_PLAN_Q64 0x4
 
 /*
+ * bsa_plan_select_flags -- plan flags for a problem shape, chosen from a
+ * table of measured forward times compiled into the library (the
+ * profile-guided selection of a runtime configuration from offline
+ * profiles, "Decoupling Logical Masks from GPU Execution for Dynamic
+ * Block-Sparse Attention" (Tessera), abstract).  The table gives, per
+ * (bq, bk, d), the physical q-tile height (BSA_PLAN_Q64 or not) that was
+ * faster over a sweep of mask densities; BSA_PLAN_REMAP is added wherever
+ * tiles combine several q-units and gqa_group == 1 (its stride is chosen on
+ * the device from exact slot counts).  Depends on shapes only, never on the
+ * mask, so it needs no device access.  Nq = NQB * bq.  Returns the flags,
+ * or a negative bsa_status for shapes bsa_plan_layout_query rejects.
+ */
+int bsa_plan_select_flags(int B, int H, int NQB, int NKB, int bq, int bk, int gqa_group, int d);
+
+/*
  * bsa_plan_layout_query -- sizes and workspace layout for a plan.
  * Arguments: mask geometry B, H (query heads), NQB, NKB; logical block sizes
  * bq, bk in {32, 64, 128, 256}; gqa_group g >= 1 dividing H; flags as for
@@ -143,7 +158,24 @@ bsa_status bsa_plan_layout_query(int B, int H, int NQB, int NKB, int bq, int bk,
                                  int gqa_group, int flags, bsa_plan_layout* out);
 
 /*
- * bsa_plan_create -- build the plan of one logical mask on the GPU.
+ * bsa_plan_workspace_bytes -- device workspace bytes a plan of this geometry
+ * needs (bsa_plan_layout_query(..., flags = 0, ...).workspace_bytes: plan
+ * arrays, plan-construction scratch and the forward's scratch).  The same
+ * for BSA_PLAN_REMAP and BSA_PLAN_NO_UNION plans (an upper bound for the
+ * latter); plans with 64-row q-tiles (BSA_PLAN_Q64) have twice the rows:
+ * query bsa_plan_layout_query with that flag.  Returns 0 for arguments
+ * bsa_plan_layout_query rejects.  Touches no device.
+ */
+size_t bsa_plan_workspace_bytes(int B, int H, int NQB, int NKB, int bq, int bk, int gqa_group);
+
+/*
+ * bsa_plan_create -- build the plan of one logical mask on the GPU: the
+ * physical mapping layer (logical blocks retained, combined or subdivided
+ * into physical tiles) and the task organisation layer (tiles grouped per
+ * q-tile and scheduled) of "Decoupling Logical Masks from GPU Execution for
+ * Dynamic Block-Sparse Attention" (Tessera), abstract, plus the per-group
+ * union table of "CompactAttention: Accelerating Chunked Prefill with
+ * Block-Union KV Selection", summary.
  * mask: device, u8 [B][H][NQB][NKB]; any non-zero byte selects the block.
  * workspace: device, >= layout.workspace_bytes bytes, 256-byte aligned, owned
  * by the caller and reused by every bsa_forward on this plan (it also holds
@@ -199,7 +231,44 @@ void* bsa_plan_workspace(const bsa_plan* plan);
 void bsa_plan_destroy(bsa_plan* plan);
 
 /*
- * bsa_forward -- block-sparse attention forward over a plan.
+ * Host copies of a plan's arrays for bsa_plan_export.  Each pointer is a
+ * caller-owned HOST buffer of the given capacity in elements, or NULL to
+ * skip that array.  Lengths needed (element counts, see bsa_plan_layout):
+ *   row_ptr rows+1, slot_ku totals[0]*rk, slot_mask totals[0],
+ *   urow_ptr urows+1 (1 when there is no union table), ukb totals[2],
+ *   order rows, plane_sigma B*H.
+ */
+typedef struct bsa_plan_arrays {
+  int32_t* row_ptr;     size_t row_ptr_cap;
+  int32_t* slot_ku;     size_t slot_ku_cap;
+  uint32_t* slot_mask;  size_t slot_mask_cap;
+  int32_t* urow_ptr;    size_t urow_ptr_cap;
+  int32_t* ukb;         size_t ukb_cap;
+  int32_t* order;       size_t order_cap;
+  int32_t* plane_sigma; size_t plane_sigma_cap;
+  int64_t totals[4];    /* written: slots, selected logical blocks, union entries, 0 */
+} bsa_plan_arrays;
+
+/*
+ * bsa_plan_export -- synchronise `stream` (the plan's kernels must have been
+ * enqueued on it or before it), then copy the plan's totals and every
+ * requested array into the caller's host buffers.  For tests, inspection
+ * and handing a plan to other tools; the forward reads the plan on the
+ * device and never needs this.  Errors: BSA_ERR_INVALID_ARG (NULL/foreign
+ * plan or `out`), BSA_ERR_WORKSPACE (a buffer smaller than its array; the
+ * totals are written first, so the caller can size the buffers from them),
+ * BSA_ERR_CUDA.
+ */
+bsa_status bsa_plan_export(const bsa_plan* plan, void* stream, bsa_plan_arrays* out);
+
+/*
+ * bsa_forward -- block-sparse attention forward over a plan: attention over
+ * exactly the (query-block, key-block) pairs the plan's mask selects, every
+ * selected interaction preserved ("Decoupling Logical Masks from GPU
+ * Execution for Dynamic Block-Sparse Attention" (Tessera), abstract), with
+ * the online-softmax fusion of FlashAttention-style kernels ("Sol-Attn"
+ * summary) and the TMA + warp-specialised tile-skipping structure the
+ * "Veda" summary describes for Hopper, here on tcgen05 tensor cores.
  * Q: device bf16 [B][Hq][Nq][d]; K, V: device bf16 [B][Hkv][Nk][d];
  * O: device bf16 [B][Hq][Nq][d] (written); LSE: device fp32 [B][Hq][Nq]
  * (written; natural log, -inf for rows with no selected key).  All 16-byte

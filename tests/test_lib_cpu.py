@@ -175,3 +175,52 @@ def test_affine_stage_and_host_argument_errors_without_device(bsa_lib, bsa):
     assert bsa_lib.bsa_attention_host(*args, 2, VP(aligned + 16), n.value, None) == -1
     assert bsa_lib.bsa_attention_host(*args, 2, p, n.value - 1, None) == -5
     assert bsa_lib.bsa_attention_host(*args, 0, p, n.value, None) == -1
+
+
+def test_plan_workspace_bytes_matches_layout(bsa):
+    for geo in ((1, 24, 128, 128, 128, 128, 1), (1, 32, 64, 1024, 64, 64, 4), (2, 16, 256, 256, 32, 32, 1)):
+        assert bsa.plan_workspace_bytes(*geo) == bsa.plan_layout(*geo).workspace_bytes
+        assert bsa.plan_workspace_bytes(*geo) == bsa.plan_layout(*geo, bsa.PLAN_REMAP).workspace_bytes
+    assert bsa.plan_workspace_bytes(1, 1, 3, 4, 64, 64, 1) == 0     # Nq = 192
+    assert bsa.plan_workspace_bytes(1, 2, 4, 4, 48, 64, 1) == 0     # unsupported block
+
+
+def test_plan_export_argument_errors_without_device(bsa_lib):
+    from block_sparse_attention_plan_gb300 import _lib as L
+    c = L.PlanArraysC()
+    assert bsa_lib.bsa_plan_export(None, None, ctypes.byref(c)) == -1
+    fake = (ctypes.c_uint32 * 64)()
+    assert bsa_lib.bsa_plan_export(ctypes.c_void_p(ctypes.addressof(fake)), None, ctypes.byref(c)) == -1
+
+
+def test_plan_select_flags_from_table(bsa):
+    from block_sparse_attention_plan_gb300 import regime_sweep as RS
+    table = {}
+    for line in open(RS.TABLE_H):
+        m = re.match(r"\s*\{(\d+), (\d+), (\d+), (\d+)\},", line)
+        if m:
+            bq, bk, d, tile = map(int, m.groups())
+            table[(bq, bk, d)] = tile
+    for (bq, bk, d) in [(32, 32, 64), (64, 64, 128), (64, 128, 128), (32, 64, 64), (128, 128, 128)]:
+        for g in (1, 2):
+            f = bsa.select_flags(1, 4, 4096 // bq, 4096 // bk, bq, bk, g, d)
+            tile = table.get((bq, bk, d), 128) if bq <= 64 else 128
+            assert bool(f & bsa.PLAN_Q64) == (tile == 64), (bq, bk, d, g, f)
+            rq = tile // min(bq, tile)
+            assert bool(f & bsa.PLAN_REMAP) == (rq > 1 and g == 1), (bq, bk, d, g, f)
+            L = bsa.plan_layout(1, 4, 4096 // bq, 4096 // bk, bq, bk, g, f)  # a valid plan layout
+            assert L.qu * L.rq == tile
+    with pytest.raises(bsa.BsaError):
+        bsa.select_flags(1, 2, 4, 4, 48, 64, 1, 128)   # unsupported block size
+    with pytest.raises(bsa.BsaError):
+        bsa.select_flags(1, 2, 4, 4, 64, 64, 1, 96)    # unsupported head dim
+
+
+def test_regime_choice_rule():
+    # the sweep keeps, per (bq, bk, d), the tile with the smaller geometric-mean time
+    from block_sparse_attention_plan_gb300 import regime_sweep as RS
+    rows = [{"bq": 64, "bk": 64, "d": 128, "tile": t, "kernel_ms": ms}
+            for t, ms in ((128, 1.0), (128, 4.0), (64, 1.5), (64, 2.5))]   # gm 2.0 vs 1.94
+    rows += [{"bq": 32, "bk": 32, "d": 64, "tile": t, "kernel_ms": ms} for t, ms in ((128, 1.0), (64, 3.0))]
+    best = RS.choose(rows)
+    assert best[(64, 64, 128)][0] == 64 and best[(32, 32, 64)][0] == 128

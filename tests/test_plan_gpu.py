@@ -133,3 +133,26 @@ def test_plan_remap_random_masks(bsa, bq, bk, g):
     assert_plan_equal(a, ref)
     if g == 1:
         assert max(a["plane_sigma"].tolist()) > 1
+
+
+@pytest.mark.parametrize("name,flags", [("chunked_prefill_small", 0), ("regular_small", 2)])
+def test_plan_export_host_copies(bsa, name, flags):
+    # bsa_plan_export: the same arrays as the device views, and the oracle's
+    w = W.make_workload(name, data=False)
+    p = bsa.plan(w.mask.cuda(), w.bq, w.bk, w.gqa_group, flags=flags)
+    host = p.export()
+    dev = {k: (v.cpu().numpy() if torch.is_tensor(v) else v) for k, v in p.arrays().items()}
+    for k in ("row_ptr", "slot_ku", "urow_ptr", "ukb", "order", "plane_sigma"):
+        assert np.array_equal(host[k], dev[k]), k
+    assert np.array_equal(host["slot_mask"].astype(np.int64), dev["slot_mask"].astype(np.int64) & 0xFFFFFFFF)
+    ref = OP.build_plan(w.mask.numpy(), w.bq, w.bk, w.gqa_group, remap=bool(flags))
+    host["slot_mask"] = host["slot_mask"].astype(np.int64)
+    assert_plan_equal(host, ref)
+    # a buffer too small: BSA_ERR_WORKSPACE, totals still written
+    from block_sparse_attention_plan_gb300 import _lib as L
+    import ctypes
+    c = L.PlanArraysC()
+    small = np.empty(1, np.int32)
+    c.row_ptr, c.row_ptr_cap = ctypes.c_void_p(small.ctypes.data), 1
+    assert L.library().bsa_plan_export(p.handle, None, ctypes.byref(c)) == -5
+    assert list(c.totals)[:3] == host["totals"][:3].tolist()
