@@ -724,8 +724,12 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
 }
 
 // kGeneral: paged K/V and/or element masks (runtime-selected inside); the
-// plain instantiation carries none of that code.
-template <int D, bool kExact, bool kGeneral>
+// plain instantiation carries none of that code.  kMulti: slots of several
+// K/V units (p.rk > 1), gathered by whole producer warps; a separate
+// instantiation, so that the kernels of one-unit slots keep the
+// single-thread producers alone (about 1 % faster than with both forms in
+// one binary).
+template <int D, bool kExact, bool kGeneral, bool kMulti>
 __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -784,11 +788,16 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
     softmax_role<D, kExact, kGeneral>(p, smem, sm, tmem, wd);
   } else {
     regs_dec<kRegsControl>();
-    if (lane == 0 && !*abort_flag) {
-      if (warp == 0) producer_role<Cfg<D>, kGeneral>(p, smem, sm, wd, true);
+    if (kMulti && (warp == 0 || warp == 3)) {
+      // Slots of several units: the producers run on their whole warp (lane
+      // u issues the copies of a slot's unit u).
+      if (__shfl_sync(0xffffffffu, *abort_flag == 0 ? 1 : 0, 0))
+        producer_role_warp<Cfg<D>, kGeneral>(p, smem, sm, wd, warp == 0);
+    } else if (lane == 0 && !*abort_flag) {
+      if (!kMulti && warp == 0) producer_role<Cfg<D>, kGeneral>(p, smem, sm, wd, true);
       else if (warp == 1) s_issuer_role<D>(p, smem, sm, tmem, wd);
       else if (warp == 2) pv_issuer_role<D>(p, smem, sm, tmem, wd);
-      else if (warp == 3) producer_role<Cfg<D>, kGeneral>(p, smem, sm, wd, false);
+      else if (!kMulti && warp == 3) producer_role<Cfg<D>, kGeneral>(p, smem, sm, wd, false);
     }
   }
 
@@ -814,14 +823,19 @@ __global__ void watchdog_selftest_kernel(int32_t* status, long long limit_ns) {
   if (mbar_wait(bar, 0, wd, kSiteSelftest)) status[3] = 1;
 }
 
-template <int D, bool kExact, bool kGeneral>
-cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t stream) {
+template <int D, bool kExact, bool kGeneral, bool kMulti>
+cudaError_t launch_dm(const FwdParams& p, int grid, cudaStream_t stream) {
   const int smem = Cfg<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(bsa_fwd_kernel<D, kExact, kGeneral>,
+  cudaError_t e = cudaFuncSetAttribute(bsa_fwd_kernel<D, kExact, kGeneral, kMulti>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  bsa_fwd_kernel<D, kExact, kGeneral><<<grid, kThreads, smem, stream>>>(p);
+  bsa_fwd_kernel<D, kExact, kGeneral, kMulti><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
+}
+template <int D, bool kExact, bool kGeneral>
+cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t stream) {
+  return p.rk > 1 ? launch_dm<D, kExact, kGeneral, true>(p, grid, stream)
+                  : launch_dm<D, kExact, kGeneral, false>(p, grid, stream);
 }
 
 // Largest key norm of every K unit (ku rows) of every K/V head, i.e. a bound

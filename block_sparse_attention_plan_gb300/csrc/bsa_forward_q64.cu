@@ -575,7 +575,11 @@ __global__ void __launch_bounds__(kQ64Threads, 1) bsa_fwd_q64_kernel(const __gri
     q64_softmax<C, kExact>(p, smem, sm, tmem, wd);
   } else {
     regs_dec<kQRegsControl>();
-    if (lane == 0 && !*abort_flag) {
+    if (p.rk > 1 && (warp == 0 || warp == 3)) {
+      // Slots of several units: the producers run on their whole warp (lane
+      // u issues the copies of a slot's unit u).
+      if (__shfl_sync(0xffffffffu, *abort_flag == 0 ? 1 : 0, 0)) producer_role_warp<C, false>(p, smem, sm, wd, warp == 0);
+    } else if (lane == 0 && !*abort_flag) {
       if (warp == 0) producer_role<C, false>(p, smem, sm, wd, true);
       else if (warp == 1) q64_s_issuer<C>(p, smem, sm, tmem, wd);
       else if (warp == 2) q64_pv_issuer<C>(p, smem, sm, tmem, wd);

@@ -163,22 +163,28 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 }
 
 // ------------------------------------------------------------------ producers
-// K/V units of one slot as the plan lists them (rk <= 4 entries, -1 = padding)
-// or, for paged K/V, their pool rows as the row-bound pass resolved them.  A
-// producer reads them two slots ahead, so the global-load latency overlaps
-// its stage waits instead of sitting between a stage freeing and its copy
-// (a block-table lookup there, dependent on the plan entry, cost the paged
-// path about 40 %).
-struct SlotKeys {
-  int y[4];
-};
+// A TMA copy instruction does not return until the copy engine has taken it,
+// about 300 cycles per box under load, so one thread issuing every box of a
+// slot made small-block slots (2-4 units of 32 or 64 keys, a box per unit and
+// 64-column half) wait for their K/V tiles.  For slots of several units
+// (kWarp) the producers run on their whole warp and lane u issues the boxes
+// of the slot's unit u (measured: chunked prefill +16 %, regular patterns
+// +40 %, outputs bit-identical); control flow is then warp-uniform and lane 0
+// alone takes the single-thread steps (work counter, publishing, barrier
+// arrivals, byte counts).  Slots of one unit keep a single thread, which is
+// 2 % faster there than the warp form.
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// This lane's K/V unit of slot j of the row (lane u < rk: slot position u,
+// -1 = padding, or for paged K/V its pool row as the row-bound pass
+// resolved it; other lanes -1).  A producer reads it two slots ahead, so the
+// global-load latency overlaps its stage waits instead of sitting between a
+// stage freeing and its copy (a block-table lookup there, dependent on the
+// plan entry, cost the paged path about 40 %).
 template <bool kGeneral>
-__device__ __forceinline__ SlotKeys fetch_keys(const FwdParams& p, const Item& m, int j) {
-  SlotKeys k;
+__device__ __forceinline__ int fetch_key(const FwdParams& p, const Item& m, int j, int lane) {
   const int32_t* ent = ((kGeneral && p.prow) ? p.prow : p.slot_ku) + (size_t)(m.s0 + j) * p.rk;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) k.y[u] = (u < p.rk) ? __ldg(ent + u) : -1;
-  return k;
+  return lane < p.rk ? __ldg(ent + lane) : -1;
 }
 
 // One ring of tile stages with a single producer and a single consumer.
@@ -189,38 +195,34 @@ struct Ring {
   int stages;
 };
 
-// Gather the 128 keys of one slot into the next stage of `r`.
+// Gather the 128 keys of one slot into the next stage of `r` (called by the
+// whole warp; `key` is the lane's unit from fetch_key).
 // kBox3: slots of one 128-key unit at d = 128 through the 3D view (one box
 // per unit), a compile-time choice so that each producer loop carries one
 // form only (the 3D branch in the 2D producer's loop slowed it by 4.5 %).
-template <class C, bool kGeneral, bool kBox3>
+template <class C, bool kGeneral, bool kBox3, bool kWarp>
 __device__ __forceinline__ bool load_tile(const FwdParams& p, const CUtensorMap* map, const Ring& r,
-                                          const Item& m, const SlotKeys& keys, uint32_t& it,
+                                          const Item& m, int key, int lane, uint32_t& it,
                                           uint64_t pol, const Watchdog& wd) {
   const uint32_t stage = it % (uint32_t)r.stages;
   const uint32_t ph = (it / (uint32_t)r.stages) & 1u;
-  if (!mbar_wait(r.empty + 8u * stage, ph ^ 1u, wd, kSiteKvEmpty)) return false;
+  bool waited = mbar_wait(r.empty + 8u * stage, ph ^ 1u, wd, kSiteKvEmpty);
+  if (kWarp) waited = __all_sync(kFullMask, waited);
+  if (!waited) return false;
   const uint32_t full = r.full + 8u * stage;
-  mbar_arrive_expect_tx(full, C::kTileBytes);
+  if (lane == 0) mbar_arrive_expect_tx(full, C::kTileBytes);
+  if (kWarp) __syncwarp();
   const bool paged = kGeneral && p.prow != nullptr;  // keys are pool rows
-  int first = keys.y[0];
+  int first = kWarp ? __shfl_sync(kFullMask, key, 0) : key;
   if (first < 0 || (!paged && first >= p.NKU)) {
-    record_status(p.control, -7, kSitePlanRange + 2);
+    if (lane == 0) record_status(p.control, -7, kSitePlanRange + 2);
     first = 0;
   }
   const uint32_t dst0 = r.data + stage * (uint32_t)C::kTileBytes;
   if constexpr (kBox3) {  // one 128-key unit: both halves in one box
-    int y = keys.y[0];
-    if (y < 0 || (!paged && y >= p.NKU)) y = first;
-    const int row = paged ? y : m.kvrow0 + y * p.ku;
-    tma_load_3d(dst0, map, 0, row, 0, full, pol);
-    ++it;
-    return true;
-  }
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    if (u >= p.rk) break;
-    int y = keys.y[u];
+    if (lane == 0) tma_load_3d(dst0, map, 0, paged ? first : m.kvrow0 + first * p.ku, 0, full, pol);
+  } else if (lane < p.rk) {
+    int y = key;
     if (y < 0) {
       y = first;  // padding position: load real rows, the sub-mask hides them
     } else if (!paged && y >= p.NKU) {
@@ -230,7 +232,7 @@ __device__ __forceinline__ bool load_tile(const FwdParams& p, const CUtensorMap*
     const int row = paged ? y : m.kvrow0 + y * p.ku;
 #pragma unroll
     for (int c = 0; c < C::kChunks; ++c)
-      tma_load_2d(dst0 + c * C::kChunkBytes + u * p.ku * 128, map, c * 64, row, full, pol);
+      tma_load_2d(dst0 + c * C::kChunkBytes + lane * p.ku * 128, map, c * 64, row, full, pol);
   }
   ++it;
   return true;
@@ -241,15 +243,22 @@ __device__ __forceinline__ bool load_tile(const FwdParams& p, const CUtensorMap*
 // over the row's slots).  V producer:
 // reads the published items and loads the V tile of every slot.  Both load in
 // slot order, which is the order the MMA thread consumes each ring in.
-template <class C, bool kGeneral, bool kBox3>
+// kWarp: run by the whole warp, else by lane 0 alone.
+template <class C, bool kGeneral, bool kBox3, bool kWarp>
 __device__ __noinline__ void producer_body(const FwdParams& p, uint8_t* smem, const Smem<C> sm,
                                            const Watchdog wd, bool kside) {
+  static_assert(!(kBox3 && kWarp), "3D boxes carry one unit per slot");
+  const int lane = kWarp ? (int)(threadIdx.x & 31) : 0;
+  auto all = [](bool v) { return kWarp ? __all_sync(kFullMask, v) : v; };
+  auto from0 = [](int v) { return kWarp ? __shfl_sync(kFullMask, v, 0) : v; };
   const CUtensorMap* map = kBox3 ? (kside ? &p.tmK3 : &p.tmV3) : (kside ? &p.tmK : &p.tmV);
-  if (kside) {
-    tma_prefetch_desc((C::kChunks == 2 && p.q_box3) ? &p.tmQ3 : &p.tmQ);
-    tma_prefetch_desc(&p.tmQu);
+  if (lane == 0) {
+    if (kside) {
+      tma_prefetch_desc((C::kChunks == 2 && p.q_box3) ? &p.tmQ3 : &p.tmQ);
+      tma_prefetch_desc(&p.tmQu);
+    }
+    tma_prefetch_desc(map);
   }
-  tma_prefetch_desc(map);
   const uint64_t pol_q = policy_evict_first();
   const uint64_t pol_kv = policy_evict_last();
   const Ring r = kside ? Ring{sm.kst(0), sm.bar(C::kBarKFull), sm.bar(C::kBarKEmpty), C::kStagesK}
@@ -262,20 +271,22 @@ __device__ __noinline__ void producer_body(const FwdParams& p, uint8_t* smem, co
     Item m;
     if (kside) {
       const int slot = (int)(t % kSchedSlots);
-      if (!mbar_wait(sm.bar(C::kBarSchedEmpty + slot), ((t / kSchedSlots) & 1u) ^ 1u, wd,
-                     kSiteSched))
+      if (!all(mbar_wait(sm.bar(C::kBarSchedEmpty + slot), ((t / kSchedSlots) & 1u) ^ 1u, wd,
+                         kSiteSched)))
         break;
-      int it = atomicAdd(p.work_counter, 1);
+      int it = 0;
+      if (lane == 0) it = atomicAdd(p.work_counter, 1);
+      it = from0(it);
       if (it >= nwork) it = -1;
       if (it >= 0) {
-        m = load_item(p, it, true);
+        m = load_item(p, it, lane == 0);  // the same loads on every lane
         if (m.n > 0) {
           m.kb = __ldg(p.rowk + m.row);
           m.split = p.split_all || __ldg(p.rowv + m.row) > kSplitV;
           if (C::kQueueSplit && m.split) {
             // This pass does not apply split weights: the row is left to
             // the exact pass (queued once) and handed on as skipped.
-            if (atomicExch(p.fb_flag + m.row, 1) == 0)
+            if (lane == 0 && atomicExch(p.fb_flag + m.row, 1) == 0)
               p.fb_list[atomicAdd(p.control + kCtlFallbackCount, 1)] = m.row;
             m.n = 0;
             m.valid = false;
@@ -284,29 +295,36 @@ __device__ __noinline__ void producer_body(const FwdParams& p, uint8_t* smem, co
       } else {
         m = Item{0, 0, 0, 0, 1, 0, false, 0, -1, 0.f, false};
       }
-      sched_publish<C>(smem, slot, m);
-      mbar_arrive(sm.bar(C::kBarSchedFull + slot));
+      if (lane == 0) {
+        sched_publish<C>(smem, slot, m);
+        mbar_arrive(sm.bar(C::kBarSchedFull + slot));
+      }
     } else {
-      m = sched_take<C>(sm, smem, t, true, false, wd);
+      m = sched_take<C>(sm, smem, t, lane == 0, kWarp, wd);
     }
     if (m.it < 0) break;
     if (m.n == 0) continue;
     if (kside) {
       const int qb = q_buf<C>(q_it);
-      if (!mbar_wait(sm.bar(C::kBarQEmpty + qb), q_par<C>(q_it) ^ 1u, wd, kSiteQEmpty)) break;
-      mbar_arrive_expect_tx(sm.bar(C::kBarQFull + qb), C::kQBytes);
+      if (!all(mbar_wait(sm.bar(C::kBarQEmpty + qb), q_par<C>(q_it) ^ 1u, wd, kSiteQEmpty))) break;
+      if (lane == 0) mbar_arrive_expect_tx(sm.bar(C::kBarQFull + qb), C::kQBytes);
+      if (kWarp) __syncwarp();
       if (m.qs == 1) {  // the tile's q-units are contiguous: one box of the tile's rows
-        const int qrow = m.bh * p.Nq + m.qx * p.qu;
-        if (C::kChunks == 2 && p.q_box3) {
-          tma_load_3d(sm.q(qb), &p.tmQ3, 0, qrow, 0, sm.bar(C::kBarQFull + qb), pol_q);
-        } else {
+        if (lane == 0) {
+          const int qrow = m.bh * p.Nq + m.qx * p.qu;
+          if (C::kChunks == 2 && p.q_box3) {
+            tma_load_3d(sm.q(qb), &p.tmQ3, 0, qrow, 0, sm.bar(C::kBarQFull + qb), pol_q);
+          } else {
 #pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_2d(sm.q(qb) + c * C::kQChunkBytes, &p.tmQ, c * 64, qrow,
-                        sm.bar(C::kBarQFull + qb), pol_q);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_2d(sm.q(qb) + c * C::kQChunkBytes, &p.tmQ, c * 64, qrow,
+                          sm.bar(C::kBarQFull + qb), pol_q);
+          }
         }
-      } else {  // q-unit i (qu rows) into tile rows [i*qu, (i+1)*qu)
-        for (int i = 0; i < p.rq; ++i) {
+      } else {
+        // q-unit i (qu rows) into tile rows [i*qu, (i+1)*qu): lane i, or
+        // every one by lane 0
+        for (int i = lane; i < p.rq; i += kWarp ? 32 : 1) {
           const int qrow = m.bh * p.Nq + (m.qx + i * m.qs) * p.qu;
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
@@ -319,17 +337,19 @@ __device__ __noinline__ void producer_body(const FwdParams& p, uint8_t* smem, co
     // Tiles of this row in consumption order: the K tiles once per sweep of
     // the row's slots (C::kKSweeps), the V tiles once.
     const int nt = (kside ? C::kKSweeps : 1) * m.n;
-    SlotKeys k0 = fetch_keys<kGeneral>(p, m, 0), k1 = k0;
-    if (nt > 1) k1 = fetch_keys<kGeneral>(p, m, C::kKSweeps == 1 ? 1 : 1 % m.n);
+    int k0 = fetch_key<kGeneral>(p, m, 0, lane), k1 = k0;
+    if (nt > 1) k1 = fetch_key<kGeneral>(p, m, C::kKSweeps == 1 ? 1 : 1 % m.n, lane);
     for (int j = 0; j < nt && ok; ++j) {
-      SlotKeys k2 = k1;
-      if (j + 2 < nt) k2 = fetch_keys<kGeneral>(p, m, C::kKSweeps == 1 ? j + 2 : (j + 2) % m.n);
-      ok = load_tile<C, kGeneral, kBox3>(p, map, r, m, k0, kv_it, pol_kv, wd);
+      int k2 = k1;
+      if (j + 2 < nt) k2 = fetch_key<kGeneral>(p, m, C::kKSweeps == 1 ? j + 2 : (j + 2) % m.n, lane);
+      ok = load_tile<C, kGeneral, kBox3, kWarp>(p, map, r, m, k0, lane, kv_it, pol_kv, wd);
       k0 = k1;
       k1 = k2;
     }
   }
-  if (*wd.abort_flag) {
+  int aborted = 0;
+  if (lane == 0) aborted = *wd.abort_flag;
+  if (from0(aborted) && lane == 0) {
     // Let copies already issued land before the CTA's shared memory goes away.
     const uint32_t nst = (uint32_t)r.stages;
     const uint32_t nk = kv_it < nst ? kv_it : nst;
@@ -343,12 +363,19 @@ __device__ __noinline__ void producer_body(const FwdParams& p, uint8_t* smem, co
   }
 }
 
-
+// Producer of a kernel whose slots hold one unit (p.rk == 1): lane 0 alone.
 template <class C, bool kGeneral>
 __device__ __forceinline__ void producer_role(const FwdParams& p, uint8_t* smem, const Smem<C> sm,
                                               const Watchdog wd, bool kside) {
-  if (C::kChunks == 2 && p.kv_box3) producer_body<C, kGeneral, C::kChunks == 2>(p, smem, sm, wd, kside);
-  else producer_body<C, kGeneral, false>(p, smem, sm, wd, kside);
+  if (C::kChunks == 2 && p.kv_box3) producer_body<C, kGeneral, C::kChunks == 2, false>(p, smem, sm, wd, kside);
+  else producer_body<C, kGeneral, false, false>(p, smem, sm, wd, kside);
+}
+// Producer of a kernel whose slots hold several units (p.rk > 1): every lane
+// of the warp.
+template <class C, bool kGeneral>
+__device__ __forceinline__ void producer_role_warp(const FwdParams& p, uint8_t* smem, const Smem<C> sm,
+                                                   const Watchdog wd, bool kside) {
+  producer_body<C, kGeneral, false, true>(p, smem, sm, wd, kside);
 }
 
 }  // namespace
