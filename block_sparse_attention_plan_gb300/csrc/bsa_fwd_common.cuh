@@ -167,9 +167,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 // about 300 cycles per box under load, so one thread issuing every box of a
 // slot made small-block slots (2-4 units of 32 or 64 keys, a box per unit and
 // 64-column half) wait for their K/V tiles.  For slots of several units
-// (kWarp) the producers run on their whole warp and lane u issues the boxes
-// of the slot's unit u (measured: chunked prefill +16 %, regular patterns
-// +40 %, outputs bit-identical); control flow is then warp-uniform and lane 0
+// (kWarp) the producers run on their whole warp and each lane issues one box
+// (measured: chunked prefill +16 %, regular patterns +40 %, outputs
+// bit-identical); control flow is then warp-uniform and lane 0
 // alone takes the single-thread steps (work counter, publishing, barrier
 // arrivals, byte counts).  Slots of one unit keep a single thread, which is
 // 2 % faster there than the warp form.
@@ -221,18 +221,23 @@ __device__ __forceinline__ bool load_tile(const FwdParams& p, const CUtensorMap*
   const uint32_t dst0 = r.data + stage * (uint32_t)C::kTileBytes;
   if constexpr (kBox3) {  // one 128-key unit: both halves in one box
     if (lane == 0) tma_load_3d(dst0, map, 0, paged ? first : m.kvrow0 + first * p.ku, 0, full, pol);
-  } else if (lane < p.rk) {
-    int y = key;
-    if (y < 0) {
-      y = first;  // padding position: load real rows, the sub-mask hides them
-    } else if (!paged && y >= p.NKU) {
-      record_status(p.control, -7, kSitePlanRange + 3);
-      y = first;
-    }
-    const int row = paged ? y : m.kvrow0 + y * p.ku;
+  } else {
+    // Warp form: lane u * kChunks + c copies 64-column chunk c of unit u (one
+    // box per lane); single thread: lane 0 copies every chunk of its unit.
+    const int u = kWarp ? lane / C::kChunks : lane;
+    int y = kWarp ? __shfl_sync(kFullMask, key, u) : key;
+    if (u < p.rk) {
+      if (y < 0) {
+        y = first;  // padding position: load real rows, the sub-mask hides them
+      } else if (!paged && y >= p.NKU) {
+        record_status(p.control, -7, kSitePlanRange + 3);
+        y = first;
+      }
+      const int row = paged ? y : m.kvrow0 + y * p.ku;
 #pragma unroll
-    for (int c = 0; c < C::kChunks; ++c)
-      tma_load_2d(dst0 + c * C::kChunkBytes + lane * p.ku * 128, map, c * 64, row, full, pol);
+      for (int c = kWarp ? lane % C::kChunks : 0; c < C::kChunks; c += kWarp ? C::kChunks : 1)
+        tma_load_2d(dst0 + c * C::kChunkBytes + u * p.ku * 128, map, c * 64, row, full, pol);
+    }
   }
   ++it;
   return true;
