@@ -49,9 +49,10 @@ METRIC = "effective TFLOP/s over active tiles & % of GB300 BF16 tensor peak"
 # `ncu --set full` capture of that workload (summaries under profiles/), and the
 # hash of the kernel sources it was taken on: a changed kernel reports null.
 NCU_TRAFFIC = {
-    "video_dit": (302.4256e6 + 79.938048e6, "75d86ea2a5bd10e4"),
+    "video_dit": (302.459136e6 + 80.098048e6, "244093159c2c018a"),
 }
 KERNEL_SOURCES = ("block_sparse_attention_plan_gb300/csrc/bsa_forward.cu",
+                  "block_sparse_attention_plan_gb300/csrc/bsa_fwd_common.cuh",
                   "block_sparse_attention_plan_gb300/csrc/bsa_device.cuh")
 
 
@@ -316,7 +317,8 @@ class _Case:
         a side stream, the key-norm pass (it reads only K and V); then the
         row-bound, bounded and exact passes once both are done
         (bsa_forward_stage).  Events: step start, plan + key norms done,
-        bounded pass start, bounded pass end, step end."""
+        bounded pass start, bounded pass end, step end, plan kernels done,
+        key-norm pass start and end (on the side stream)."""
         bsa, w, stream = self.bsa, self.w, self.stream
         if ev is not None:
             ev[0].record(stream)
@@ -328,10 +330,16 @@ class _Case:
         else:
             p = bsa.plan(self.mask_d, w.bq, w.bk, w.gqa_group, workspace=self.wsbuf,
                          flags=self.plan_flags)
+        if ev is not None:
+            ev[5].record(stream)  # the plan kernels are done
         self.side.wait_event(self.fork)  # starts with the plan kernels, not after them
         args = (p, self.q, self.k, self.v)
         kw = dict(out=self.o, lse=self.lse, **self.fwd_extra)
+        if ev is not None:
+            ev[6].record(self.side)
         bsa.forward(*args, stages=bsa.STAGE_KNORM, stream=self.side, **kw)
+        if ev is not None:
+            ev[7].record(self.side)
         stream.wait_stream(self.side)
         if ev is not None:
             ev[1].record(stream)
@@ -360,7 +368,7 @@ class _Case:
 
     def timed(self, steps, barrier=lambda: None):
         """Time `steps` steps; returns (per-step events, wall t0, wall t1)."""
-        fev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(5)) for _ in range(steps)]
+        fev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(8)) for _ in range(steps)]
         barrier()
         torch.cuda.synchronize()
         t0 = time.time()
@@ -392,11 +400,16 @@ class _Case:
 
 
 def _times(fev):
+    """Mean over the timed steps: step, forward (after the preparation),
+    preparation (plan and key norms side by side), bounded pass, plan kernels
+    alone, key-norm pass alone (ms)."""
     ms = float(np.mean([e[0].elapsed_time(e[4]) for e in fev]))
     fwd_ms = float(np.mean([e[1].elapsed_time(e[4]) for e in fev]))
-    plan_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in fev]))
+    prep_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in fev]))
     bounded_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in fev]))
-    return ms, fwd_ms, plan_ms, bounded_ms
+    plan_ms = float(np.mean([e[0].elapsed_time(e[5]) for e in fev]))
+    knorm_ms = float(np.mean([e[6].elapsed_time(e[7]) for e in fev]))
+    return ms, fwd_ms, prep_ms, bounded_ms, plan_ms, knorm_ms
 
 
 # GB300 nominal dense bf16 tensor throughput per GPU (datasheet figure without
@@ -419,7 +432,7 @@ def per_config_entry(bsa, W, name, dev, stream, clocks, peak, target_s=0.5):
     est = (time.perf_counter() - t0) / 3
     steps = int(min(2000, max(20, math.ceil(target_s / max(est, 1e-6)))))
     fev, w0, w1 = c.timed(steps)
-    ms, fwd_ms, plan_ms, bounded_ms = _times(fev)
+    ms, fwd_ms, prep_ms, bounded_ms, plan_ms, knorm_ms = _times(fev)
     _, computed, ratio = c.plan_stats()
     flop = w.active_flop
     kern = flop / (bounded_ms * 1e-3) / 1e12
@@ -430,7 +443,7 @@ def per_config_entry(bsa, W, name, dev, stream, clocks, peak, target_s=0.5):
          "kernel": "bsa_fwd_kernel<%d, bounded>" % w.d, "kernel_ms": bounded_ms,
          "roofline": {"achieved": kern, "peak": peak, "frac": kern / peak,
                       "frac_of_nominal": kern / NOMINAL_BF16_TFLOPS},
-         "forward_ms": fwd_ms, "plan_ms": plan_ms,
+         "forward_ms": fwd_ms, "plan_ms": plan_ms, "knorm_ms": knorm_ms, "prep_ms": prep_ms,
          "clocks": clocks.summary(w0, w1)}
     c.free()
     del c, w
@@ -511,8 +524,11 @@ def run_gb300(args):
     c.warm(args.warmup)
     fev, t_wall0, t_wall1 = c.timed(args.steps, barrier)
     plan_bytes, computed, ratio = c.plan_stats()
+    # key-norm pass: K and V read once, a float per unit and tensor written
+    Lk = c.p.layout
+    knorm_bytes = 2 * w.k.numel() * 2 + 2 * 4 * Lk.B * Lk.Hkv * Lk.NKU
     # a step = plan start -> forward end, timed with events on the launching stream
-    ms, fwd_ms, plan_ms, bounded_ms = _times(fev)
+    ms, fwd_ms, prep_ms, bounded_ms, plan_ms, knorm_ms = _times(fev)
     ms, fwd_ms, bounded_ms = max_over_ranks([ms, fwd_ms, bounded_ms], dev)
     clk = clocks.summary(t_wall0, t_wall1)
     launches = c.launches_per_step * args.steps
@@ -569,8 +585,14 @@ def run_gb300(args):
         "plan": {"ms": plan_ms, "bytes": int(plan_bytes),
                  "gbs": plan_bytes / (plan_ms * 1e-3) / 1e9,
                  "frac_of_hbm": plan_bytes / (plan_ms * 1e-3) / 1e9 / _hbm_gbs(),
-                 "note": "ms: step start until the plan kernels and the key-norm pass, run side by "
-                         "side, are both done; the plan kernels are latency-bound at these sizes"},
+                 "knorm_ms": knorm_ms, "knorm_bytes": int(knorm_bytes),
+                 "knorm_gbs": knorm_bytes / (knorm_ms * 1e-3) / 1e9,
+                 "knorm_frac_of_hbm": knorm_bytes / (knorm_ms * 1e-3) / 1e9 / _hbm_gbs(),
+                 "prep_ms": prep_ms,
+                 "note": "ms: step start until the plan kernels are done (their own time, beside "
+                         "the key-norm pass on a second stream); knorm_ms: the key-norm pass, "
+                         "which reads K and V once; prep_ms: step start until both are done. The "
+                         "plan kernels are latency-bound at these sizes"},
         "gpu_launches": launches,
         "clocks": clk,
     }
