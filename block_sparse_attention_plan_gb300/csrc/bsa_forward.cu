@@ -843,24 +843,36 @@ cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t stream) {
 // |v| element of every V unit (which decides whether a row applies split
 // weights); also clears the fallback flags.  The K units come first, then
 // the V units: each CTA streams groups of kKmaxGroupBytes / (ku*d*2)
-// consecutive units of one tensor through a ring of shared-memory stages
-// with bulk copies (one thread issues them, completion on the stage's
-// mbarrier), so many bytes are in flight per SM with few registers; each
-// thread then reduces the rows it owns (16-byte reads rotated across the row
-// so the threads of a warp hit different banks).  Units wholly past the
+// consecutive units of one tensor through shared-memory stages with bulk
+// copies (one thread issues them, completion on the stage's mbarrier), so
+// many bytes are in flight per SM with few registers; each thread then
+// reduces the rows it owns (16-byte reads rotated across the row so the
+// threads of a warp hit different banks).  One stage per CTA and
+// kKmaxCtasPerSm CTAs per SM: more CTAs reducing side by side beat deeper
+// rings in a CTA (video-DiT, same bytes in flight: 3 stages x 2 CTAs
+// 46.4 us, 2 x 3 42.0 us, 1 x 6 38.3 us with the cache hint below).  The
+// copies carry an L2 evict-first hint: K and V are streamed once here, and
+// the plan kernels running beside this pass keep their small working set in
+// L2 (their time in the step: 60 -> 50 us).  Units wholly past the
 // sequence's key length (or, paged, without a valid page) get 0 and are not
 // read: their keys are masked.  A wait that runs out is recorded in the
 // pass's own status words (its stage may run on another stream beside the
 // plan kernels).
 constexpr int kKmaxThreads = 128;
-constexpr int kKmaxStages = 3;
+constexpr int kKmaxStages = 1;
+constexpr int kKmaxCtasPerSm = 6;
 constexpr uint32_t kKmaxGroupBytes = 32768;
 constexpr int kKmaxSmem = kKmaxStages * (int)kKmaxGroupBytes + 1024;
+static_assert(kKmaxStages <= 4, "the stage flags end where the row maxima begin");
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-               : "memory");
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
 }
 
 template <int D>
@@ -1056,7 +1068,7 @@ cudaError_t launch_passes(const FwdParams& p, int grid, cudaStream_t stream, int
   if (stages & (BSA_STAGE_PREPARE | BSA_STAGE_KNORM)) {
   const long long units = (long long)p.B * p.Hkv * p.NKU;
   const long long kgroups = 2 * ((units + (kKmaxGroupBytes / (p.ku * D * 2)) - 1) / (kKmaxGroupBytes / (p.ku * D * 2)));
-  long long kgrid = 2ll * (p.sms > 0 ? p.sms : 1);
+  long long kgrid = (long long)kKmaxCtasPerSm * (p.sms > 0 ? p.sms : 1);
   if (kgrid > kgroups) kgrid = kgroups;
   if (kgrid < 1) kgrid = 1;
   e = cudaFuncSetAttribute(kmax_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kKmaxSmem);
