@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libbsa.so")
-SOURCES = ["bsa_api.cu", "bsa_plan.cu", "bsa_forward.cu", "bsa_forward_q64.cu", "bsa_noalloc.cu",
+SOURCES = ["bsa_api.cu", "bsa_plan.cu", "bsa_prep.cu", "bsa_forward.cu", "bsa_forward_q64.cu", "bsa_noalloc.cu",
            "bsa_pipeline.cu"]
 HEADERS = ["bsa_internal.h", "bsa_device.cuh", "bsa_fwd_common.cuh", "bsa_regime_table.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

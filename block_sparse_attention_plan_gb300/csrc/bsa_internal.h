@@ -183,6 +183,9 @@ cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream);
 cudaError_t launch_forward(const FwdParams& p, int d, int grid, cudaStream_t stream,
                            int stages = BSA_STAGE_ALL);
 int forward_smem_bytes(int d);
+// Key-norm and row-bound passes of `stages` (BSA_STAGE_PREPARE, _KNORM,
+// _ROWBOUND bits; others ignored), see bsa_prep.cu.
+cudaError_t launch_prep(const FwdParams& p, int d, int stages, cudaStream_t stream);
 // Bounded (exact = false) or exact pass of a plan with 64-row q-tiles
 // (bsa_forward_q64.cu); launched by launch_forward for such plans.
 cudaError_t launch_forward_q64(const FwdParams& p, int d, int grid, cudaStream_t stream, bool exact);
