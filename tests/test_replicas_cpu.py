@@ -63,3 +63,32 @@ def test_cpu_baseline_sampler_and_config_on_cpu():
     cfg = bench._config(w, gpu=False)
     assert cfg["workload"] == "tiny" and cfg["active_blocks"] == w.active_blocks
     assert cfg["active_flop_per_step"] == w.active_flop
+
+
+class _Ev:
+    """Stand-in for a CUDA event: a timestamp in ms."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def elapsed_time(self, other):
+        return other.t - self.t
+
+
+def test_step_times_from_events():
+    # Events of one step: start, preparation done, bounded start, bounded
+    # end, step end, plan kernels done, key-norm start, key-norm end.
+    step = [_Ev(t) for t in (0.0, 0.053, 0.058, 0.497, 0.508, 0.050, 0.001, 0.039)]
+    ms, fwd_ms, prep_ms, bounded_ms, plan_ms, knorm_ms = bench._times([step, step])
+    assert ms == pytest.approx(0.508)
+    assert fwd_ms == pytest.approx(0.508 - 0.053)
+    assert prep_ms == pytest.approx(0.053)
+    assert bounded_ms == pytest.approx(0.497 - 0.058)
+    assert plan_ms == pytest.approx(0.050)
+    assert knorm_ms == pytest.approx(0.038)
+
+
+def test_traffic_figure_is_keyed_to_the_kernel_sources():
+    value, key = bench.NCU_TRAFFIC["video_dit"]
+    assert bench._traffic("video_dit") == (value if key == bench._kernel_hash() else None)
+    assert bench._traffic("no_such_workload") is None
