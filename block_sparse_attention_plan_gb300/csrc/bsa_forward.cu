@@ -45,11 +45,12 @@
 //   [0,128) S buffer 0   [128,256) S buffer 1   [256,256+d) O
 //   [384,448) P buffer 0 [448,512) P buffer 1   (P: bf16 pairs, keys 2c, 2c+1
 //   in column c).  Slot g of the CTA uses S and P buffer g mod 2.  A row with
-//   split weights keeps the low-order terms of slot g in S buffer g mod 2:
-//   the softmax thread of key half h, which loaded that buffer's columns
-//   [64h, 64h+64), writes them over [64h, 64h+32) (pairs laid out as in P);
-//   no thread rewrites a column another one has yet to read, and that S
-//   buffer is released by the slot's P V instead of by the softmax.
+//   split weights writes the low-order terms of slot g into the other P
+//   buffer (same layout), which the P V of slot g - 1 must have finished
+//   reading first; so such a slot waits for the P V of the slot before it
+//   as well as for the one two slots back, and the first slot after such a
+//   row waits for the P V of the row's last slot.  The S buffers are
+//   released by the softmax after loading in every row.
 //
 // Split weights.  P V on the tensor cores applies P rounded to bf16, i.e.
 // each weight with a relative error of up to 2^-8, which moves O by up to
@@ -192,11 +193,10 @@ __device__ __forceinline__ void issue_pv(MmaState<D>& st, uint32_t tmem, uint32_
     mma_ts(tmem + kColO, pcol + 8u * (uint32_t)kk, vd + (uint64_t)(kk * (2048 >> 4)), kIdescPV,
            (accumulate || kk > 0) ? 1u : 0u);
   if (split) {
-    const uint32_t lcol = tmem + kColS + 128u * (st.pg & 1u);
+    const uint32_t lcol = tmem + kColP + 64u * ((st.pg & 1u) ^ 1u);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-      mma_ts(tmem + kColO, lcol + 64u * (uint32_t)(kk >> 2) + 8u * (uint32_t)(kk & 3),
-             vd + (uint64_t)(kk * (2048 >> 4)), kIdescPV, 1u);
+      mma_ts(tmem + kColO, lcol + 8u * (uint32_t)kk, vd + (uint64_t)(kk * (2048 >> 4)), kIdescPV, 1u);
   }
 }
 
@@ -264,14 +264,7 @@ __device__ __noinline__ void pv_issuer_role(const FwdParams& p, const uint8_t* s
       tc_fence_after();
       issue_pv<D>(st, tmem, stage, j > 0, m.split);
       mma_commit(sm.bar(C::kBarVEmpty + (int)stage));
-      mma_commit(sm.bar(C::kBarPFree + b));
-      if (m.split) {
-        // The S buffer held this slot's low-order terms: release it for the
-        // next S once they are read, with as many arrivals as the softmax
-        // warps give it otherwise.
-#pragma unroll
-        for (int w8 = 0; w8 < 8; ++w8) mma_commit(sm.bar(C::kBarSFree + b));
-      }
+      mma_commit(sm.bar(C::kBarPFree + b));  // also frees the other buffer's low-order terms
       if (j == n - 1) mma_commit(sm.bar(C::kBarOFull));
       ++st.vc;
       ++st.pg;
@@ -309,6 +302,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   const uint64_t sl2x2 = f2_make(sl2, sl2);
   float* xbuf = reinterpret_cast<float*>(smem + C::kOffX);
   uint32_t sg = 0, rows = 0, xc = 0, q_it = 0;
+  bool lo_prev = false;  // the last row with slots applied split weights
   uint32_t bits = 0xffffffffu;  // this row's sub-mask bits for the current slot
   // Element mask (causal / key lengths): key position of the first key of each
   // of this thread's two 32-key chunks of the current slot (-1: padding), the
@@ -546,39 +540,52 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       tc_fence_after();
       uint32_t v[64];
       load_s(tmem + tl + kColS + 128u * (uint32_t)b, v);
-      if constexpr (!kSplit) {
-        // The scores are in registers: hand the S buffer back for the next S.
-        // (Split weights keep their low-order terms there; the slot's P V
-        // hands it back.)
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sm.bar(C::kBarSFree + b));
-      }
+      // The scores are in registers: hand the S buffer back for the next S.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.bar(C::kBarSFree + b));
       uint32_t pk[32];
+      uint32_t lo[kSplit ? 32 : 1];
       float sum, sum_w, factor = 1.f;
       const uint32_t pcol = tmem + tl + kColP + 64u * (uint32_t)b + 32u * (uint32_t)h;
-      // Weights against reference `mr` into pk (and, split, the low-order
-      // terms straight into this thread's own S columns).
+      // Split weights: the low-order terms go to the same columns of the
+      // other P buffer (the slot's P V reads both).
+      const uint32_t lcol = tmem + tl + kColP + 64u * (uint32_t)(b ^ 1) + 32u * (uint32_t)h;
+      // Weights against reference `mr` into pk (and, split, lo).
       auto exps = [&](float mr) -> float {
         if constexpr (kSplit) {
-          uint32_t lo[32];
           const float t = exp_pack_split(v, pk, lo, mr);
           sum_w = t;
-          tmem_st32(tmem + tl + kColS + 128u * (uint32_t)b + 64u * (uint32_t)h, lo);
           return t;
         } else {
           return exp_pack(v, pk, mr, &sum_w);
         }
       };
+      // Until the P V of slot g has finished (both threads of a row ask
+      // together, so the warp waits together).
+      auto wait_pv = [&](uint32_t g) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + (int)(g & 1u)), (g >> 1) & 1u, wd,
+                                                 kSitePFull));
+      };
+      // P buffer b was last read by the P V of slot sg - 2.  With split
+      // weights the other buffer, where this slot writes its low-order terms,
+      // is read by the P V of slot sg - 1: wait for that one too.
+      auto store_p = [&]() -> bool {
+        if (u > 0 && !wait_pv(sg - 2)) return false;
+        if constexpr (kSplit) {
+          if (sg > 0 && !wait_pv(sg - 1)) return false;
+        }
+        tmem_st32(pcol, pk);
+        if constexpr (kSplit) tmem_st32(lcol, lo);
+        return true;
+      };
       if constexpr (!kExact) {
         has_keys |= live;  // (set by load_s)
         sum = exps(m_ref);
-        // P buffer b was last read by the P V of slot g - 2.
-        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
+        if (!store_p()) {
           ok = false;
           break;
         }
-        tmem_st32(pcol, pk);
       } else if (m_ref == -INFINITY) {
         // No reference yet in this row: the whole-row maximum first (both
         // threads of a row get the same value and so the same reference).
@@ -599,21 +606,19 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         }
         m_ref = fmaxf(mx, mo) * sl2;  // stays -inf while every key so far is masked
         sum = exps(m_ref);
-        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
+        if (!store_p()) {
           ok = false;
           break;
         }
-        tmem_st32(pcol, pk);
       } else {
         // Exponentials against the current reference right away; whether a
         // rescale is due is settled while P is being written.
         sum = exps(m_ref);
         post(sum_w);
-        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + b), (u - 1) & 1u, wd, kSitePFull))) {
+        if (!store_p()) {
           ok = false;
           break;
         }
-        tmem_st32(pcol, pk);
         float sw_other = 0.f;
         if (!collect(sw_other)) {
           ok = false;
@@ -656,6 +661,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
             tc_fence_after();
             tmem_wait_st();
             tmem_st32(pcol, pk);
+            if constexpr (kSplit) tmem_st32(lcol, lo);
             const uint32_t o_addr = tmem + tl + kColO + (uint32_t)(h * (D / 2));
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
@@ -678,6 +684,14 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       ++sg;
     }
     };
+    // After a row with split weights, the low-order terms of its last slot
+    // sit in the P buffer this row's first slot writes: wait for the P V
+    // that reads them (once per such row, outside the slot loop).
+    if (lo_prev && sg > 0 &&
+        !__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarPFree + (int)((sg - 1) & 1u)), ((sg - 1) >> 1) & 1u,
+                                           wd, kSitePFull)))
+      break;
+    lo_prev = m.split;
     if (m.split) slot_loop(std::true_type{});
     else slot_loop(std::false_type{});
     if (!ok) break;
@@ -752,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
       mbar_init(sm.bar(C::kBarQFull + i), 1);
       mbar_init(sm.bar(C::kBarQEmpty + i), 1 + 8);  // S issuer commit + softmax warps
       mbar_init(sm.bar(C::kBarSFull + i), 1);
-      // one arrival per softmax warp, or (split weights) 8 P V commits
+      // one arrival per softmax warp
       mbar_init(sm.bar(C::kBarSFree + i), 8);
       mbar_init(sm.bar(C::kBarPFull + i), 8);  // one arrival per softmax warp
       mbar_init(sm.bar(C::kBarPFree + i), 1);
