@@ -381,15 +381,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// acc_lo += low bf16 of w, acc_hi += high bf16 of w (each widened exactly to
-// fp32, then a round-to-nearest fp32 add).
-__device__ __forceinline__ void add_bf16x2_f32(float& acc_lo, float& acc_hi, uint32_t w) {
-  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
-      : "+f"(acc_lo), "+f"(acc_hi)
-      : "r"(w));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   // cvt packs its first source into the upper half.

@@ -384,16 +384,15 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     }
   };
   // p = 2^(s*scale*log2e - m) as bf16 pairs into pk (keys 2e, 2e+1 -> pk[e]).
-  // Returns the sum of the 64 values of p; *sum_w gets the sum of the same
-  // values as rounded to bf16, i.e. of the weights the P V product applies
-  // (O is divided by that sum, so exactly those weights are normalised; the
-  // log-sum-exp uses the exact one).  Chunks dropped from `chunks` get +0
-  // weights without exponentials (adding +0 leaves the sums as they are).
-  auto exp_pack = [&](const uint32_t (&v)[64], uint32_t (&pk)[32], float m, float* sum_w) -> float {
+  // Returns the fp32 sum of the 64 values of p, which both the log-sum-exp
+  // and the normalisation of O use (the bf16 weights the P V product applies
+  // differ from p by at most 2^-8 relatively, in unbiased round-to-nearest
+  // steps).  Chunks dropped from `chunks` get +0 weights without
+  // exponentials (adding +0 leaves the sum as it is).
+  auto exp_pack = [&](const uint32_t (&v)[64], uint32_t (&pk)[32], float m) -> float {
     const float mb = (m == -INFINITY) ? 0.f : m;
     const uint64_t nmbx2 = f2_make(-mb, -mb);
     uint64_t acc2[2] = {0ull, 0ull};
-    float accw[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       if (chunks & (1u << c)) {
@@ -405,14 +404,12 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
           const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           pk[e] = pack_bf16x2(p0, p1);
           acc2[e & 1] = fadd2(acc2[e & 1], f2_make(p0, p1));
-          add_bf16x2_f32(accw[2 * (e & 1)], accw[2 * (e & 1) + 1], pk[e]);
         }
       } else {
 #pragma unroll
         for (int e = 16 * c; e < 16 * c + 16; ++e) pk[e] = 0u;
       }
     }
-    *sum_w = (accw[0] + accw[1]) + (accw[2] + accw[3]);
     float s0, s1, s2, s3;
     f2_split(acc2[0], s0, s1);
     f2_split(acc2[1], s2, s3);
@@ -420,7 +417,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   };
   // Split weights: pk gets hi = bf16(p), lo gets bf16(p - hi) (p - hi is
   // exact in fp32: hi is within a factor of two of p).  The weights applied,
-  // hi + lo, are within 2^-16 of p, so the fp32 sum of p normalises them.
+  // hi + lo, are within 2^-16 of p; the fp32 sum of p normalises them.
   auto exp_pack_split = [&](const uint32_t (&v)[64], uint32_t (&pk)[32], uint32_t (&lo)[32],
                             float m) -> float {
     const float mb = (m == -INFINITY) ? 0.f : m;
@@ -460,8 +457,6 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     f2_split(acc2[1], s2, s3);
     return (s0 + s1) + (s2 + s3);
   };
-  // The slot's weights of this thread as bf16 pairs into its P columns (and,
-  // split, the low-order terms 32 columns on); sum_w as exp_pack.
   for (uint32_t t = 0;; ++t) {
     const Item m = sched_take<Cfg<D>>(sm, smem, t, lane == 0, true, wd);
     if (m.it < 0) break;
@@ -514,7 +509,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       lim_warp = min(p.causal ? qmin + p.causal_off : 0x7fffffff, kvl - 1);
       lim_warp_hi = min(p.causal ? qmin + 31 + p.causal_off : 0x7fffffff, kvl - 1);
     }
-    float l_run = 0.f, lw_run = 0.f;  // exact and applied-weight row sums
+    float l_run = 0.f;                // the row sum of p (this thread's keys)
     bool has_keys = false;            // (bounded pass) some key of this thread's columns is kept
     bool ok = true;
     // The slot loop, instantiated per kind of row (split weights or not): a
@@ -546,20 +541,15 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       if (lane == 0) mbar_arrive(sm.bar(C::kBarSFree + b));
       uint32_t pk[32];
       uint32_t lo[kSplit ? 32 : 1];
-      float sum, sum_w, factor = 1.f;
+      float sum, factor = 1.f;
       const uint32_t pcol = tmem + tl + kColP + 64u * (uint32_t)b + 32u * (uint32_t)h;
       // Split weights: the low-order terms go to the same columns of the
       // other P buffer (the slot's P V reads both).
       const uint32_t lcol = tmem + tl + kColP + 64u * (uint32_t)(b ^ 1) + 32u * (uint32_t)h;
-      // Weights against reference `mr` into pk (and, split, lo).
+      // Weights against reference `mr` into pk (and, split, lo); their sum.
       auto exps = [&](float mr) -> float {
-        if constexpr (kSplit) {
-          const float t = exp_pack_split(v, pk, lo, mr);
-          sum_w = t;
-          return t;
-        } else {
-          return exp_pack(v, pk, mr, &sum_w);
-        }
+        if constexpr (kSplit) return exp_pack_split(v, pk, lo, mr);
+        else return exp_pack(v, pk, mr);
       };
       // Until the P V of slot g has finished (both threads of a row ask
       // together, so the warp waits together).
@@ -614,7 +604,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         // Exponentials against the current reference right away; whether a
         // rescale is due is settled while P is being written.
         sum = exps(m_ref);
-        post(sum_w);
+        post(sum);
         if (!store_p()) {
           ok = false;
           break;
@@ -626,7 +616,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         }
         // Both threads of a row see the same two sums, and the two warps of a
         // lane quadrant hold the same rows: they take this branch together.
-        if (__any_sync(0xffffffffu, sum_w > kRescaleSumBound || sw_other > kRescaleSumBound)) {
+        if (__any_sync(0xffffffffu, sum > kRescaleSumBound || sw_other > kRescaleSumBound)) {
           float mx4[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) mx4[c] = fmaxf(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1]));
@@ -677,7 +667,6 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       }
       tmem_wait_st();
       l_run = l_run * factor + sum;
-      lw_run = lw_run * factor + sum_w;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sm.bar(C::kBarPFull + b));  // one arrival per warp
@@ -698,19 +687,18 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     // ------------------------------------------------------------ epilogue
     if (!__all_sync(0xffffffffu, mbar_wait(sm.bar(C::kBarOFull), rows & 1u, wd, kSiteODone))) break;
     tc_fence_after();
-    float l_other = 0.f, lw_other = 0.f;
+    float l_other = 0.f;
     if (!exchange(l_run, l_other)) break;
-    if (!exchange(lw_run, lw_other)) break;
-    const float L = l_run + l_other, Lw = lw_run + lw_other;
-    const float inv = (Lw > 0.f) ? 1.f / Lw : 0.f;
+    const float L = l_run + l_other;
+    const float inv = (L > 0.f) ? 1.f / L : 0.f;
     if constexpr (!kExact) {
       // Whether the row keeps any key: without an element mask both threads
       // see the same sub-mask bits; with one, they combine their columns.
       float hk_other = has_keys ? 1.f : 0.f;
       if (kGeneral && p.elem_mask && !exchange(has_keys ? 1.f : 0.f, hk_other)) break;
       const bool row_keys = has_keys || hk_other > 0.f;
-      // Both threads of a row compute the same Lw and row_keys.
-      const bool need = row_keys && !(Lw >= kFallbackPerKey * (float)(m.n * 128));
+      // Both threads of a row compute the same L and row_keys.
+      const bool need = row_keys && !(L >= kFallbackPerKey * (float)(m.n * 128));
       if (__any_sync(0xffffffffu, need) && lane == 0) {
         if (atomicExch(p.fb_flag + m.row, 1) == 0)
           p.fb_list[atomicAdd(p.control + kCtlFallbackCount, 1)] = m.row;

@@ -107,7 +107,7 @@ struct QCfg {
   static constexpr int kOffSched = kOffMisc + 16;           // int [kSchedSlots][8] work items
   static constexpr int kOffM = kOffSched + 32 * kSchedSlots;  // float [64] reference per query
   static constexpr int kOffRed = kOffM + 64 * 4;            // float [4 quads][64] partials
-  static constexpr int kOffInv = kOffRed + 4 * 64 * 4;      // float [64] 1 / weight sum
+  static constexpr int kOffInv = kOffRed + 4 * 64 * 4;      // float [64] 1 / row sum
   static constexpr int kOffFlag = kOffInv + 64 * 4;         // int [2 halves][4 quads]
   static constexpr int kSmemBytes = kOffFlag + 8 * 4;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -336,8 +336,7 @@ __device__ __forceinline__ void q64_softmax(const FwdParams& p, uint8_t* smem, c
     // One sweep over the row's slots.  kMaxOnly: the exact pass's first
     // sweep, each query's largest score into mx; otherwise the weights
     // against the references nm2 (negated, pairs) into P^T, with the sums.
-    auto sweep = [&](auto max_only, float (&mx)[32], const uint64_t (&nm2)[16], uint64_t (&acc_e)[16],
-                     float (&acc_w)[32]) {
+    auto sweep = [&](auto max_only, float (&mx)[32], const uint64_t (&nm2)[16], uint64_t (&acc_e)[16]) {
       constexpr bool kMaxOnly = decltype(max_only)::value;
       uint32_t wnext = submask ? __ldg(p.slot_mask + m.s0) : 0u;
       for (int j = 0; j < m.n; ++j) {
@@ -385,8 +384,6 @@ __device__ __forceinline__ void q64_softmax(const FwdParams& p, uint8_t* smem, c
                                f2_make(-1.f, -1.f), p2),
                          r0, r1);
                 lo[e] = pack_bf16x2(r0, r1);
-              } else {
-                add_bf16x2_f32(acc_w[2 * e], acc_w[2 * e + 1], pk[e]);
               }
             }
           } else {
@@ -424,17 +421,13 @@ __device__ __forceinline__ void q64_softmax(const FwdParams& p, uint8_t* smem, c
     float mx[32];
     uint64_t nm2[16];
     uint64_t acc_e[16];
-    float acc_w[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      mx[i] = -INFINITY;
-      acc_w[i] = 0.f;
-    }
+    for (int i = 0; i < 32; ++i) mx[i] = -INFINITY;
 #pragma unroll
     for (int e = 0; e < 16; ++e) acc_e[e] = 0ull;
     if constexpr (kExact) {
       // First sweep: each query's largest score over the row's selected keys.
-      sweep(std::true_type{}, mx, nm2, acc_e, acc_w);
+      sweep(std::true_type{}, mx, nm2, acc_e);
       if (!ok) break;
       red_s[quad * 64 + 32 * h + lane] = xpose_reduce<true>(mx, lane);
       if (!sm_sync()) break;
@@ -454,7 +447,7 @@ __device__ __forceinline__ void q64_softmax(const FwdParams& p, uint8_t* smem, c
       b = (b == -INFINITY) ? 0.f : b;
       nm2[e] = f2_make(-a, -b);
     }
-    sweep(std::false_type{}, mx, nm2, acc_e, acc_w);
+    sweep(std::false_type{}, mx, nm2, acc_e);
     if (!ok) break;
 
     // ------------------------------------------------------------ epilogue
@@ -464,32 +457,23 @@ __device__ __forceinline__ void q64_softmax(const FwdParams& p, uint8_t* smem, c
 #pragma unroll
     for (int e = 0; e < 16; ++e) f2_split(acc_e[e], ce[2 * e], ce[2 * e + 1]);
     const float se = xpose_reduce<false>(ce, lane);
-    float sw = se;
-    if constexpr (!kExact) sw = xpose_reduce<false>(acc_w, lane);
     if (lane == 0) flag_s[h * 4 + quad] = kept ? 1 : 0;
     red_s[quad * 64 + 32 * h + lane] = se;
     if (!sm_sync()) break;
-    float L = 0.f;
     if (quad == 0) {
+      // The fp32 sum of p normalises O as well as giving the log-sum-exp.
       const int q = 32 * h + lane;
-      L = red_s[q] + red_s[64 + q] + red_s[128 + q] + red_s[192 + q];
-    }
-    if (!sm_sync()) break;
-    red_s[quad * 64 + 32 * h + lane] = sw;
-    if (!sm_sync()) break;
-    if (quad == 0) {
-      const int q = 32 * h + lane;
-      const float Lw = red_s[q] + red_s[64 + q] + red_s[128 + q] + red_s[192 + q];
+      const float L = red_s[q] + red_s[64 + q] + red_s[128 + q] + red_s[192 + q];
       const bool keys = flag_s[h * 4] | flag_s[h * 4 + 1] | flag_s[h * 4 + 2] | flag_s[h * 4 + 3];
       if constexpr (!kExact) {
         // weights underflowed although the query has selected keys
-        const bool need = keys && !(Lw >= kFallbackPerKey * (float)(m.n * 128));
+        const bool need = keys && !(L >= kFallbackPerKey * (float)(m.n * 128));
         if (__any_sync(0xffffffffu, need) && lane == 0) {
           if (atomicExch(p.fb_flag + m.row, 1) == 0)
             p.fb_list[atomicAdd(p.control + kCtlFallbackCount, 1)] = m.row;
         }
       }
-      inv_s[q] = (Lw > 0.f) ? 1.f / Lw : 0.f;
+      inv_s[q] = (L > 0.f) ? 1.f / L : 0.f;
       p.LSE[orow(q)] = (L > 0.f) ? (m_s[q] + __log2f(L)) * 0.69314718055994531f : -INFINITY;
     }
     if (!sm_sync()) break;  // inv_s
