@@ -209,6 +209,7 @@ bsa_status make_fwd_params(const bsa_plan_layout& L, const PlanDev& pd, uint8_t*
   fp.order = pd.order;
   fp.control = pd.control;
   fp.O = static_cast<uint16_t*>(O);
+  fp.o_v8 = (reinterpret_cast<uintptr_t>(O) & 31u) == 0 ? 1 : 0;
   fp.LSE = LSE;
   fp.K = static_cast<const uint16_t*>(K);
   fp.V = static_cast<const uint16_t*>(V);

@@ -714,9 +714,19 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
 #pragma unroll
       for (int e = 0; e < 16; ++e)
         pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv);
+      if (p.o_v8) {  // whole 32-byte sectors: half the store instructions
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
-        optr[c * 4 + q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+        for (int q8 = 0; q8 < 2; ++q8) {
+          uint32_t w8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) w8[e] = pk[8 * q8 + e];
+          st_global_v8(optr + c * 4 + 2 * q8, w8);
+        }
+      } else {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          optr[c * 4 + q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+      }
     }
     // O has been read: the next row's first P V may overwrite it.
     tc_fence_before();

@@ -143,6 +143,7 @@ struct FwdParams {
   int32_t* control;
   uint16_t* O;       // bf16 bits
   float* LSE;
+  int o_v8;          // O is 32-byte aligned: rows are written with 32-byte stores
   const uint16_t* K;     // bf16 bits, [B*Hkv*Nk, d] (read by the key-norm pass)
   const uint16_t* V;     // bf16 bits, same view as K (read by the key-norm pass)
   float* kmax;           // largest key norm per K unit

@@ -110,6 +110,23 @@ def test_forward_bounded_pass_queues_nothing_on_workloads(bsa, name):
     assert int(p.control()[FALLBACK_COUNT].item()) == 0
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_forward_output_16_byte_aligned(bsa, d):
+    """An O whose base is 16- but not 32-byte aligned (the alignment the C ABI
+    asks for) is written with 16-byte stores instead of 32-byte ones: the same
+    values, bit for bit."""
+    w = W.random_problem(13 + d, 1, 2, 2, 512, 768, d, 128, 128, 0.5)
+    p = bsa.plan(w.mask.cuda(), w.bq, w.bk, 1)
+    q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    o1, l1 = bsa.forward(p, q, k, v)
+    buf = torch.empty(o1.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    o2 = buf[8:].view(o1.shape)
+    assert o1.data_ptr() % 32 == 0 and o2.data_ptr() % 32 == 16
+    _, l2 = bsa.forward(p, q, k, v, out=o2)
+    assert bsa.sync_status(p)[0] == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 def test_forward_repeat_and_plan_reuse(bsa):
     w = W.make_workload("video_dit_small")
     p = bsa.plan(w.mask.cuda(), w.bq, w.bk, 1)
