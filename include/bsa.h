@@ -272,8 +272,10 @@ bsa_status bsa_plan_export(const bsa_plan* plan, void* stream, bsa_plan_arrays* 
  * Q: device bf16 [B][Hq][Nq][d]; K, V: device bf16 [B][Hkv][Nk][d];
  * O: device bf16 [B][Hq][Nq][d] (written); LSE: device fp32 [B][Hq][Nq]
  * (written; natural log, -inf for rows with no selected key).  All 16-byte
- * aligned; Q/K/V/O must not alias.  d in {64, 128}.  scale <= 0 selects
- * 1/sqrt(d).  Nq, Nk, Hkv and the block sizes come from the plan.
+ * aligned (an O that is also 32-byte aligned is written with 32-byte stores,
+ * a little faster; the values are the same); Q/K/V/O must not alias.
+ * d in {64, 128}.  scale <= 0 selects 1/sqrt(d).  Nq, Nk, Hkv and the block
+ * sizes come from the plan.
  * Enqueues one memset of the plan's control words and four kernels on
  * `stream`: the key-norm and row-bound passes, the forward pass over every
  * plan row, and an exact second pass over the rows the first one queued (it
