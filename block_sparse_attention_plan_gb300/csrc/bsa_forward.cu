@@ -284,7 +284,7 @@ __device__ __noinline__ void pv_issuer_role(const FwdParams& p, const uint8_t* s
 // was far above its scores) is queued for the exact pass.
 // Exact pass (kExact = true): the running row maximum, agreed between the
 // two threads of a row, with a lazy rescale of O.
-template <int D, bool kExact, bool kGeneral>
+template <int D, bool kExact, bool kElem>
 __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, const Smem<Cfg<D>>& sm,
                                              uint32_t tmem, const Watchdog& wd) {
   using C = Cfg<D>;
@@ -360,7 +360,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       }
     }
     live = !submask || bits != 0u;  // the row keeps a key of this slot (block level)
-    if constexpr (kGeneral) {
+    if constexpr (kElem) {
       if (p.elem_mask) {
         live = false;
 #pragma unroll
@@ -502,7 +502,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     __syncwarp();
     if (lane == 0) mbar_arrive(sm.bar(C::kBarQEmpty + qb));
     ++q_it;
-    if (kGeneral && p.elem_mask) {
+    if (kElem && p.elem_mask) {
       const int qmin = qpos - lane;  // the warp's 32 rows lie in one q-unit (qu >= 32)
       const int kvl = p.kv_lens ? __ldg(p.kv_lens + m.bh / p.H) : 0x7fffffff;
       lim_row = min(p.causal ? qpos + p.causal_off : 0x7fffffff, kvl - 1);
@@ -520,7 +520,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       const int b = (int)(sg & 1u);
       const uint32_t u = sg >> 1;
       if (submask) bits = (__ldg(p.slot_mask + m.s0 + j) >> (qi * p.rk)) & my_bits_mask;
-      if (kGeneral && p.elem_mask) {
+      if (kElem && p.elem_mask) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int col0 = 64 * h + 32 * c;  // ku = 32 << ku_shift
@@ -695,7 +695,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       // Whether the row keeps any key: without an element mask both threads
       // see the same sub-mask bits; with one, they combine their columns.
       float hk_other = has_keys ? 1.f : 0.f;
-      if (kGeneral && p.elem_mask && !exchange(has_keys ? 1.f : 0.f, hk_other)) break;
+      if (kElem && p.elem_mask && !exchange(has_keys ? 1.f : 0.f, hk_other)) break;
       const bool row_keys = has_keys || hk_other > 0.f;
       // Both threads of a row compute the same L and row_keys.
       const bool need = row_keys && !(L >= kFallbackPerKey * (float)(m.n * 128));
@@ -737,15 +737,19 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   }
 }
 
-// kGeneral: paged K/V and/or element masks (runtime-selected inside); the
-// plain instantiation carries none of that code.  kMulti: slots of several
-// K/V units (p.rk > 1), gathered by whole producer warps; a separate
-// instantiation, so that the kernels of one-unit slots keep the
-// single-thread producers alone (about 1 % faster than with both forms in
+// kMode: 0 plain; 1 paged K/V (the producers read pool rows, the softmax is
+// the plain one); 2 element masks (causal / key lengths), with or without
+// pages (runtime-selected inside).  The softmax's element-mask code alone
+// costs 3.5-10 % where no mask is set, so only mode 2 carries it.
+// kMulti: slots of several K/V units (p.rk > 1), gathered by whole producer
+// warps; a separate instantiation, so that the kernels of one-unit slots keep
+// the single-thread producers alone (about 1 % faster than with both forms in
 // one binary).
-template <int D, bool kExact, bool kGeneral, bool kMulti>
+template <int D, bool kExact, int kMode, bool kMulti>
 __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
+  constexpr bool kPaged = kMode != 0;  // producers: keys may be pool rows
+  constexpr bool kElem = kMode == 2;   // softmax: element masks
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -799,19 +803,19 @@ __global__ void __launch_bounds__(kThreads, 1) bsa_fwd_kernel(const __grid_const
 
   if (warp >= 4) {
     regs_inc<kRegsSoftmax>();
-    softmax_role<D, kExact, kGeneral>(p, smem, sm, tmem, wd);
+    softmax_role<D, kExact, kElem>(p, smem, sm, tmem, wd);
   } else {
     regs_dec<kRegsControl>();
     if (kMulti && (warp == 0 || warp == 3)) {
       // Slots of several units: the producers run on their whole warp (lane
       // u issues the copies of a slot's unit u).
       if (__shfl_sync(0xffffffffu, *abort_flag == 0 ? 1 : 0, 0))
-        producer_role_warp<Cfg<D>, kGeneral>(p, smem, sm, wd, warp == 0);
+        producer_role_warp<Cfg<D>, kPaged>(p, smem, sm, wd, warp == 0);
     } else if (lane == 0 && !*abort_flag) {
-      if (!kMulti && warp == 0) producer_role<Cfg<D>, kGeneral>(p, smem, sm, wd, true);
+      if (!kMulti && warp == 0) producer_role<Cfg<D>, kPaged>(p, smem, sm, wd, true);
       else if (warp == 1) s_issuer_role<D>(p, smem, sm, tmem, wd);
       else if (warp == 2) pv_issuer_role<D>(p, smem, sm, tmem, wd);
-      else if (!kMulti && warp == 3) producer_role<Cfg<D>, kGeneral>(p, smem, sm, wd, false);
+      else if (!kMulti && warp == 3) producer_role<Cfg<D>, kPaged>(p, smem, sm, wd, false);
     }
   }
 
@@ -837,25 +841,30 @@ __global__ void watchdog_selftest_kernel(int32_t* status, long long limit_ns) {
   if (mbar_wait(bar, 0, wd, kSiteSelftest)) status[3] = 1;
 }
 
-template <int D, bool kExact, bool kGeneral, bool kMulti>
+template <int D, bool kExact, int kMode, bool kMulti>
 cudaError_t launch_dm(const FwdParams& p, int grid, cudaStream_t stream) {
   const int smem = Cfg<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(bsa_fwd_kernel<D, kExact, kGeneral, kMulti>,
+  cudaError_t e = cudaFuncSetAttribute(bsa_fwd_kernel<D, kExact, kMode, kMulti>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  bsa_fwd_kernel<D, kExact, kGeneral, kMulti><<<grid, kThreads, smem, stream>>>(p);
+  bsa_fwd_kernel<D, kExact, kMode, kMulti><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
-template <int D, bool kExact, bool kGeneral>
+template <int D, bool kExact, int kMode>
+cudaError_t launch_dk(const FwdParams& p, int grid, cudaStream_t stream) {
+  return p.rk > 1 ? launch_dm<D, kExact, kMode, true>(p, grid, stream)
+                  : launch_dm<D, kExact, kMode, false>(p, grid, stream);
+}
+template <int D, bool kExact>
 cudaError_t launch_d(const FwdParams& p, int grid, cudaStream_t stream) {
-  return p.rk > 1 ? launch_dm<D, kExact, kGeneral, true>(p, grid, stream)
-                  : launch_dm<D, kExact, kGeneral, false>(p, grid, stream);
+  if (p.elem_mask) return launch_dk<D, kExact, 2>(p, grid, stream);
+  if (p.block_table != nullptr) return launch_dk<D, kExact, 1>(p, grid, stream);
+  return launch_dk<D, kExact, 0>(p, grid, stream);
 }
 
 template <int D>
 cudaError_t launch_passes(const FwdParams& p, int grid, cudaStream_t stream, int stages) {
   cudaError_t e = cudaSuccess;
-  const bool general = p.block_table != nullptr || p.elem_mask;
   // Key-norm and row-bound passes (bsa_prep.cu).
   e = launch_prep(p, D, stages, stream);
   if (e != cudaSuccess) return e;
@@ -867,7 +876,7 @@ cudaError_t launch_passes(const FwdParams& p, int grid, cudaStream_t stream, int
     a.work_counter = p.control + kCtlWorkCounter;
     a.work_count = nullptr;
     e = q64 ? launch_forward_q64(a, D, grid, stream, false)
-            : general ? launch_d<D, false, true>(a, grid, stream) : launch_d<D, false, false>(a, grid, stream);
+            : launch_d<D, false>(a, grid, stream);
     if (e != cudaSuccess) return e;
   }
   if (stages & BSA_STAGE_EXACT) {
@@ -877,7 +886,7 @@ cudaError_t launch_passes(const FwdParams& p, int grid, cudaStream_t stream, int
     x.work_counter = p.control + kCtlFallbackWork;
     x.work_count = p.control + kCtlFallbackCount;
     e = q64 ? launch_forward_q64(x, D, grid, stream, true)
-            : general ? launch_d<D, true, true>(x, grid, stream) : launch_d<D, true, false>(x, grid, stream);
+            : launch_d<D, true>(x, grid, stream);
   }
   return e;
 }
