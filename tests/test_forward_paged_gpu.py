@@ -16,6 +16,8 @@ from compare import assert_attention_close
 
 pytestmark = pytest.mark.gpu
 
+FALLBACK_COUNT = 3  # control word: rows the bounded pass queued for the exact pass
+
 
 def make_pool(k, v, page_size, seed, extra_pages=3, kv_lens=None):
     """Scatter contiguous K/V [B, Hkv, Nk, d] into shuffled pages of pools
@@ -41,6 +43,28 @@ def make_pool(k, v, page_size, seed, extra_pages=3, kv_lens=None):
             k_pool[phys, :, :hi - lo] = k[b, :, lo:hi]
             v_pool[phys, :, :hi - lo] = v[b, :, lo:hi]
     return k_pool.cuda(), v_pool.cuda(), table.cuda()
+
+
+def test_paged_rows_taking_the_exact_pass(bsa):
+    """Rows whose bound is far above their scores go to the exact pass; with
+    paged K/V (no element mask) both passes run the paged kernels and give
+    the contiguous result bit for bit, and the oracle's within tolerance."""
+    w = W.random_problem(21, 1, 4, 2, 512, 1024, 128, 128, 128, 0.7)
+    q, k = w.q.float(), w.k.float()
+    q[:, :2, :, 0] = 150.0
+    k[:, :1, :, 1] = 150.0
+    w.q, w.k = q.to(torch.bfloat16), k.to(torch.bfloat16)
+    p = bsa.plan(w.mask.cuda(), w.bq, w.bk, w.gqa_group)
+    qd = w.q.cuda()
+    o1, l1 = bsa.forward(p, qd, w.k.cuda(), w.v.cuda())
+    kp, vp, table = make_pool(w.k, w.v, 128, seed=5)
+    o2, l2 = bsa.forward(p, qd, kp, vp, block_table=table)
+    st, det = bsa.sync_status(p)
+    assert st == 0, (st, hex(det))
+    assert int(p.control()[FALLBACK_COUNT].item()) > 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    O, L = OA.block_gather(w.q, w.k, w.v, w.mask, 128, 128)
+    assert_attention_close(o2, l2, O, L, "paged, exact pass")
 
 
 @pytest.mark.parametrize("name,page_mult", [("video_dit_small", 1), ("video_dit_small", 2),
